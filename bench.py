@@ -1,0 +1,357 @@
+#!/usr/bin/env python
+"""Throughput of one MoE layer, forward + backward, on GB300.
+
+One step = the whole hot path over one batch of synthetic tokens: router,
+deterministic dispatch, grouped-GEMM SwiGLU experts, fixed-order combine,
+and the backward (input and weight gradients).  The workload is the
+DeepSeek-V2-Lite-like layer (T=8192 tokens, d=2048, f=1408, 64 routed
+experts top-6, 2 shared experts); its weights (1.15 GB) and activations are
+far larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica on its own batch
+(weak scaling, no collective on the data path); the barrier-bracketed time
+is the max over ranks and `value` counts the tokens of all ranks.
+`--impl reference` times the CPU fp64 oracle on the host cores instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s (fwd+bwd, 1xGB300)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv2lite_T8192_d2048_f1408_E64_k6_S2")
+    ap.add_argument("--megakernel", type=int, default=-1, help="1: forward MegaKernel, 0: kernel chain, "
+                    "-1: MegaKernel when the library provides it")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller captures for profiling)")
+    return ap.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, k)
+                elif isinstance(o, (int, float)):
+                    flat[pre] = float(o)
+            walk(d)
+            if "bf16_tflops" in flat or "hbm_gbs" in flat:
+                return flat, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_index)], stdout=self.tmp,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = [l.strip().split(", ") for l in open(self.tmp.name) if l.strip()]
+        os.unlink(self.tmp.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm)}
+
+
+def workload_cfg(name, tokens=0):
+    from combine_fp32_softmax_gb300.configs import BY_NAME
+    cfg = BY_NAME[name]
+    if tokens:
+        cfg = cfg.with_(T=tokens, name=cfg.name.replace(f"T{cfg.T}_", f"T{tokens}_"))
+    return cfg
+
+
+def gemm_flops_per_launch(cfg):
+    """Algorithmic flops of one launch of each grouped GEMM (2 flops per
+    multiply-add; every routed and shared row, no padding)."""
+    dfr = 2 * cfg.d * cfg.f * cfg.Rs
+    return {"gemm1_swiglu": 2 * dfr, "gemm2_scale": dfr, "gemm_dh": dfr, "gemm_dx": 2 * dfr,
+            "gemm_dw13": 2 * dfr, "gemm_dw2": dfr}
+
+
+def traffic_from_profiles(kernel, workload):
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, or None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.strip().startswith("traffic_bytes_per_launch:"):
+            try:
+                return float(line.split(":", 1)[1].strip().split()[0])
+            except ValueError:
+                return None
+    return None
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_step_time(cfg, inp, ntok):
+    """Seconds of the fp64 oracle for forward + backward of the same layer on
+    the first `ntok` tokens (a bounded sample of the batch)."""
+    from oracle import moe_oracle as O
+    x, z, dy = inp.x[:ntok], inp.logits[:ntok], inp.dy[:ntok]
+    t0 = time.perf_counter()
+    fw = O.layer_fwd(x, z, inp.W1, inp.W3, inp.W2, k=cfg.k, S=cfg.S, renorm=cfg.renorm)
+    O.layer_bwd(fw, dy, x, inp.W1, inp.W3, inp.W2, renorm=cfg.renorm)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, inp, ntok, reps=1):
+    times = [oracle_step_time(cfg, inp, ntok) for _ in range(reps)]
+    t = min(times)
+    return {"value": ntok / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of the same layer on the first {ntok} of {cfg.T} tokens "
+                      f"(all experts' weight gradients included), best of {reps}"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    cfg = workload_cfg(args.workload, args.tokens)
+    from combine_fp32_softmax_gb300.inputs import make_layer_inputs
+    inp = make_layer_inputs(cfg, seed=0)
+    ntok = args.cpu_sample_tokens
+    for _ in range(args.warmup):
+        oracle_step_time(cfg, inp, ntok)
+    times = [oracle_step_time(cfg, inp, ntok) for _ in range(args.steps)]
+    total = sum(times)
+    value = ntok * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(cfg, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"each step: fp64 oracle fwd+bwd on the first {ntok} of {cfg.T} tokens"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(cfg, megakernel):
+    return {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E, "k": cfg.k,
+            "n_shared": cfg.S, "renorm": cfg.renorm, "megakernel": megakernel,
+            "l2": "inputs larger than L2 (no flush): weights 1.15 GB + activations per step",
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from combine_fp32_softmax_gb300 import moe
+    from combine_fp32_softmax_gb300.inputs import make_layer_inputs
+
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload_cfg(args.workload, args.tokens)
+    inp = make_layer_inputs(cfg, seed=rank)
+    g = {k: getattr(inp, k).to(dev) for k in ("x", "logits", "W1", "W3", "W2", "dy")}
+    ws = moe.alloc_workspace(cfg, dev)
+    f32 = torch.float32
+    nexp = cfg.E + cfg.S
+    out = dict(y=torch.empty(cfg.T, cfg.d, dtype=f32, device=dev),
+               idx=torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev),
+               w=torch.empty(cfg.T, cfg.k, dtype=f32, device=dev),
+               dx=torch.empty(cfg.T, cfg.d, dtype=f32, device=dev),
+               dz=torch.empty(cfg.T, cfg.E, dtype=f32, device=dev),
+               dW1=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
+               dW3=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
+               dW2=torch.empty(nexp, cfg.d, cfg.f, dtype=f32, device=dev))
+    mk = args.megakernel
+    if mk < 0:  # probe: the MegaKernel is used when the library provides it
+        try:
+            moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
+                              ws, use_megakernel=1)
+            mk = 1
+        except moe.MoeError:
+            mk = 0
+
+    def step(src=g):
+        moe.moe_layer_fwd(cfg, src["logits"], src["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
+                          ws, use_megakernel=mk)
+        moe.moe_layer_bwd(cfg, src["dy"], src["logits"], src["x"], g["W1"], g["W3"], g["W2"], out["idx"], out["w"],
+                          ws, out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], which=3)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    code, info = moe.moe_get_device_error(ws)
+    if code != 0:
+        raise RuntimeError(f"device error {code} ({info}) during warm-up")
+
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local)
+    moe.moe_trace_reset()
+    moe.moe_trace_enable(True)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    moe.moe_trace_enable(False)
+    trace = moe.moe_trace_read()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = cfg.T * world / (ms / 1000.0)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: getattr(inp, k).pin_memory() for k in ("x", "logits", "dy")}
+        src = {k: torch.empty_like(g[k]) for k in ("x", "logits", "dy")}
+        host_out = {k: torch.empty(out[k].shape, dtype=out[k].dtype, pin_memory=True) for k in ("y", "dx", "dz")}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for k in pin:
+                src[k].copy_(pin[k], non_blocking=True)
+            step(src)
+            for k in host_out:
+                host_out[k].copy_(out[k], non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": cfg.T * world / (ems / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    code, info = moe.moe_get_device_error(ws)
+    if code != 0:
+        raise RuntimeError(f"device error {code} ({info}) in the timed region")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (largest share of device time)
+    peaks, peak_src = load_peaks()
+    flops = gemm_flops_per_launch(cfg)
+    total_ms = sum(v[0] for v in trace.values())
+    dom = max(trace, key=lambda k: trace[k][0])
+    dom_ms = trace[dom][0] / trace[dom][1]
+    if dom in flops:
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        achieved = flops[dom] / (dom_ms / 1000.0) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"bf16 sustained, {peak_src}"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                "frac": None, "peak_source": peak_src}
+    roof["traffic"] = traffic_from_profiles(dom, cfg.name)
+    roof["share"] = trace[dom][0] / total_ms
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1], "share": v[0] / total_ms} for k, v in trace.items()}
+    gemm_ms = sum(trace[k][0] for k in flops if k in trace) / args.steps
+    all_gemm_tflops = sum(flops.values()) / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg, mk),
+            "e2e": e2e, "gpu_launches": int(sum(v[1] for v in trace.values())),
+            "roofline": roof, "clocks": clocks,
+            "gemm_tflops_all": all_gemm_tflops, "kernels": kernels}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_sample_tokens)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

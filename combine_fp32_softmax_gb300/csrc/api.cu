@@ -1,0 +1,350 @@
+// C ABI entry points (declared in include/moe.h): argument checks, workspace
+// carving and the launch sequences of the forward and backward passes.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+
+namespace moe {
+int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint16_t* x, const uint16_t* W1,
+                   const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* y, int grid_limit,
+                   cudaStream_t s);
+}
+
+using namespace moe;
+
+namespace {
+
+int g_grid_limit = 0;
+
+int persistent_grid() {
+  const int n = num_sms();
+  return g_grid_limit > 0 ? std::min(g_grid_limit, n) : n;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cfg(const moe_cfg* c) {
+  if (!c) return MOE_ERR_ARG;
+  if (c->T < 1 || c->d_model < 64 || c->d_ff < 64 || c->E < 1 || c->k < 1 || c->n_shared < 0) return MOE_ERR_SHAPE;
+  if (c->E > 256 || c->k > c->E || c->k > 8 || c->n_shared > 4) return MOE_ERR_SHAPE;
+  if (c->d_model % 64 || c->d_ff % 64) return MOE_ERR_SHAPE;
+  if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_SHAPE;
+  if (static_cast<long long>(c->T) * (c->k + c->n_shared) >= (1ll << 31) - 256) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+// Checks required (non-null, 16-byte aligned) and optional (aligned if set)
+// pointers plus the workspace.
+int check_ptrs(std::initializer_list<const void*> req, std::initializer_list<const void*> opt, const void* ws) {
+  for (const void* p : req) {
+    if (!p) return MOE_ERR_ARG;
+    if (!al16(p)) return MOE_ERR_ALIGN;
+  }
+  for (const void* p : opt)
+    if (p && !al16(p)) return MOE_ERR_ALIGN;
+  if (!ws) return MOE_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)             \
+  do {                            \
+    const int _rc = (expr);       \
+    if (_rc != MOE_OK) return _rc; \
+  } while (0)
+#define MOE_TRY_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+GemmArgs base_args(const moe_cfg& c, void* ws, const WsLayout& L) {
+  GemmArgs a{};
+  a.T = c.T;
+  a.d = c.d_model;
+  a.f = c.d_ff;
+  a.E = c.E;
+  a.k = c.k;
+  a.S = c.n_shared;
+  a.err = at<int>(ws, L.err);
+  return a;
+}
+
+// Permutation builder from a histogram already in ws.hist.
+int build_tables(const moe_cfg& c, const WsLayout& L, void* ws, const int32_t* topk_idx, int32_t* counts,
+                 int32_t* offsets, int32_t* dest, int32_t* row_token, int32_t* row_slot, cudaStream_t s) {
+  const int R = c.T * c.k;
+  MOE_TRY_CUDA(launch_scan(at<int32_t>(ws, L.hist), c.E, L.nb_route, R, at<int32_t>(ws, L.base), counts, offsets, s));
+  MOE_TRY_CUDA(launch_scatter(topk_idx, at<int32_t>(ws, L.base), c.T, c.E, c.k, L.nb_route, dest, row_token,
+                              row_slot, s));
+  return MOE_OK;
+}
+
+int fwd_gemms(const moe_cfg& c, const WsLayout& L, void* ws, const uint16_t* Xp, const uint16_t* x,
+              const int32_t* offsets, const int32_t* row_slot, const float* topk_w, const uint16_t* W1,
+              const uint16_t* W3, const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Op, cudaStream_t s) {
+  GemmArgs a = base_args(c, ws, L);
+  a.offsets = offsets;
+  a.row_slot = row_slot;
+  a.topk_w = topk_w;
+  a.Xp = Xp;
+  a.x = x;
+  a.W1 = W1;
+  a.W3 = W3;
+  a.W2 = W2;
+  a.H = H;
+  a.H_out = H;
+  a.AB_out = AB;
+  a.Op_out = Op;
+  MOE_TRY(launch_gemm(kG1, a, s, persistent_grid()));
+  MOE_TRY(launch_gemm(kG2, a, s, persistent_grid()));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg).total;
+}
+
+int moe_ws_init(const moe_cfg* cfg, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({}, {}, ws));
+  const WsLayout L = ws_layout(*cfg);
+  MOE_TRY_CUDA(cudaMemsetAsync(at<uint8_t>(ws, L.err), 0, 64, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_num_sms(void) { return num_sms(); }
+
+int moe_set_grid_limit(int n) {
+  g_grid_limit = n > 0 ? n : 0;
+  return MOE_OK;
+}
+
+int moe_route(const moe_cfg* cfg, const float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({logits, topk_idx, topk_w}, {}, ws));
+  const WsLayout L = ws_layout(*cfg);
+  const moe_cfg& c = *cfg;
+  MOE_TRY_CUDA(launch_route(logits, c.T, c.E, c.k, c.renorm, topk_idx, topk_w, at<int32_t>(ws, L.hist), L.nb_route,
+                            at<int>(ws, L.err), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x, int32_t* counts, int32_t* offsets,
+                 int32_t* dest, int32_t* row_token, int32_t* row_slot, uint16_t* Xp, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({topk_idx, counts, offsets, dest, row_token, row_slot}, {x, Xp}, ws));
+  const WsLayout L = ws_layout(*cfg);
+  const moe_cfg& c = *cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_TRY_CUDA(launch_hist(topk_idx, c.T, c.E, c.k, at<int32_t>(ws, L.hist), L.nb_route, at<int>(ws, L.err), s));
+  MOE_TRY(build_tables(c, L, ws, topk_idx, counts, offsets, dest, row_token, row_slot, s));
+  if (x && Xp) MOE_TRY_CUDA(launch_gather_rows_bf16(x, row_token, c.T, c.T * c.k, c.d_model, Xp, MOE_K_GATHER, s));
+  return MOE_OK;
+}
+
+int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x, const int32_t* offsets,
+                          const int32_t* row_slot, const float* topk_w, const uint16_t* W1, const uint16_t* W3,
+                          const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({Xp, offsets, row_slot, topk_w, W1, W3, W2, H, Oprime}, {x, AB}, ws));
+  if (cfg->n_shared > 0 && !x) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  return fwd_gemms(*cfg, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, H, AB, Oprime,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_cfg* cfg, const float* Oprime, const int32_t* dest, float* y, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({Oprime, dest, y}, {}, ws));
+  const moe_cfg& c = *cfg;
+  MOE_TRY_CUDA(launch_sum_rows_f32(Oprime, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                  const uint16_t* W2, float* y, int32_t* topk_idx, float* topk_w, void* ws, int use_megakernel,
+                  void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({logits, x, W1, W3, W2, y, topk_idx, topk_w}, {}, ws));
+  const moe_cfg& c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = c.T * c.k;
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  int32_t* row_slot = at<int32_t>(ws, L.row_slot);
+  int32_t* dest = at<int32_t>(ws, L.dest);
+  MOE_TRY_CUDA(launch_route(logits, c.T, c.E, c.k, c.renorm, topk_idx, topk_w, at<int32_t>(ws, L.hist), L.nb_route,
+                            at<int>(ws, L.err), s));
+  MOE_TRY(build_tables(c, L, ws, topk_idx, at<int32_t>(ws, L.counts), offsets, dest, row_token, row_slot, s));
+  if (use_megakernel)
+    return megakernel_fwd(c, L, static_cast<uint8_t*>(ws), x, W1, W3, W2, topk_w, y, persistent_grid(), s);
+  uint16_t* Xp = at<uint16_t>(ws, L.Xp);
+  float* Op = at<float>(ws, L.Op);
+  MOE_TRY_CUDA(launch_gather_rows_bf16(x, row_token, c.T, R, c.d_model, Xp, MOE_K_GATHER, s));
+  MOE_TRY(fwd_gemms(c, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, at<uint16_t>(ws, L.H),
+                    at<uint16_t>(ws, L.AB), Op, s));
+  MOE_TRY_CUDA(launch_sum_rows_f32(Op, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, s));
+  return MOE_OK;
+}
+
+int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_token, uint16_t* G, void* ws,
+                    void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({dy, row_token, G}, {}, ws));
+  const moe_cfg& c = *cfg;
+  MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, c.T * c.k, c.d_model, G, MOE_K_COMBINE_BWD, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint16_t* dy, const uint16_t* Xp,
+                              const uint16_t* x, const int32_t* offsets, const int32_t* row_slot, const int32_t* dest,
+                              const float* topk_w, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                              const uint16_t* H, const uint16_t* AB, uint16_t* dAB, uint16_t* Hw, float* dw,
+                              float* dXp, float* dW1, float* dW3, float* dW2, int which, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  if (which < 1 || which > 3) return MOE_ERR_ARG;
+  MOE_TRY(check_ptrs({G, dy, offsets, row_slot, dAB, Hw}, {Xp, x, dest, topk_w, W1, W3, W2, H, AB, dw, dXp, dW1, dW3, dW2}, ws));
+  if ((which & 1) && !(dest && topk_w && W1 && W3 && W2 && H && AB && dw && dXp)) return MOE_ERR_ARG;
+  if ((which & 2) && !(Xp && dW1 && dW3 && dW2)) return MOE_ERR_ARG;
+  if (cfg->n_shared > 0 && (which & 2) && !x) return MOE_ERR_ARG;
+  const moe_cfg& c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmArgs a = base_args(c, ws, L);
+  a.offsets = offsets;
+  a.row_slot = row_slot;
+  a.topk_w = topk_w;
+  a.Xp = Xp;
+  a.x = x;
+  a.W1 = W1;
+  a.W3 = W3;
+  a.W2 = W2;
+  a.H = H;
+  a.AB = AB;
+  a.G = G;
+  a.dy = dy;
+  a.dAB = dAB;
+  a.Hw = Hw;
+  a.dAB_out = dAB;
+  a.Hw_out = Hw;
+  a.partial_out = at<float>(ws, L.partial);
+  a.dXp_out = dXp;
+  a.dW1_out = dW1;
+  a.dW3_out = dW3;
+  a.dW2_out = dW2;
+  if (which & 1) {
+    MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, c.T * c.k, L.nt_dh, dw, s));
+    MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
+  }
+  if (which & 2) {
+    MOE_TRY(launch_gemm(kDW13, a, s, persistent_grid()));
+    MOE_TRY(launch_gemm(kDW2, a, s, persistent_grid()));
+  }
+  return MOE_OK;
+}
+
+int moe_dispatch_bwd(const moe_cfg* cfg, const float* dXp, const int32_t* dest, float* dx, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({dXp, dest, dx}, {}, ws));
+  const moe_cfg& c = *cfg;
+  MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_route_bwd(const moe_cfg* cfg, const float* logits, const int32_t* topk_idx, const float* topk_w,
+                  const float* dw, float* dlogits, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({logits, topk_idx, topk_w, dw, dlogits}, {}, ws));
+  const moe_cfg& c = *cfg;
+  MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits,
+                                static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, const uint16_t* x, const uint16_t* W1,
+                  const uint16_t* W3, const uint16_t* W2, const int32_t* topk_idx, const float* topk_w, void* ws,
+                  float* dx, float* dlogits, float* dW1, float* dW3, float* dW2, int which, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  if (which < 1 || which > 3) return MOE_ERR_ARG;
+  MOE_TRY(check_ptrs({dy, logits, x, W1, W3, W2, topk_idx, topk_w}, {dx, dlogits, dW1, dW3, dW2}, ws));
+  if ((which & 1) && !(dx && dlogits)) return MOE_ERR_ARG;
+  if ((which & 2) && !(dW1 && dW3 && dW2)) return MOE_ERR_ARG;
+  const moe_cfg& c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = c.T * c.k;
+  const int32_t* offsets = at<int32_t>(ws, L.offsets);
+  const int32_t* row_token = at<int32_t>(ws, L.row_token);
+  const int32_t* row_slot = at<int32_t>(ws, L.row_slot);
+  const int32_t* dest = at<int32_t>(ws, L.dest);
+  uint16_t* G = at<uint16_t>(ws, L.G);
+  uint16_t* dAB = at<uint16_t>(ws, L.dAB);
+  uint16_t* Hw = at<uint16_t>(ws, L.Hw);
+  float* dXp = at<float>(ws, L.dXp);
+  float* dw = at<float>(ws, L.dw);
+  GemmArgs a = base_args(c, ws, L);
+  a.offsets = offsets;
+  a.row_slot = row_slot;
+  a.topk_w = topk_w;
+  a.Xp = at<uint16_t>(ws, L.Xp);
+  a.x = x;
+  a.W1 = W1;
+  a.W3 = W3;
+  a.W2 = W2;
+  a.H = at<uint16_t>(ws, L.H);
+  a.AB = at<uint16_t>(ws, L.AB);
+  a.G = G;
+  a.dy = dy;
+  a.dAB = dAB;
+  a.Hw = Hw;
+  a.dAB_out = dAB;
+  a.Hw_out = Hw;
+  a.partial_out = at<float>(ws, L.partial);
+  a.dXp_out = dXp;
+  a.dW1_out = dW1;
+  a.dW3_out = dW3;
+  a.dW2_out = dW2;
+  if (which & 1) {  // B part: input gradients (critical path)
+    MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, R, c.d_model, G, MOE_K_COMBINE_BWD, s));
+    MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
+    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+    MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
+    MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, s));
+  }
+  if (which & 2) {  // W part: weight gradients (deferrable)
+    MOE_TRY(launch_gemm(kDW13, a, s, persistent_grid()));
+    MOE_TRY(launch_gemm(kDW2, a, s, persistent_grid()));
+  }
+  return MOE_OK;
+}
+
+int moe_get_device_error(const void* ws, void* stream, int* code, int* info) {
+  if (!ws || !code || !info) return MOE_ERR_ARG;
+  int host[2] = {0, 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The error word is the first field of every workspace layout.
+  MOE_TRY_CUDA(cudaMemcpyAsync(host, ws, sizeof(host), cudaMemcpyDeviceToHost, s));
+  MOE_TRY_CUDA(cudaStreamSynchronize(s));
+  *code = host[0];
+  *info = host[1];
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Shared definitions of the CUDA library: error recording, workspace layout,
+// tile constants.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Error codes as stored in the device error word (same values as moe.h).
+constexpr int MOE_ERR_NONFINITE_CODE = MOE_ERR_NONFINITE;
+constexpr int MOE_ERR_TIMEOUT_CODE = MOE_ERR_TIMEOUT;
+
+// Longest any spin in this library waits before giving up (1 s).  Normal
+// waits last microseconds; the limit only turns a bug into an error code
+// instead of a hung GPU.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+#ifdef __CUDACC__
+// First error wins: code in err[0], detail in err[1].
+__device__ __forceinline__ void record_error(int* err, int code, int info) {
+  if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, info);
+}
+#endif
+
+// Router / permutation: tokens per block.
+constexpr int kRouteTokensPerBlock = 256;
+
+// Grouped GEMM tile: 128 rows x 256 accumulator columns, K staged 64 at a
+// time (one 128-byte swizzle atom of bf16).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Offsets of the regions inside the caller's workspace (bytes from ws).
+struct WsLayout {
+  size_t err, hist, base, counts, offsets, dest, row_token, row_slot;
+  size_t Xp, AB, H, Op, G, dAB, Hw, dXp, partial, dw, mk;
+  size_t total;
+  int nb_route;  // router/permutation blocks
+  int nt_dh;     // column tiles of the dH GEMM (partial dot products per row)
+  int mk_ints;   // ints in the MegaKernel counter region
+};
+
+inline WsLayout ws_layout(const moe_cfg& c) {
+  WsLayout L{};
+  const size_t T = c.T, d = c.d_model, f = c.d_ff, E = c.E, k = c.k, S = c.n_shared;
+  const size_t R = T * k, Rs = R + S * T;
+  L.nb_route = ceil_div(c.T, kRouteTokensPerBlock);
+  L.nt_dh = ceil_div(c.d_ff, kBN);
+  // MegaKernel counters: cursor + 3 phase counters, one readiness counter
+  // per 128-row block of Xp, one per GEMM-1 m-tile (bounded by the m-tiles
+  // of every segment), padding.
+  const size_t mtiles_max = R / kBM + E + S * static_cast<size_t>(ceil_div(c.T, kBM)) + 2;
+  L.mk_ints = static_cast<int>(16 + ceil_div(static_cast<long long>(R), kBM) + mtiles_max + 16);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  L.err = take(64);
+  L.hist = take(sizeof(int) * E * L.nb_route);
+  L.base = take(sizeof(int) * E * L.nb_route);
+  L.counts = take(sizeof(int) * E);
+  L.offsets = take(sizeof(int) * (E + 1));
+  L.dest = take(sizeof(int) * R);
+  L.row_token = take(sizeof(int) * R);
+  L.row_slot = take(sizeof(int) * R);
+  L.Xp = take(2 * R * d);
+  L.AB = take(2 * Rs * 2 * f);
+  L.H = take(2 * Rs * f);
+  L.Op = take(4 * Rs * d);
+  L.G = take(2 * R * d);
+  L.dAB = take(2 * Rs * 2 * f);
+  L.Hw = take(2 * Rs * f);
+  L.dXp = take(4 * Rs * d);
+  L.partial = take(4 * R * L.nt_dh);
+  L.dw = take(4 * T * k);
+  L.mk = take(sizeof(int) * L.mk_ints);
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe

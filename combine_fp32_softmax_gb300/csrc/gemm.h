@@ -1,0 +1,54 @@
+// Grouped GEMM family over ragged expert segments (host launchers).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+enum GemmKind : int {
+  kG1 = 0,    // forward gate/up: A = Xp (x for shared rows), B = [W1 | W3] -> H (+ [a|b])
+  kG2 = 1,    // forward down:    A = H, B = W2 -> O' = w * o (fp32)
+  kDH = 2,    // backward dH:     A = G (dy for shared rows), B = W2 (MN-major) -> dAB, Hw, dw partials
+  kDX = 3,    // backward dX:     A = dAB, B = [W1 ; W3] (MN-major) -> dXp (fp32)
+  kDW13 = 4,  // backward dW1/3:  A = dAB^T, B = Xp^T (x^T for shared), ragged K -> dW1, dW3 (fp32)
+  kDW2 = 5,   // backward dW2:    A = G^T (dy^T for shared), B = Hw^T, ragged K -> dW2 (fp32)
+};
+
+// Pointers of one layer-level GEMM call.  Which are used depends on the kind.
+struct GemmArgs {
+  int T, d, f, E, k, S;
+  const int32_t* offsets;
+  const int32_t* row_slot;
+  const float* topk_w;
+  // operands (bf16)
+  const uint16_t* Xp;
+  const uint16_t* x;
+  const uint16_t* W1;
+  const uint16_t* W3;
+  const uint16_t* W2;
+  const uint16_t* H;
+  const uint16_t* AB;
+  const uint16_t* G;
+  const uint16_t* dy;
+  const uint16_t* dAB;
+  const uint16_t* Hw;
+  // outputs
+  uint16_t* H_out;
+  uint16_t* AB_out;
+  float* Op_out;
+  uint16_t* dAB_out;
+  uint16_t* Hw_out;
+  float* partial_out;
+  float* dXp_out;
+  float* dW1_out;
+  float* dW3_out;
+  float* dW2_out;
+  int* err;
+};
+
+// Returns MOE_OK or a negative MOE_ERR_* (tensor-map encoding or launch).
+int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_override = 0);
+
+}  // namespace moe

@@ -1,0 +1,33 @@
+// Host-side launchers of the library's kernels (internal; the public entry
+// points in api.cu validate arguments and call these).  All launch on
+// `stream` and return cudaGetLastError() of the launch.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* topk_idx,
+                         float* topk_w, int32_t* hist, int nb, int* err, cudaStream_t s);
+cudaError_t launch_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* hist, int nb, int* err,
+                        cudaStream_t s);
+cudaError_t launch_scan(const int32_t* hist, int E, int nb, int R, int32_t* base, int32_t* counts,
+                        int32_t* offsets, cudaStream_t s);
+cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, int E, int k, int nb,
+                           int32_t* dest, int32_t* row_token, int32_t* row_slot, cudaStream_t s);
+// dst[r] = src[idx[r]] for r < nrows, rows of `d` bf16 (zero row if the
+// index is outside [0, nsrc)).
+cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
+                                    uint16_t* dst, int trace_kind, cudaStream_t s);
+// out[t] = sum_j rows[sel[t*k+j]] (slot order) + sum_s rows[R + s*T + t], fp32.
+cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
+                                int trace_kind, cudaStream_t s);
+// dw[i] = sum_nt partial[dest[i] * nt + n] for the T*k slots.
+cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, int nt, float* dw, cudaStream_t s);
+cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const float* topk_w, const float* dw,
+                             int T, int E, int k, int renorm, float* dlogits, cudaStream_t s);
+int num_sms();
+
+}  // namespace moe

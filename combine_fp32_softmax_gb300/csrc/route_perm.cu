@@ -1,0 +1,486 @@
+// Router, deterministic token mapping, row gather and fixed-order row sums.
+//
+// Router: UniEP page ("Unified Expert-Parallel MoE MegaKernel for LLM
+// Training"), section 1.1: the gating network gives each token a probability
+// per expert, then top-k picks the target experts.
+// Token mapping: same page, section 2.2, Algorithm 1 (deterministic global
+// token mapping): a local stable sort by expert plus prefix-sum base offsets
+// gives every (token, slot) a unique, conflict-free address without atomics
+// on the addresses; with one rank the cross-rank base is 0.  Here the
+// "stable sort" is a per-block expert histogram, one flat exclusive scan over
+// the expert-major [E][blocks] table, and an in-block stable rank from warp
+// match/ballot masks.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "trace.h"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRouteWarps = 8;
+constexpr int kMaxRowsPerToken = 12;  // k <= 8 routed + S <= 4 shared
+
+// Softmax statistics of one logit row held lane-strided by a warp
+// (expert e = lane + 32 * i).  Router forward and backward both use this,
+// so the backward's probabilities are bit-identical to the forward's.
+template <int EPL>
+struct RowSoftmax {
+  float v[EPL];   // logits (-inf beyond E)
+  float ex[EPL];  // expf(v - m) (0 beyond E)
+  float m, s;     // max, sum of ex
+};
+
+template <int EPL>
+__device__ __forceinline__ bool row_softmax(const float* __restrict__ row, int E, int lane, RowSoftmax<EPL>& r) {
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    r.v[i] = (e < E) ? row[e] : -INFINITY;
+    if (e < E && !isfinite(r.v[i])) bad = true;
+  }
+  bad = __any_sync(kFull, bad);
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) m = fmaxf(m, r.v[i]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    r.ex[i] = (e < E) ? expf(r.v[i] - m) : 0.f;
+    s += r.ex[i];
+  }
+  // xor butterfly: every lane adds the same pairs, so all lanes end with
+  // the same bits.
+#pragma unroll
+  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  r.m = m;
+  r.s = s;
+  return !bad;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm, int32_t* __restrict__ topk_idx,
+                 float* __restrict__ topk_w, int32_t* __restrict__ hist, int nb, int* err) {
+  __shared__ int s_hist[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  const int tok0 = blockIdx.x * kRouteTokensPerBlock;
+  for (int tt = warp; tt < kRouteTokensPerBlock; tt += kRouteWarps) {
+    const int t = tok0 + tt;
+    if (t >= T) break;
+    RowSoftmax<EPL> r;
+    int my_idx = lane;  // placeholder routing for a rejected row: slot j -> expert j
+    float my_w = 0.f;
+    if (!row_softmax<EPL>(logits + static_cast<size_t>(t) * E, E, lane, r)) {
+      if (lane == 0) record_error(err, MOE_ERR_NONFINITE_CODE, t);
+    } else {
+      uint32_t taken = 0;
+      float psum = 0.f, my_p = 0.f;
+      for (int j = 0; j < k; ++j) {
+        // Best untaken entry of this lane: strictly greater keeps the lower
+        // index on ties (entries are visited in increasing expert index).
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && !(taken & (1u << i)) && (bi == 0x7fffffff || r.v[i] > bv)) {
+            bv = r.v[i];
+            bi = e;
+          }
+        }
+        // Warp argmax under (value desc, index asc): a strict total order,
+        // so every lane agrees on the winner.  -0.0 == +0.0 compares equal.
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+          const float ov = __shfl_xor_sync(kFull, bv, off);
+          const int oi = __shfl_xor_sync(kFull, bi, off);
+          if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        const int owner = bi & 31, which = bi >> 5;
+        float p_local = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (lane == owner && i == which) {
+            taken |= 1u << i;
+            p_local = r.ex[i] / r.s;
+          }
+        const float p = __shfl_sync(kFull, p_local, owner);
+        if (lane == j) {
+          my_idx = bi;
+          my_p = p;
+        }
+        psum += p;
+      }
+      my_w = renorm ? my_p / psum : my_p;
+    }
+    if (lane < k) {
+      topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+      topk_w[static_cast<size_t>(t) * k + lane] = my_w;
+      atomicAdd(&s_hist[my_idx], 1);  // integer count: order-independent
+    }
+  }
+  __syncthreads();
+  if (hist)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(e) * nb + blockIdx.x] = s_hist[e];
+}
+
+// Histogram of caller-provided expert indices (moe_dispatch without the
+// router).  Out-of-range indices are clamped (and reported) so the tables
+// stay a valid permutation.
+__global__ void __launch_bounds__(256)
+    hist_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k, int32_t* __restrict__ hist, int nb,
+                int* err) {
+  __shared__ int s_hist[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  const size_t s0 = static_cast<size_t>(blockIdx.x) * kRouteTokensPerBlock * k;
+  const int nslot = (min(T, (blockIdx.x + 1) * kRouteTokensPerBlock) - blockIdx.x * kRouteTokensPerBlock) * k;
+  for (int i = threadIdx.x; i < nslot; i += blockDim.x) {
+    int e = topk_idx[s0 + i];
+    if (e < 0 || e >= E) {
+      record_error(err, MOE_ERR_ARG, static_cast<int>(s0 + i));
+      e = min(max(e, 0), E - 1);
+    }
+    atomicAdd(&s_hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(e) * nb + blockIdx.x] = s_hist[e];
+}
+
+// One flat exclusive scan of the expert-major [E][nb] histogram: at (e, b)
+// it equals offsets[e] + (slots of expert e in blocks < b), i.e. the base
+// address of block b's first slot for expert e.
+__global__ void __launch_bounds__(1024)
+    scan_kernel(const int32_t* __restrict__ hist, int E, int nb, int R, int32_t* __restrict__ base,
+                int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int warp_tot[32];
+  const int n = E * nb;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (n + 1023) / 1024;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int local = 0;
+  for (int i = lo; i < hi; ++i) local += hist[i];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int v = warp_tot[lane];
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, off);
+      if (lane >= off) inc += y;
+    }
+    warp_tot[lane] = inc - v;
+  }
+  __syncthreads();
+  int run = warp_tot[w] + incl - local;
+  for (int i = lo; i < hi; ++i) {
+    base[i] = run;
+    run += hist[i];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int b0 = base[static_cast<size_t>(e) * nb];
+    const int b1 = (e + 1 < E) ? base[static_cast<size_t>(e + 1) * nb] : R;
+    offsets[e] = b0;
+    counts[e] = b1 - b0;
+  }
+  if (tid == 0) offsets[E] = R;
+}
+
+// Stable in-block ranks.  Warp w owns tokens [32w, 32w+32) of the block, i.e.
+// a contiguous run of 32*k flat slots, visited in k rounds of 32.  Pass 1
+// counts per (warp, expert); a prefix over warps (starting at the block's
+// global base) gives each warp's first address per expert; pass 2 ranks each
+// slot among equal-expert lanes of its round (match mask) and advances.
+__global__ void __launch_bounds__(256)
+    scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, int T, int E, int k,
+                   int nb, int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
+                   int32_t* __restrict__ row_slot) {
+  __shared__ int wrun[8][256];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, b = blockIdx.x;
+  for (int i = tid; i < 8 * 256; i += 256) (&wrun[0][0])[i] = 0;
+  __syncthreads();
+  const size_t slot0 = static_cast<size_t>(b) * kRouteTokensPerBlock * k;
+  const int nslot = (min(T, (b + 1) * kRouteTokensPerBlock) - b * kRouteTokensPerBlock) * k;
+  const int wslot0 = w * 32 * k;
+  for (int rnd = 0; rnd < k; ++rnd) {
+    const int il = wslot0 + rnd * 32 + lane;
+    const bool valid = il < nslot;
+    const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (valid && lane == __ffs(peers) - 1) wrun[w][e] += __popc(peers);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = base[static_cast<size_t>(e) * nb + b];
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) {
+      const int c = wrun[ww][e];
+      wrun[ww][e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int rnd = 0; rnd < k; ++rnd) {
+    const int il = wslot0 + rnd * 32 + lane;
+    const bool valid = il < nslot;
+    const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
+    const unsigned peers = __match_any_sync(kFull, e);
+    const int r = valid ? wrun[w][e] + __popc(peers & lt) : 0;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wrun[w][e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      const size_t i = slot0 + il;
+      dest[i] = r;
+      row_token[r] = static_cast<int>(i / k);
+      row_slot[r] = static_cast<int>(i);
+    }
+  }
+}
+
+// dst[r] = src[idx[r]]: one warp per row, 16-byte vectors, 4 in flight per
+// lane.  An index outside [0, nsrc) writes a zero row.
+__global__ void __launch_bounds__(256)
+    gather_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ idx, int nsrc, int nrows,
+                            int nvec, uint4* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows; r += nwarps) {
+    const int sr = idx[r];
+    const bool ok = static_cast<unsigned>(sr) < static_cast<unsigned>(nsrc);
+    const uint4* s = src + static_cast<size_t>(ok ? sr : 0) * nvec;
+    uint4* o = dst + static_cast<size_t>(r) * nvec;
+    for (int v = lane; v < nvec; v += 32 * 4) {
+      uint4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < nvec) t[u] = ok ? __ldg(s + v + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < nvec) o[v + 32 * u] = t[u];
+    }
+  }
+}
+
+// out[t] = ((rows[sel[t*k]] + rows[sel[t*k+1]]) + ...) + rows[R + t] + ...
+// in exactly that order, fp32, float4 per lane, one warp per token.
+__global__ void __launch_bounds__(256)
+    sum_rows_f32_kernel(const float4* __restrict__ rows, const int32_t* __restrict__ sel, int T, int k, int S,
+                        int nvec, float4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const long long R = static_cast<long long>(T) * k;
+  const long long nrows = R + static_cast<long long>(S) * T;
+  const int nr = k + S;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    long long myrow = 0;
+    if (lane < k) {
+      myrow = sel[static_cast<size_t>(t) * k + lane];
+      if (myrow < 0 || myrow >= nrows) myrow = 0;
+    } else if (lane < nr) {
+      myrow = R + static_cast<long long>(lane - k) * T + t;
+    }
+    const float4* base[kMaxRowsPerToken];
+#pragma unroll
+    for (int j = 0; j < kMaxRowsPerToken; ++j)
+      base[j] = rows + static_cast<size_t>(__shfl_sync(kFull, myrow, j)) * nvec;
+    float4* o = out + static_cast<size_t>(t) * nvec;
+    for (int v = lane; v < nvec; v += 32) {
+      float4 val[kMaxRowsPerToken];
+#pragma unroll
+      for (int j = 0; j < kMaxRowsPerToken; ++j)
+        if (j < nr) val[j] = __ldg(base[j] + v);
+      float4 acc = val[0];
+#pragma unroll
+      for (int j = 1; j < kMaxRowsPerToken; ++j)
+        if (j < nr) {
+          acc.x += val[j].x;
+          acc.y += val[j].y;
+          acc.z += val[j].z;
+          acc.w += val[j].w;
+        }
+      o[v] = acc;
+    }
+  }
+}
+
+// dw[i] = sum over column tiles n (in order) of partial[dest[i] * nt + n].
+__global__ void dw_reduce_kernel(const float* __restrict__ partial, const int32_t* __restrict__ dest, int R, int nt,
+                                 float* __restrict__ dw) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= R) return;
+  const size_t r = static_cast<size_t>(dest[i]);
+  float s = 0.f;
+  for (int n = 0; n < nt; ++n) s += partial[r * nt + n];
+  dw[i] = s;
+}
+
+// Router backward (softmax Jacobian restricted to the picked experts'
+// weights), one warp per token.
+template <int EPL>
+__global__ void __launch_bounds__(256)
+    route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
+                     const float* __restrict__ topk_w, const float* __restrict__ dw, int T, int E, int k, int renorm,
+                     float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    RowSoftmax<EPL> r;
+    const bool ok = row_softmax<EPL>(logits + static_cast<size_t>(t) * E, E, lane, r);
+    int my_idx = -1;
+    float my_w = 0.f, my_dw = 0.f;
+    if (lane < k) {
+      my_idx = topk_idx[static_cast<size_t>(t) * k + lane];
+      my_w = topk_w[static_cast<size_t>(t) * k + lane];
+      my_dw = dw[static_cast<size_t>(t) * k + lane];
+    }
+    float inner = 0.f;  // sum_j dw_j w_j in slot order
+    for (int j = 0; j < k; ++j)
+      inner += __shfl_sync(kFull, my_dw, j) * __shfl_sync(kFull, my_w, j);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      float pick_dw = 0.f, pick_w = 0.f;
+      bool picked = false;
+      for (int j = 0; j < k; ++j) {
+        const int sj = __shfl_sync(kFull, my_idx, j);
+        const float dj = __shfl_sync(kFull, my_dw, j);
+        const float wj = __shfl_sync(kFull, my_w, j);
+        if (sj == e) {
+          picked = true;
+          pick_dw = dj;
+          pick_w = wj;
+        }
+      }
+      if (e < E) {
+        float dz;
+        if (!ok)
+          dz = 0.f;
+        else if (renorm == 0)
+          dz = (r.ex[i] / r.s) * ((picked ? pick_dw : 0.f) - inner);
+        else
+          dz = picked ? pick_w * (pick_dw - inner) : 0.f;
+        dlogits[static_cast<size_t>(t) * E + e] = dz;
+      }
+    }
+  }
+}
+
+int sm_count_cached() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+int num_sms() { return sm_count_cached(); }
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* topk_idx, float* topk_w,
+                         int32_t* hist, int nb, int* err, cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_ROUTE, s);
+  const dim3 grid(ceil_div(T, kRouteTokensPerBlock)), block(kRouteWarps * 32);
+  if (E <= 32)
+    route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, renorm, topk_idx, topk_w, hist, nb, err);
+  else if (E <= 64)
+    route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, renorm, topk_idx, topk_w, hist, nb, err);
+  else if (E <= 128)
+    route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, renorm, topk_idx, topk_w, hist, nb, err);
+  else
+    route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, renorm, topk_idx, topk_w, hist, nb, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* hist, int nb, int* err,
+                        cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_HIST, s);
+  hist_kernel<<<nb, 256, 0, s>>>(topk_idx, T, E, k, hist, nb, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* hist, int E, int nb, int R, int32_t* base, int32_t* counts, int32_t* offsets,
+                        cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_SCAN, s);
+  scan_kernel<<<1, 1024, 0, s>>>(hist, E, nb, R, base, counts, offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, int E, int k, int nb, int32_t* dest,
+                           int32_t* row_token, int32_t* row_slot, cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_SCATTER, s);
+  scatter_kernel<<<nb, 256, 0, s>>>(topk_idx, base, T, E, k, nb, dest, row_token, row_slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
+                                    uint16_t* dst, int trace_kind, cudaStream_t s) {
+  if (nrows <= 0) return cudaSuccess;
+  TraceScope trace_scope(trace_kind, s);
+  const int blocks = min(ceil_div(nrows, 8), num_sms() * 8);
+  gather_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), idx, nsrc, nrows, d / 8,
+                                                 reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
+                                int trace_kind, cudaStream_t s) {
+  TraceScope trace_scope(trace_kind, s);
+  const int blocks = min(ceil_div(T, 8), num_sms() * 8);
+  sum_rows_f32_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(rows), sel, T, k, S, d / 4,
+                                             reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, int nt, float* dw, cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_DW_REDUCE, s);
+  dw_reduce_kernel<<<ceil_div(R, 256), 256, 0, s>>>(partial, dest, R, nt, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const float* topk_w, const float* dw,
+                             int T, int E, int k, int renorm, float* dlogits, cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_ROUTE_BWD, s);
+  const int blocks = min(ceil_div(T, 8), num_sms() * 8);
+  if (E <= 32)
+    route_bwd_kernel<1><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+  else if (E <= 64)
+    route_bwd_kernel<2><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+  else if (E <= 128)
+    route_bwd_kernel<4><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+  else
+    route_bwd_kernel<8><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,254 @@
+"""Python binding of libmoe_gb300 (include/moe.h).
+
+Argument marshalling only: every function turns torch CUDA tensors into raw
+device pointers and the current CUDA stream, calls the C entry point of the
+same name, and raises MoeError on a non-zero status.  All arithmetic runs in
+the library's CUDA kernels; there is no fallback path.  If the library is
+not built, loading it raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+from .configs import MoEConfig
+
+CODES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGN",
+         -4: "MOE_ERR_CUDA", -5: "MOE_ERR_NONFINITE", -6: "MOE_ERR_TIMEOUT"}
+MOE_OK, MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_ALIGN = 0, -1, -2, -3
+MOE_ERR_CUDA, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT = -4, -5, -6
+
+
+class MoeError(RuntimeError):
+    def __init__(self, name: str, code: int):
+        super().__init__(f"{name} returned {code} ({CODES.get(code, '?')})")
+        self.code = code
+
+
+class moe_cfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("T", "d_model", "d_ff", "E", "k", "n_shared", "renorm")]
+
+
+def cfg_of(c: MoEConfig) -> moe_cfg:
+    return moe_cfg(c.T, c.d, c.f, c.E, c.k, c.S, c.renorm)
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_CFG = ctypes.POINTER(moe_cfg)
+# name -> argument types (after the cfg pointer, before ws/stream where present)
+_SIGS = {
+    "moe_workspace_bytes": ([_CFG], ctypes.c_size_t),
+    "moe_ws_init": ([_CFG, _P, _P], _I),
+    "moe_route": ([_CFG, _P, _P, _P, _P, _P], _I),
+    "moe_dispatch": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_group_gemm_swiglu": ([_CFG] + [_P] * 13, _I),
+    "moe_combine": ([_CFG, _P, _P, _P, _P, _P], _I),
+    "moe_layer_fwd": ([_CFG] + [_P] * 9 + [_I, _P], _I),
+    "moe_combine_bwd": ([_CFG, _P, _P, _P, _P, _P], _I),
+    "moe_group_gemm_swiglu_bwd": ([_CFG] + [_P] * 20 + [_I, _P, _P], _I),
+    "moe_dispatch_bwd": ([_CFG, _P, _P, _P, _P, _P], _I),
+    "moe_route_bwd": ([_CFG, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_layer_bwd": ([_CFG] + [_P] * 14 + [_I, _P], _I),
+    "moe_get_device_error": ([_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "moe_num_sms": ([], _I),
+    "moe_set_grid_limit": ([_I], _I),
+    "moe_trace_enable": ([_I], _I),
+    "moe_trace_reset": ([], _I),
+    "moe_trace_read": ([_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
+    "moe_trace_kind_name": ([_I], ctypes.c_char_p),
+}
+
+# kernel kinds of the timing trace (MOE_K_* in include/moe.h)
+TRACE_KINDS = ["route", "hist", "scan", "scatter", "gather", "gemm1_swiglu", "gemm2_scale", "combine",
+               "combine_bwd", "gemm_dh", "dw_reduce", "route_bwd", "gemm_dx", "dispatch_bwd", "gemm_dw13",
+               "gemm_dw2", "megakernel"]
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = handle
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != 0:
+        raise MoeError(name, rc)
+
+
+def _cfg(c):
+    return ctypes.byref(c if isinstance(c, moe_cfg) else cfg_of(c))
+
+
+# ------------------------------------------------------------ entry points
+def moe_workspace_bytes(cfg) -> int:
+    return int(lib().moe_workspace_bytes(_cfg(cfg)))
+
+
+def moe_ws_init(cfg, ws, stream=None):
+    _call("moe_ws_init", _cfg(cfg), _ptr(ws), _stream(stream))
+
+
+def moe_route(cfg, logits, topk_idx, topk_w, ws, stream=None):
+    _call("moe_route", _cfg(cfg), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), _stream(stream))
+
+
+def moe_dispatch(cfg, topk_idx, x, counts, offsets, dest, row_token, row_slot, Xp, ws, stream=None):
+    _call("moe_dispatch", _cfg(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(dest),
+          _ptr(row_token), _ptr(row_slot), _ptr(Xp), _ptr(ws), _stream(stream))
+
+
+def moe_group_gemm_swiglu(cfg, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, H, AB, Oprime, ws, stream=None):
+    _call("moe_group_gemm_swiglu", _cfg(cfg), _ptr(Xp), _ptr(x), _ptr(offsets), _ptr(row_slot), _ptr(topk_w),
+          _ptr(W1), _ptr(W3), _ptr(W2), _ptr(H), _ptr(AB), _ptr(Oprime), _ptr(ws), _stream(stream))
+
+
+def moe_combine(cfg, Oprime, dest, y, ws, stream=None):
+    _call("moe_combine", _cfg(cfg), _ptr(Oprime), _ptr(dest), _ptr(y), _ptr(ws), _stream(stream))
+
+
+def moe_layer_fwd(cfg, logits, x, W1, W3, W2, y, topk_idx, topk_w, ws, use_megakernel=0, stream=None):
+    _call("moe_layer_fwd", _cfg(cfg), _ptr(logits), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y),
+          _ptr(topk_idx), _ptr(topk_w), _ptr(ws), int(use_megakernel), _stream(stream))
+
+
+def moe_combine_bwd(cfg, dy, row_token, G, ws, stream=None):
+    _call("moe_combine_bwd", _cfg(cfg), _ptr(dy), _ptr(row_token), _ptr(G), _ptr(ws), _stream(stream))
+
+
+def moe_group_gemm_swiglu_bwd(cfg, G, dy, Xp, x, offsets, row_slot, dest, topk_w, W1, W3, W2, H, AB,
+                              dAB, Hw, dw, dXp, dW1, dW3, dW2, which, ws, stream=None):
+    _call("moe_group_gemm_swiglu_bwd", _cfg(cfg), _ptr(G), _ptr(dy), _ptr(Xp), _ptr(x), _ptr(offsets),
+          _ptr(row_slot), _ptr(dest), _ptr(topk_w), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(H), _ptr(AB),
+          _ptr(dAB), _ptr(Hw), _ptr(dw), _ptr(dXp), _ptr(dW1), _ptr(dW3), _ptr(dW2), int(which), _ptr(ws),
+          _stream(stream))
+
+
+def moe_dispatch_bwd(cfg, dXp, dest, dx, ws, stream=None):
+    _call("moe_dispatch_bwd", _cfg(cfg), _ptr(dXp), _ptr(dest), _ptr(dx), _ptr(ws), _stream(stream))
+
+
+def moe_route_bwd(cfg, logits, topk_idx, topk_w, dw, dlogits, ws, stream=None):
+    _call("moe_route_bwd", _cfg(cfg), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(dw), _ptr(dlogits),
+          _ptr(ws), _stream(stream))
+
+
+def moe_layer_bwd(cfg, dy, logits, x, W1, W3, W2, topk_idx, topk_w, ws, dx, dlogits, dW1, dW3, dW2,
+                  which=3, stream=None):
+    _call("moe_layer_bwd", _cfg(cfg), _ptr(dy), _ptr(logits), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2),
+          _ptr(topk_idx), _ptr(topk_w), _ptr(ws), _ptr(dx), _ptr(dlogits), _ptr(dW1), _ptr(dW3), _ptr(dW2),
+          int(which), _stream(stream))
+
+
+def moe_get_device_error(ws, stream=None):
+    code, info = _I(0), _I(0)
+    _call("moe_get_device_error", _ptr(ws), _stream(stream), ctypes.byref(code), ctypes.byref(info))
+    return code.value, info.value
+
+
+def moe_num_sms() -> int:
+    return int(lib().moe_num_sms())
+
+
+def moe_set_grid_limit(n: int):
+    _call("moe_set_grid_limit", int(n))
+
+
+def moe_trace_enable(on: bool):
+    _call("moe_trace_enable", int(bool(on)))
+
+
+def moe_trace_reset():
+    _call("moe_trace_reset")
+
+
+def moe_trace_read() -> dict:
+    """{kernel kind: (total device ms, launches)} since the last reset."""
+    out = {}
+    for i, name in enumerate(TRACE_KINDS):
+        ms, n = ctypes.c_double(0), _I(0)
+        _call("moe_trace_read", i, ctypes.byref(ms), ctypes.byref(n))
+        if n.value:
+            out[name] = (ms.value, n.value)
+    return out
+
+
+# ------------------------------------------------------- workspace layout
+def ws_offsets(cfg: MoEConfig) -> dict:
+    """Byte offsets of the workspace regions, mirroring the library's layout
+    (used by tests and the benchmark to look at saved activations)."""
+    T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
+    R, Rs = T * k, T * k + S * T
+    nb = -(-T // 256)
+    nt = -(-f // 256)
+    o = 0
+    out = {}
+
+    def take(name, nbytes):
+        nonlocal o
+        out[name] = o
+        o = (o + nbytes + 255) // 256 * 256
+
+    for name, nbytes in [("err", 64), ("hist", 4 * E * nb), ("base", 4 * E * nb), ("counts", 4 * E),
+                         ("offsets", 4 * (E + 1)), ("dest", 4 * R), ("row_token", 4 * R),
+                         ("row_slot", 4 * R), ("Xp", 2 * R * d), ("AB", 4 * Rs * f), ("H", 2 * Rs * f),
+                         ("Op", 4 * Rs * d), ("G", 2 * R * d), ("dAB", 4 * Rs * f), ("Hw", 2 * Rs * f),
+                         ("dXp", 4 * Rs * d), ("partial", 4 * R * nt), ("dw", 4 * T * k)]:
+        take(name, nbytes)
+    out["_mk"] = o
+    return out
+
+
+def ws_view(ws: torch.Tensor, cfg: MoEConfig, name: str) -> torch.Tensor:
+    """A typed view of one workspace region."""
+    T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
+    R, Rs = T * k, T * k + S * T
+    shapes = {"counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
+              "row_token": ((R,), torch.int32), "row_slot": ((R,), torch.int32),
+              "Xp": ((R, d), torch.bfloat16), "AB": ((Rs, 2 * f), torch.bfloat16), "H": ((Rs, f), torch.bfloat16),
+              "Op": ((Rs, d), torch.float32), "G": ((R, d), torch.bfloat16), "dAB": ((Rs, 2 * f), torch.bfloat16),
+              "Hw": ((Rs, f), torch.bfloat16), "dXp": ((Rs, d), torch.float32), "dw": ((T, k), torch.float32)}
+    shape, dt = shapes[name]
+    off = ws_offsets(cfg)[name]
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty(0, dtype=dt).element_size()
+    return ws[off:off + nbytes].view(dt).view(*shape)
+
+
+def alloc_workspace(cfg: MoEConfig, device="cuda", stream=None) -> torch.Tensor:
+    ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=device)
+    moe_ws_init(cfg, ws, stream)
+    return ws

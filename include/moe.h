@@ -1,0 +1,255 @@
+/*
+ * moe.h — C ABI of libmoe_gb300: the single-GPU hot path of a
+ * Mixture-of-Experts layer on GB300 (sm_103a).
+ *
+ * The layer is the one UniEP fuses into a MegaKernel (UniEP page, "Unified
+ * Expert-Parallel MoE MegaKernel for LLM Training", section 1.1, Figure 1):
+ *   gate (softmax) -> top-k -> dispatch (scatter) -> GroupGEMM -> SwiGLU ->
+ *   GroupGEMM -> combine (weighted sum by gate score),
+ * and its backward, which mirrors the forward and needs the transposed
+ * GroupGEMM for the weight gradients (same section).  The SwiGLU expert is
+ * the MLP of the GraphPP page, sections 5.1-5.2 (gate projection W1, up
+ * projection W3, SiLU, gate product, down projection W2).
+ *
+ * Conventions shared by every call:
+ *  - Every data pointer is DEVICE memory owned by the caller.  The library
+ *    never allocates, frees or synchronises the host; every call enqueues
+ *    work on `stream` (a cudaStream_t passed as void*; NULL = legacy stream)
+ *    and returns immediately.
+ *  - bf16 tensors are passed as uint16_t* (raw bf16 bit patterns).
+ *  - Layouts are row-major.  Weights use the [out, in] layout of a linear
+ *    layer: W1, W3 are [E+S, f, d], W2 is [E+S, d, f]; the S shared
+ *    experts' weights follow the E routed experts' in the same arrays.
+ *  - Row space of the expert GEMMs ("GEMM rows"): rows [0, R) are the R=T*k
+ *    routed rows grouped by expert (expert e owns [offsets[e],
+ *    offsets[e+1])), rows [R + s*T, R + (s+1)*T) are shared expert s in
+ *    token order.  R_s = R + S*T.
+ *  - Every pointer must be 16-byte aligned (MOE_ERR_ALIGN otherwise); `ws`
+ *    must be 256-byte aligned and at least moe_workspace_bytes() long.
+ *  - Return value: MOE_OK, or a negative MOE_ERR_* detected on the host
+ *    before anything was enqueued.  Errors found by the kernels themselves
+ *    (non-finite logits, a bounded wait that ran out) are recorded in a
+ *    device error word inside `ws`; read it with moe_get_device_error().
+ *  - Results are bitwise deterministic: no call accumulates floating-point
+ *    values with atomics, and every reduction runs in a fixed order.
+ *  - Every output is fully overwritten (no accumulate-into mode).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Layer shape.  T tokens, model width d_model, expert hidden width d_ff,
+ * E routed experts, top-k routing, n_shared always-on shared experts,
+ * renorm = 0: routing weight = softmax probability of the expert;
+ * renorm = 1: probabilities renormalised over the k picks.
+ * Limits (MOE_ERR_SHAPE otherwise): 1 <= E <= 256, 1 <= k <= min(E, 8),
+ * 0 <= n_shared <= 4, d_model and d_ff multiples of 64, T >= 1,
+ * T * (k + n_shared) < 2^31 - 256, renorm in {0, 1}. */
+typedef struct moe_cfg {
+  int T, d_model, d_ff, E, k, n_shared, renorm;
+} moe_cfg;
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,       /* null pointer where one is required */
+  MOE_ERR_SHAPE = -2,     /* cfg outside the limits above */
+  MOE_ERR_ALIGN = -3,     /* pointer not 16-byte aligned (ws: 256-byte) */
+  MOE_ERR_CUDA = -4,      /* a CUDA runtime/driver call or launch failed */
+  MOE_ERR_NONFINITE = -5, /* device: a router logit was NaN or Inf */
+  MOE_ERR_TIMEOUT = -6    /* device: a bounded wait ran out */
+};
+
+/* Bytes of workspace for `cfg`.  The workspace holds the routing tables,
+ * the activations the backward needs (Xp, [a|b], H, O'), the backward's
+ * intermediates, scratch counters and the device error word.  The caller
+ * allocates it once; moe_layer_fwd fills it and moe_layer_bwd reads it, so
+ * it must stay alive and unmodified between the two. */
+size_t moe_workspace_bytes(const moe_cfg* cfg);
+
+/* Clears the device error word in `ws` (async on `stream`).  Call once after
+ * allocating the workspace; the layer calls do not clear it. */
+int moe_ws_init(const moe_cfg* cfg, void* ws, void* stream);
+
+/* Router (UniEP page, section 1.1: gating probabilities, then top-k).
+ * logits [T, E] fp32.  p = softmax over all E (fp32: max-subtract, expf,
+ * sum, divide).  The k experts are picked on the LOGITS, larger first, ties
+ * to the lower index, -0.0 == +0.0; slot j holds the j-th pick.
+ * topk_idx [T, k] int32, topk_w [T, k] fp32 (p, or p / sum of the k picked
+ * p when renorm = 1).  A NaN/Inf logit sets MOE_ERR_NONFINITE in the device
+ * error word (that token's outputs are then unspecified). */
+int moe_route(const moe_cfg* cfg, const float* logits, int32_t* topk_idx,
+              float* topk_w, void* ws, void* stream);
+
+/* Deterministic token mapping (UniEP page, section 2.2, Algorithm 1, for a
+ * single rank: the cross-rank base offset is 0) and dispatch gather.
+ * counts [E]: slots routed to each expert; offsets [E+1]: exclusive prefix
+ * sum (offsets[E] = R); dest [R]: flat slot t*k+j -> GEMM row; row_token [R]
+ * and row_slot [R]: GEMM row -> token and flat slot.  Within an expert the
+ * rows are in ascending flat-slot order, independent of thread scheduling.
+ * If x [T, d] (bf16) and Xp [R, d] (bf16) are both non-NULL, also gathers
+ * Xp[r] = x[row_token[r]]. */
+int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
+                 int32_t* counts, int32_t* offsets, int32_t* dest,
+                 int32_t* row_token, int32_t* row_slot, uint16_t* Xp,
+                 void* ws, void* stream);
+
+/* Expert FFN as two grouped GEMMs over the ragged expert segments
+ * (UniEP page, section 1.1 "GroupGEMM -> SwiGLU -> GroupGEMM"; padding-free
+ * grouped GEMM with per-segment pointer arithmetic, section 2.2).
+ * GEMM 1, per GEMM row r of segment e (A row = Xp[r], or x[t] for shared
+ * rows):  a = A.W1_e^T, b = A.W3_e^T accumulated in fp32;
+ *         H[r] = bf16(silu(a) * b), silu(a) = a / (1 + exp(-a)).
+ *         If AB is non-NULL, AB[r] = [bf16(a) | bf16(b)]  ([R_s, 2f]).
+ * GEMM 2: O'[r] = fl32(w_r * (H[r].W2_e^T)) with w_r = topk_w[row_slot[r]]
+ *         for routed rows and 1 for shared rows.  H [R_s, f] bf16,
+ *         O' [R_s, d] fp32.  Experts with no rows are skipped.
+ * offsets/row_slot come from moe_dispatch. */
+int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x,
+                          const int32_t* offsets, const int32_t* row_slot,
+                          const float* topk_w, const uint16_t* W1, const uint16_t* W3,
+                          const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime,
+                          void* ws, void* stream);
+
+/* Combine (UniEP page, section 1.1: weighted sum by gate score; the
+ * weight is already applied in O').  y [T, d] fp32:
+ *   y[t] = ((O'[dest[t*k]] + O'[dest[t*k+1]]) + ... + O'[dest[t*k+k-1]])
+ *          + O'[R + t] + ... + O'[R + (S-1)*T + t]
+ * summed in exactly this order in fp32, so y is bitwise reproducible. */
+int moe_combine(const moe_cfg* cfg, const float* Oprime, const int32_t* dest,
+                float* y, void* ws, void* stream);
+
+/* Whole forward: route -> dispatch -> GEMM 1 -> GEMM 2 -> combine.
+ * Outputs y [T, d] fp32, topk_idx [T, k], topk_w [T, k]; the routing tables
+ * and activations are kept in `ws` for moe_layer_bwd.  use_megakernel = 1
+ * runs dispatch..combine as one persistent launch that claims tasks from an
+ * atomic ticket counter and orders them with device-side readiness counters
+ * (UniEP page, section 2.2: persistent workers, scoreboard, dynamic SM
+ * scheduling); its outputs are bitwise equal to use_megakernel = 0. */
+int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x,
+                  const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                  float* y, int32_t* topk_idx, float* topk_w, void* ws,
+                  int use_megakernel, void* stream);
+
+/* ---------------------------------------------------------------- backward
+ * Gradients of a loss L given dy = dL/dy (bf16 [T, d]).  The backward is the
+ * mirror of the forward plus the transposed GroupGEMM for the weight
+ * gradients (UniEP page, section 1.1); it splits into the input-gradient
+ * part (B) and the weight-gradient part (W) (GraphPP page, sections 2 and
+ * 5.1). */
+
+/* Combine backward: G[r] = dy[row_token[r]] for the R routed rows (bf16,
+ * exact copy; shared rows read dy directly). */
+int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_token,
+                    uint16_t* G, void* ws, void* stream);
+
+/* Expert FFN backward.  For GEMM row r (token t, weight w_r, expert e):
+ *   dHraw = dy_t . W2_e            (fp32 accumulate, K = d)
+ *   dH = w_r * dHraw;  s = sigmoid(a)
+ *   dA = dH * b * s * (1 + a * (1 - s));  dB = dH * a * s
+ *   dAB[r] = [bf16(dA) | bf16(dB)]          ([R_s, 2f])
+ *   Hw[r]  = bf16(w_r * H[r])               ([R_s, f])
+ *   dw[t, j] = <dHraw, H[r]> for routed rows (= <dy_t, unscaled o_r>),
+ *              summed over fixed column tiles in tile order      ([T, k])
+ *   dXp[r] = dA . W1_e + dB . W3_e          (fp32 [R_s, d], K = 2f)
+ *   dW1_e = sum_r dA_r^T A_r, dW3_e = sum_r dB_r^T A_r   (fp32 [E+S, f, d])
+ *   dW2_e = sum_r dy_t^T Hw_r                              (fp32 [E+S, d, f])
+ * where A_r = Xp[r] (routed) or x[t] (shared); each weight-gradient sum
+ * runs over the segment's rows in ascending order inside one CTA (no
+ * split-K atomics), and experts with no rows get exact zeros.
+ * which: 1 = input part (dAB, Hw, dw, dXp), 2 = weight part (dW1, dW3, dW2;
+ * needs dAB and Hw from a previous which=1 call), 3 = both.
+ * G from moe_combine_bwd; AB, H from moe_group_gemm_swiglu. */
+int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint16_t* dy,
+                              const uint16_t* Xp, const uint16_t* x,
+                              const int32_t* offsets, const int32_t* row_slot,
+                              const int32_t* dest, const float* topk_w,
+                              const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                              const uint16_t* H, const uint16_t* AB,
+                              uint16_t* dAB, uint16_t* Hw, float* dw, float* dXp,
+                              float* dW1, float* dW3, float* dW2, int which,
+                              void* ws, void* stream);
+
+/* Dispatch backward: dx[t] = sum over j in slot order of dXp[dest[t*k+j]],
+ * then + dXp[R + s*T + t] for s = 0..S-1, fp32 (same order as combine). */
+int moe_dispatch_bwd(const moe_cfg* cfg, const float* dXp, const int32_t* dest,
+                     float* dx, void* ws, void* stream);
+
+/* Router backward.  dw [T, k] = dL/dw.  p recomputed from the logits
+ * exactly as moe_route computes it.
+ *   renorm = 0: dlogits_i = p_i * (dw_{j(i)} [i picked] - sum_j dw_j w_j)
+ *   renorm = 1: dlogits_i = w_{j(i)} (dw_{j(i)} - sum_j dw_j w_j) if i
+ *               was picked, else 0.
+ * The top-k choice itself is piecewise constant and has no gradient. */
+int moe_route_bwd(const moe_cfg* cfg, const float* logits, const int32_t* topk_idx,
+                  const float* topk_w, const float* dw, float* dlogits,
+                  void* ws, void* stream);
+
+/* Whole backward from the state moe_layer_fwd left in `ws`.
+ * which: 1 = dx and dlogits only (B part), 2 = dW1, dW3, dW2 only (W part;
+ * needs a previous which=1 or 3 call on the same ws), 3 = everything.
+ * Outputs not requested may be NULL. */
+int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits,
+                  const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                  const uint16_t* W2, const int32_t* topk_idx, const float* topk_w,
+                  void* ws, float* dx, float* dlogits, float* dW1, float* dW3,
+                  float* dW2, int which, void* stream);
+
+/* Reads the device error word of `ws` into *code (MOE_OK or a negative
+ * MOE_ERR_*) and *info (a code-specific detail, e.g. the token of a
+ * non-finite logit or the task of a timed-out wait).  Synchronises
+ * `stream` only. */
+int moe_get_device_error(const void* ws, void* stream, int* code, int* info);
+
+/* Number of SMs of the current device as the library sees it (grid size of
+ * its persistent kernels). */
+int moe_num_sms(void);
+
+/* Caps the number of CTAs of the persistent kernels (grouped GEMMs and the
+ * MegaKernel) at n; n <= 0 restores one CTA per SM.  Results never depend
+ * on it (each output element has one fixed producer and reduction order);
+ * it exists to test exactly that.  Process-wide, not thread-safe. */
+int moe_set_grid_limit(int n);
+
+/* ------------------------------------------------------- kernel timing
+ * Optional profiling aid.  While enabled, every kernel launch the library
+ * makes is bracketed by a pair of CUDA events recorded on the launching
+ * stream (no device memory is allocated; events come from a host pool).
+ * moe_trace_read() waits for the recorded events of that kind and returns
+ * the summed device time in milliseconds and the number of launches since
+ * the last moe_trace_reset().  Process-wide; thread-safe. */
+enum {
+  MOE_K_ROUTE = 0,        /* router (+ per-block expert histogram) */
+  MOE_K_HIST = 1,         /* histogram of caller-given expert indices */
+  MOE_K_SCAN = 2,         /* flat exclusive scan -> offsets, bases */
+  MOE_K_SCATTER = 3,      /* stable in-block ranks -> dest, row_token, row_slot */
+  MOE_K_GATHER = 4,       /* dispatch gather Xp[r] = x[row_token[r]] */
+  MOE_K_GEMM1 = 5,        /* grouped GEMM gate/up + SiLU*mul */
+  MOE_K_GEMM2 = 6,        /* grouped GEMM down + routing-weight scale */
+  MOE_K_COMBINE = 7,      /* slot-order fp32 combine */
+  MOE_K_COMBINE_BWD = 8,  /* G[r] = dy[row_token[r]] */
+  MOE_K_GEMM_DH = 9,      /* grouped GEMM dy.W2 + SwiGLU backward */
+  MOE_K_DW_REDUCE = 10,   /* dw from per-tile partial dots */
+  MOE_K_ROUTE_BWD = 11,   /* router backward */
+  MOE_K_GEMM_DX = 12,     /* grouped GEMM [dA|dB].[W1;W3] */
+  MOE_K_DISPATCH_BWD = 13,/* slot-order fp32 dx sum */
+  MOE_K_GEMM_DW13 = 14,   /* ragged-K grouped GEMM dW1, dW3 */
+  MOE_K_GEMM_DW2 = 15,    /* ragged-K grouped GEMM dW2 */
+  MOE_K_MEGAKERNEL = 16,  /* forward MegaKernel */
+  MOE_K_COUNT = 17
+};
+int moe_trace_enable(int on);
+int moe_trace_reset(void);
+int moe_trace_read(int kind, double* total_ms, int* launches);
+const char* moe_trace_kind_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

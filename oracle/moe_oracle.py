@@ -259,6 +259,10 @@ class Backward:
     dW3: np.ndarray      # [E+S, f, d]
     dW2: np.ndarray      # [E+S, d, f]
     dw: np.ndarray       # [T, k]
+    # per GEMM row (routed rows in segment order, then shared rows)
+    dA: np.ndarray = None    # [R_s, f] dL/da
+    dB: np.ndarray = None    # [R_s, f] dL/db
+    dXp: np.ndarray = None   # [R_s, d] dL/d(expert input) of the row
 
 
 def layer_bwd(fw: Forward, dy, x, W1, W3, W2, renorm: int = 0) -> Backward:
@@ -271,6 +275,8 @@ def layer_bwd(fw: Forward, dy, x, W1, W3, W2, renorm: int = 0) -> Backward:
     dx = np.zeros((T, d))
     dW1 = np.zeros((nexp, f, d)); dW3 = np.zeros((nexp, f, d)); dW2 = np.zeros((nexp, d, f))
     dw_rows = np.zeros(T * k)
+    Rs = fw.a.shape[0]
+    dA_rows = np.zeros((Rs, f)); dB_rows = np.zeros((Rs, f)); dXp_rows = np.zeros((Rs, d))
     for sg in fw.segs:
         if len(sg.rows) == 0:
             continue
@@ -282,13 +288,15 @@ def layer_bwd(fw: Forward, dy, x, W1, W3, W2, renorm: int = 0) -> Backward:
         dh = wg @ W2[sg.expert]                  # dL/dh   [n, f]
         dA = dh * b * dsilu(a)                   # dL/da
         dB = dh * silu(a)                        # dL/db
-        dx[sg.tokens] += dA @ W1[sg.expert] + dB @ W3[sg.expert]
+        dXp = dA @ W1[sg.expert] + dB @ W3[sg.expert]
+        dx[sg.tokens] += dXp
+        dA_rows[sg.rows], dB_rows[sg.rows], dXp_rows[sg.rows] = dA, dB, dXp
         dW2[sg.expert] = wg.T @ h
         dW1[sg.expert] = dA.T @ x[sg.tokens]
         dW3[sg.expert] = dB.T @ x[sg.tokens]
     dw = dw_rows[fw.perm.dest].reshape(T, k)
     dlogits = route_bwd(fw.routing, dw, renorm)
-    return Backward(dx, dlogits, dW1, dW3, dW2, dw)
+    return Backward(dx, dlogits, dW1, dW3, dW2, dw, dA_rows, dB_rows, dXp_rows)
 
 
 # --------------------------------------------------------------------------

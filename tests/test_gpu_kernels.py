@@ -1,0 +1,217 @@
+"""Each kernel alone through its C-ABI entry point against the CPU oracle
+(GPU).  Integer tables bit-exact; floats at the tolerances of gpu_util."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from combine_fp32_softmax_gb300 import moe
+from combine_fp32_softmax_gb300.configs import TINY, MoEConfig
+from combine_fp32_softmax_gb300.inputs import make_layer_inputs, make_logits, make_x
+from oracle import moe_oracle as O
+from tests.gpu_util import (DEV, assert_bf16_rounding_close, assert_grad_close, device_error, np64,
+                            to_dev)
+
+pytestmark = pytest.mark.gpu
+
+MID = MoEConfig("mid_T700_d256_f320_E6_k2_S1", 700, 256, 320, 6, 2, S=1)
+D192 = MoEConfig("d192_T333_d192_f128_E4_k3", 333, 192, 128, 4, 3)
+SKEW = MoEConfig("skew_T2048_d128_f192_E32_k4_zipf", 2048, 128, 192, 32, 4, zipf=True)
+EK = MoEConfig("ek_T200_d128_f128_E4_k4_renorm", 200, 128, 128, 4, 4, renorm=1)
+GEMM_CFGS = [TINY, MID, D192, SKEW, EK]
+
+
+def _route(cfg, logits_dev):
+    ws = moe.alloc_workspace(cfg, DEV)
+    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=DEV)
+    moe.moe_route(cfg, logits_dev, idx, w, ws)
+    return idx, w, ws
+
+
+def _dispatch(cfg, idx, x_dev, ws):
+    R = cfg.T * cfg.k
+    t = {n: torch.empty(s, dtype=torch.int32, device=DEV) for n, s in
+         [("counts", cfg.E), ("offsets", cfg.E + 1), ("dest", R), ("row_token", R), ("row_slot", R)]}
+    Xp = torch.empty(R, cfg.d, dtype=torch.bfloat16, device=DEV) if x_dev is not None else None
+    moe.moe_dispatch(cfg, idx, x_dev, t["counts"], t["offsets"], t["dest"], t["row_token"], t["row_slot"], Xp, ws)
+    return t, Xp
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("cfg", [TINY, MID, SKEW, EK,
+                                 MoEConfig("e256k8", 1000, 64, 64, 256, 8),
+                                 MoEConfig("e1k1", 77, 64, 64, 1, 1),
+                                 MoEConfig("e33k5_renorm", 513, 64, 64, 33, 5, renorm=1)],
+                         ids=lambda c: c.name)
+def test_route_matches_oracle(cfg):
+    z = make_logits(cfg, seed=1)
+    idx, w, ws = _route(cfg, z.to(DEV))
+    ref = O.route(z, cfg.k, cfg.renorm)
+    assert np.array_equal(idx.cpu().numpy(), ref.sel)
+    np.testing.assert_allclose(np64(w), ref.w, rtol=4e-6, atol=0)
+    assert device_error(ws) == (0, 0)
+
+
+def test_route_ties_and_signed_zero():
+    """Integer-valued logits with many ties and signed zeros."""
+    cfg = MoEConfig("ties", 4096, 64, 64, 48, 6)
+    g = torch.Generator().manual_seed(7)
+    z = torch.randint(-2, 3, (cfg.T, cfg.E), generator=g).float()
+    z[torch.rand(cfg.T, cfg.E, generator=g) < 0.2] = -0.0
+    idx, w, ws = _route(cfg, z.to(DEV))
+    ref = O.route(z, cfg.k)
+    assert np.array_equal(idx.cpu().numpy(), ref.sel)
+    np.testing.assert_allclose(np64(w), ref.w, rtol=4e-6)
+
+
+def test_hand_case_through_the_library():
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "route_hand_T8E4k2.json")))["cases"]
+    for case in cases:
+        z = torch.tensor(case["logits"], dtype=torch.float32)
+        cfg = MoEConfig("hand", z.shape[0], 64, 64, case["E"], case["k"])
+        idx, w, ws = _route(cfg, z.to(DEV))
+        assert idx.cpu().tolist() == case["sel"]
+        t, _ = _dispatch(cfg, idx, None, ws)
+        for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
+            assert t[name].cpu().tolist() == case[name], name
+
+
+def test_nonfinite_logit_is_reported():
+    cfg = MoEConfig("nan", 300, 64, 64, 8, 2)
+    z = make_logits(cfg)
+    z[123, 5] = float("nan")
+    idx, w, ws = _route(cfg, z.to(DEV))
+    code, info = device_error(ws)
+    assert code == moe.MOE_ERR_NONFINITE and info == 123
+    # the tables stay a valid permutation
+    t, _ = _dispatch(cfg, idx, None, ws)
+    assert sorted(t["dest"].cpu().tolist()) == list(range(cfg.T * cfg.k))
+
+
+# ------------------------------------------------------------ permutation
+@pytest.mark.parametrize("cfg", [TINY, MID, SKEW, EK, MoEConfig("big_e", 70000, 64, 64, 200, 8)],
+                         ids=lambda c: c.name)
+def test_dispatch_tables_bit_exact(cfg):
+    inp_x = make_x(cfg, seed=2)
+    z = make_logits(cfg, seed=2)
+    idx, w, ws = _route(cfg, z.to(DEV))
+    x_dev = inp_x.to(DEV)
+    t, Xp = _dispatch(cfg, idx, x_dev, ws)
+    ref = O.permute(O.route(z, cfg.k).sel, cfg.E)
+    for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
+        assert np.array_equal(t[name].cpu().numpy(), getattr(ref, name)), name
+    assert torch.equal(Xp, x_dev[t["row_token"].long()])
+
+
+def test_dispatch_rejects_out_of_range_expert_index():
+    cfg = MoEConfig("badidx", 100, 64, 64, 8, 2)
+    idx = torch.zeros(cfg.T, cfg.k, dtype=torch.int32)
+    idx[:, 1] = 1
+    idx[17, 0] = 9  # out of range
+    ws = moe.alloc_workspace(cfg, DEV)
+    t, _ = _dispatch(cfg, idx.to(DEV), None, ws)
+    code, info = device_error(ws)
+    assert code == moe.MOE_ERR_ARG and info == 17 * 2
+    assert sorted(t["dest"].cpu().tolist()) == list(range(cfg.T * cfg.k))
+
+
+# ---------------------------------------------------------------- combine
+@pytest.mark.parametrize("cfg", [TINY, MID, EK], ids=lambda c: c.name)
+def test_combine_and_dispatch_bwd_sum_in_slot_order(cfg):
+    """y[t] = ((O'[dest[t,0]] + O'[dest[t,1]]) + ...) + shared rows, in fp32:
+    the same sum in the same order in numpy float32 gives the same bits."""
+    z = make_logits(cfg, seed=3)
+    idx, _, ws = _route(cfg, z.to(DEV))
+    t, _ = _dispatch(cfg, idx, None, ws)
+    g = torch.Generator().manual_seed(3)
+    Op = torch.randn(cfg.Rs, cfg.d, generator=g, dtype=torch.float32)
+    dest = t["dest"].cpu().numpy().reshape(cfg.T, cfg.k)
+    Opn = Op.numpy()
+    want = Opn[dest[:, 0]].copy()
+    for j in range(1, cfg.k):
+        want = want + Opn[dest[:, j]]
+    for s in range(cfg.S):
+        want = want + Opn[cfg.R + s * cfg.T: cfg.R + (s + 1) * cfg.T]
+    for fn in (moe.moe_combine, moe.moe_dispatch_bwd):
+        y = torch.empty(cfg.T, cfg.d, dtype=torch.float32, device=DEV)
+        fn(cfg, Op.to(DEV), t["dest"], y, ws)
+        assert np.array_equal(y.cpu().numpy(), want)
+
+
+# --------------------------------------------------------------- route bwd
+@pytest.mark.parametrize("cfg", [MID, EK, MoEConfig("e64k6", 999, 64, 64, 64, 6)], ids=lambda c: c.name)
+def test_route_bwd_matches_oracle(cfg):
+    z = make_logits(cfg, seed=4)
+    idx, w, ws = _route(cfg, z.to(DEV))
+    dw = torch.randn(cfg.T, cfg.k, generator=torch.Generator().manual_seed(4))
+    dz = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=DEV)
+    moe.moe_route_bwd(cfg, z.to(DEV), idx, w, dw.to(DEV), dz, ws)
+    ref = O.route_bwd(O.route(z, cfg.k, cfg.renorm), dw.double().numpy(), cfg.renorm)
+    assert_grad_close("dlogits", dz, ref)
+
+
+# ------------------------------------------------------------ expert GEMMs
+def _fwd_pieces(cfg, seed=5):
+    inp = make_layer_inputs(cfg, seed)
+    g = to_dev(inp)
+    idx, w, ws = _route(cfg, g["logits"])
+    t, Xp = _dispatch(cfg, idx, g["x"], ws)
+    H = torch.empty(cfg.Rs, cfg.f, dtype=torch.bfloat16, device=DEV)
+    AB = torch.empty(cfg.Rs, 2 * cfg.f, dtype=torch.bfloat16, device=DEV)
+    Op = torch.empty(cfg.Rs, cfg.d, dtype=torch.float32, device=DEV)
+    moe.moe_group_gemm_swiglu(cfg, Xp, g["x"], t["offsets"], t["row_slot"], w, g["W1"], g["W3"], g["W2"],
+                              H, AB, Op, ws)
+    fw = O.layer_fwd(inp.x, inp.logits, inp.W1, inp.W3, inp.W2, k=cfg.k, S=cfg.S, renorm=cfg.renorm)
+    return inp, g, idx, w, ws, t, Xp, H, AB, Op, fw
+
+
+@pytest.mark.parametrize("cfg", GEMM_CFGS, ids=lambda c: c.name)
+def test_gemm_fwd_matches_oracle(cfg):
+    inp, g, idx, w, ws, t, Xp, H, AB, Op, fw = _fwd_pieces(cfg)
+    assert device_error(ws) == (0, 0)
+    assert_bf16_rounding_close("a", AB[:, :cfg.f], fw.a)
+    assert_bf16_rounding_close("b", AB[:, cfg.f:], fw.b)
+    assert_bf16_rounding_close("H", H, fw.h)
+    wrow = np.ones(cfg.Rs)
+    wrow[:cfg.R] = fw.routing.w.reshape(-1)[fw.perm.row_slot]
+    assert_grad_close("O'", Op, wrow[:, None] * fw.o)
+
+
+@pytest.mark.parametrize("cfg", GEMM_CFGS, ids=lambda c: c.name)
+def test_gemm_bwd_matches_oracle(cfg):
+    inp, g, idx, w, ws, t, Xp, H, AB, Op, fw = _fwd_pieces(cfg)
+    bw = O.layer_bwd(fw, inp.dy, inp.x, inp.W1, inp.W3, inp.W2, renorm=cfg.renorm)
+    G = torch.empty(cfg.R, cfg.d, dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine_bwd(cfg, g["dy"], t["row_token"], G, ws)
+    assert torch.equal(G, g["dy"][t["row_token"].long()])
+    nexp = cfg.E + cfg.S
+    dAB = torch.empty(cfg.Rs, 2 * cfg.f, dtype=torch.bfloat16, device=DEV)
+    Hw = torch.empty(cfg.Rs, cfg.f, dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=DEV)
+    dXp = torch.empty(cfg.Rs, cfg.d, dtype=torch.float32, device=DEV)
+    dW1 = torch.full((nexp, cfg.f, cfg.d), float("nan"), device=DEV)
+    dW3 = torch.full((nexp, cfg.f, cfg.d), float("nan"), device=DEV)
+    dW2 = torch.full((nexp, cfg.d, cfg.f), float("nan"), device=DEV)
+    moe.moe_group_gemm_swiglu_bwd(cfg, G, g["dy"], Xp, g["x"], t["offsets"], t["row_slot"], t["dest"], w,
+                                  g["W1"], g["W3"], g["W2"], H, AB, dAB, Hw, dw, dXp, dW1, dW3, dW2, 3, ws)
+    assert device_error(ws) == (0, 0)
+    wrow = np.ones(cfg.Rs)
+    wrow[:cfg.R] = fw.routing.w.reshape(-1)[fw.perm.row_slot]
+    assert_grad_close("dA", dAB[:, :cfg.f], bw.dA)
+    assert_grad_close("dB", dAB[:, cfg.f:], bw.dB)
+    # Hw = bf16(w * bf16(h)): two bf16 roundings of w * h
+    ref_hw = wrow[:, None] * fw.h
+    bad = np.abs(np64(Hw) - ref_hw) > 2.0 ** -7 * np.abs(ref_hw) + 1e-4 * np.sqrt(np.mean(ref_hw ** 2))
+    assert not bad.any(), f"Hw: {int(bad.sum())} elements beyond two bf16 roundings"
+    assert_grad_close("dw", dw, bw.dw)
+    assert_grad_close("dXp", dXp, bw.dXp)
+    assert_grad_close("dW1", dW1, bw.dW1)
+    assert_grad_close("dW3", dW3, bw.dW3)
+    assert_grad_close("dW2", dW2, bw.dW2)
+    counts = t["counts"].cpu().numpy()
+    for e in np.nonzero(counts == 0)[0]:  # empty experts: exact zeros
+        assert torch.count_nonzero(dW1[e]) == 0 and torch.count_nonzero(dW3[e]) == 0
+        assert torch.count_nonzero(dW2[e]) == 0

@@ -1,0 +1,121 @@
+"""The whole layer (forward + backward) through moe_layer_fwd/moe_layer_bwd
+against the CPU oracle, determinism, and the full-size sampled check (GPU)."""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+from combine_fp32_softmax_gb300 import moe
+from combine_fp32_softmax_gb300.configs import DSV2_LITE, TINY, MoEConfig
+from combine_fp32_softmax_gb300.inputs import make_layer_inputs
+from oracle import moe_oracle as O
+from tests.gpu_util import (DEV, assert_grad_close, assert_layer_close, device_error, np64, run_layer,
+                            to_dev)
+
+pytestmark = pytest.mark.gpu
+
+MID = MoEConfig("mid_T700_d256_f320_E6_k2_S1", 700, 256, 320, 6, 2, S=1)
+SKEW = MoEConfig("skew_T2048_d128_f192_E32_k4_zipf", 2048, 128, 192, 32, 4, zipf=True)
+EK = MoEConfig("ek_T200_d128_f128_E4_k4_renorm", 200, 128, 128, 4, 4, renorm=1)
+WIDE = MoEConfig("wide_T1500_d512_f704_E8_k2_S2", 1500, 512, 704, 8, 2, S=2)
+LAYER_CFGS = [TINY, MID, SKEW, EK, WIDE]
+
+
+def _check_layer(cfg, out, inp):
+    fw = O.layer_fwd(inp.x, inp.logits, inp.W1, inp.W3, inp.W2, k=cfg.k, S=cfg.S, renorm=cfg.renorm)
+    bw = O.layer_bwd(fw, inp.dy, inp.x, inp.W1, inp.W3, inp.W2, renorm=cfg.renorm)
+    assert np.array_equal(out["topk_idx"].cpu().numpy(), fw.routing.sel)
+    np.testing.assert_allclose(np64(out["topk_w"]), fw.routing.w, rtol=4e-6)
+    assert_layer_close("y", out["y"], fw.y)
+    assert_grad_close("dx", out["dx"], bw.dx)
+    assert_grad_close("dlogits", out["dlogits"], bw.dlogits)
+    assert_grad_close("dW1", out["dW1"], bw.dW1)
+    assert_grad_close("dW3", out["dW3"], bw.dW3)
+    assert_grad_close("dW2", out["dW2"], bw.dW2)
+
+
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_layer_matches_oracle(cfg):
+    inp = make_layer_inputs(cfg, seed=11)
+    out, ws = run_layer(cfg, to_dev(inp), fill=float("nan"))
+    assert device_error(ws) == (0, 0)
+    _check_layer(cfg, out, inp)
+
+
+def _digest(out):
+    h = hashlib.sha256()
+    for k in sorted(out):
+        h.update(out[k].contiguous().cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+def test_bitwise_identical_across_10_runs():
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=12))
+    digests = {_digest(run_layer(cfg, g)[0]) for _ in range(10)}
+    assert len(digests) == 1
+
+
+def test_results_do_not_depend_on_grid_size():
+    cfg = SKEW
+    g = to_dev(make_layer_inputs(cfg, seed=13))
+    digests = set()
+    try:
+        for n in (1, 7, 0):
+            moe.moe_set_grid_limit(n)
+            digests.add(_digest(run_layer(cfg, g)[0]))
+    finally:
+        moe.moe_set_grid_limit(0)
+    assert len(digests) == 1
+
+
+def test_b_and_w_parts_split():
+    """which=1 then which=2 gives the same bits as which=3."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=14))
+    full, _ = run_layer(cfg, g, which=3)
+    ws = moe.alloc_workspace(cfg, DEV)
+    part, ws = run_layer(cfg, g, ws=ws, which=1)
+    moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"], part["topk_idx"],
+                      part["topk_w"], ws, None, None, part["dW1"], part["dW3"], part["dW2"], which=2)
+    for k in full:
+        assert torch.equal(full[k], part[k]), k
+
+
+@pytest.mark.slow
+def test_full_size_sampled_parity():
+    """The benchmark workload (DeepSeek-V2-Lite-like layer: T=8192, d=2048,
+    f=1408, 64 experts top-6, 2 shared) in the benchmark's launch
+    configuration: routing and the permutation in full, y / dx / dlogits on
+    256 seeded tokens, and weight-gradient entries of several experts summed
+    over their whole segments."""
+    cfg = DSV2_LITE
+    inp = make_layer_inputs(cfg, seed=0)
+    out, ws = run_layer(cfg, to_dev(inp))
+    assert device_error(ws) == (0, 0)
+    routing = O.route(inp.logits, cfg.k, cfg.renorm)
+    assert np.array_equal(out["topk_idx"].cpu().numpy(), routing.sel)
+    perm = O.permute(routing.sel, cfg.E)
+    for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
+        assert np.array_equal(moe.ws_view(ws, cfg, name).cpu().numpy(), getattr(perm, name)), name
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(cfg.T, 256, replace=False))
+    _, y, dx, dz, _ = O.tokens_fwd_bwd(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
+                                       cfg.renorm, toks)
+    assert_layer_close("y", np64(out["y"])[toks], y)
+    assert_grad_close("dx", np64(out["dx"])[toks], dx)
+    assert_grad_close("dlogits", np64(out["dlogits"])[toks], dz)
+    counts = perm.counts
+    experts = [int(np.argmax(counts)), int(np.argmin(counts)), 7, cfg.E, cfg.E + 1]
+    for which, gpu in (("W1", out["dW1"]), ("W3", out["dW3"]), ("W2", out["dW2"])):
+        for e in experts:
+            nr, nc = gpu.shape[1], gpu.shape[2]
+            rows, cols = rng.integers(0, nr, 64), rng.integers(0, nc, 64)
+            ref = O.dW_entries(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
+                               cfg.renorm, which, e, rows, cols)
+            got = np64(gpu[e])[rows, cols]
+            if counts[e] == 0 if e < cfg.E else False:
+                assert np.all(got == 0)
+                continue
+            assert_grad_close(f"d{which}[{e}] sample", got, ref)
