@@ -1,11 +1,407 @@
-// Forward MegaKernel (placeholder until the persistent task-queue kernel is in).
-#include <cuda_runtime.h>
-
-#include "common.cuh"
+// Forward MegaKernel: dispatch gather -> GEMM 1 (+SiLU*mul) -> GEMM 2
+// (+routing weight) -> combine, as one persistent launch.
+//
+// UniEP page ("Unified Expert-Parallel MoE MegaKernel for LLM Training"),
+// section 2.2: exactly one persistent worker per SM, roles chosen at run time
+// from a ticket taken off one global atomic counter (the linearised task
+// space puts communication tasks first, compute tasks after), and a
+// global-memory scoreboard that marks when every token of a GroupGEMM tile
+// has arrived, which compute workers poll before starting the tile.  On one
+// GPU the communication task is the local dispatch gather; the scoreboard is
+// a set of readiness counters:
+//   ctr[0]                   ticket cursor
+//   ctr[1]                   GEMM-2 warp-tiles finished (combine waits on all)
+//   ctr[kCtrXp + g]          Xp row block g (128 rows) gathered
+//   ctr[kCtrXp + NG + mt]    GEMM-1 warp-tiles finished of m-tile mt
+//                            (GEMM-2 tiles of mt wait for all of them)
+// A task only ever waits on tasks with lower tickets, and each CTA runs its
+// tasks in ticket order, so the lowest unfinished task can always proceed:
+// no deadlock, with or without co-residency of all CTAs.  Every wait is
+// bounded (1 s) and reports MOE_ERR_TIMEOUT instead of hanging.
+//
+// GEMM tiles run exactly the MMA sequence and epilogue of the stand-alone
+// grouped GEMM kernels and the combine sums in the same order as the
+// combine kernel, so the outputs are bitwise equal to the unfused chain.
+#include "gemm_tiles.cuh"
 
 namespace moe {
-int megakernel_fwd(const moe_cfg&, const WsLayout&, uint8_t*, const uint16_t*, const uint16_t*, const uint16_t*,
-                   const uint16_t*, const float*, float*, int, cudaStream_t) {
-  return MOE_ERR_ARG;
+namespace {
+
+constexpr int kTq = 4;              // depth of the producer -> consumer task FIFO
+constexpr int kGatherRows = 128;    // Xp rows per gather task
+constexpr int kCombineTokens = 32;  // tokens per combine task (8 per epilogue warp)
+constexpr int kCtrXp = 8;
+constexpr int kMaxTokRows = 12;     // k <= 8 routed + S <= 4 shared rows per token
+
+struct MegaParams {
+  GemmParams g1, g2;
+  const uint16_t* x;
+  const int32_t* row_token;
+  const int32_t* dest;
+  uint16_t* Xp;
+  const float* Op;
+  float* y;
+  int* ctr;
+  int NG, NC;
+  int skip;  // testing aid: ticket treated as never done (-1: none)
+};
+
+int g_skip_ticket = -1;
+
+struct MegaShared {
+  SharedState g;
+  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kStages];
+  int tq[kTq];
+  int ntn1, ntn2, nt1, nt2, total;
+};
+
+constexpr int kMegaSmemBytes = 1024 + kStages * kStageBytes + static_cast<int>(sizeof(MegaShared));
+
+// ------------------------------------------------------ bulk copies (1D)
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst_smem)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src_smem)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bounded acquire-spin until *c >= target.
+__device__ bool wait_counter(const int* c, int target, volatile int* abort, int* err, int where) {
+  if (ld_acquire_gpu(c) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(c) < target) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, MOE_ERR_TIMEOUT_CODE, where);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Publishes this warp's global stores (generic and to the async proxy that
+// TMA reads through), then lane 0 adds one to the readiness counter.
+__device__ __forceinline__ void warp_signal(int* counter) {
+  fence_proxy_async_global();
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) red_release_gpu_add(counter, 1);
+}
+
+// Gather task g (producer lane): Xp rows [128g, 128g+128) <- x[row_token],
+// row by row with bulk copies through the stage buffers (up to 3 chunks in
+// flight), then publish the block.
+struct GatherState {
+  uint32_t par = 0;      // next wait parity of gbar[b] (bit b)
+  uint32_t pending = 0;  // buffers with loads issued but not yet waited on
+};
+
+__device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem, int g, GatherState& gs,
+                            volatile int* abort, int where) {
+  const int d = mp.g1.d;
+  const uint32_t rb = 2u * d;
+  const int rps = min(kGatherRows, kStageBytes / static_cast<int>(rb));
+  const int r0 = g * kGatherRows;
+  const int nrows = min(kGatherRows, mp.g1.R - r0);
+  const int nchunk = (nrows + rps - 1) / rps;
+  for (int c = 0; c <= nchunk; ++c) {
+    if (c < nchunk) {
+      const int b = c % kStages;
+      if (c >= kStages) bulk_wait_read<kStages - 2>();  // chunk c-4 finished reading buffer b
+      const int n = min(rps, nrows - c * rps);
+      uint8_t* buf = smem + b * kStageBytes;
+      mbar_arrive_expect_tx(&ms.gbar[b], n * rb);
+      for (int i = 0; i < n; ++i) {
+        const int tok = mp.row_token[r0 + c * rps + i];
+        bulk_load(buf + i * rb, mp.x + static_cast<size_t>(tok) * d, rb, &ms.gbar[b]);
+      }
+      gs.pending |= 1u << b;
+    }
+    if (c > 0) {
+      const int pc = c - 1, b = pc % kStages;
+      if (!mbar_wait(&ms.gbar[b], (gs.par >> b) & 1, abort, mp.g1.err, where)) return false;
+      gs.par ^= 1u << b;
+      gs.pending &= ~(1u << b);
+      const int n = min(rps, nrows - pc * rps);
+      uint8_t* buf = smem + b * kStageBytes;
+      for (int i = 0; i < n; ++i) bulk_store(mp.Xp + static_cast<size_t>(r0 + pc * rps + i) * d, buf + i * rb, rb);
+      bulk_commit();
+    }
+  }
+  bulk_wait_all();
+  fence_proxy_async_global();
+  red_release_gpu_add(&mp.ctr[kCtrXp + g], 1);
+  return true;
+}
+
+__device__ void gather_drain(MegaShared& ms, const GatherState& gs) {
+  bulk_wait_all();
+  for (int b = 0; b < kStages; ++b)
+    if (gs.pending & (1u << b)) mbar_wait_drain(&ms.gbar[b], (gs.par >> b) & 1);
+}
+
+// GEMM-2 tile t2 described with GEMM-1's segment table (same m-tiles).
+__device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaShared& ms, int t2) {
+  const int mt = t2 / ms.ntn2, nb = t2 - mt * ms.ntn2;
+  TileInfo t = decode_tile<kG1>(mp.g1, ms.g, mt * ms.ntn1);
+  t.n0 = nb * kBN;
+  t.nkb = mp.g2.K / kBK;
+  return t;
+}
+
+// Combine task (one epilogue warp, 8 tokens): the same fp32 sum, in the same
+// order, as the stand-alone combine kernel.
+__device__ void combine_warp(const MegaParams& mp, int c) {
+  const int lane = threadIdx.x & 31, ew = (threadIdx.x >> 5) - 2;
+  const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R;
+  const int nr = k + S, nvec = mp.g1.d / 4;
+  const float4* rows = reinterpret_cast<const float4*>(mp.Op);
+  for (int i = 0; i < kCombineTokens / 4; ++i) {
+    const int t = c * kCombineTokens + ew * (kCombineTokens / 4) + i;
+    if (t >= T) break;
+    long long myrow = 0;
+    if (lane < k)
+      myrow = mp.dest[static_cast<size_t>(t) * k + lane];
+    else if (lane < nr)
+      myrow = R + static_cast<long long>(lane - k) * T + t;
+    const float4* base[kMaxTokRows];
+#pragma unroll
+    for (int j = 0; j < kMaxTokRows; ++j) base[j] = rows + static_cast<size_t>(__shfl_sync(0xffffffffu, myrow, j)) * nvec;
+    float4* o = reinterpret_cast<float4*>(mp.y) + static_cast<size_t>(t) * nvec;
+    for (int v = lane; v < nvec; v += 32) {
+      float4 val[kMaxTokRows];
+#pragma unroll
+      for (int j = 0; j < kMaxTokRows; ++j)
+        if (j < nr) val[j] = base[j][v];
+      float4 acc = val[0];
+#pragma unroll
+      for (int j = 1; j < kMaxTokRows; ++j)
+        if (j < nr) {
+          acc.x += val[j].x;
+          acc.y += val[j].y;
+          acc.z += val[j].z;
+          acc.w += val[j].w;
+        }
+      o[v] = acc;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_constant__ MegaParams mp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + kStages * kStageBytes);
+  SharedState& ss = ms.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* err = mp.g1.err;
+
+  if (threadIdx.x == 0) {
+    init_gemm_barriers(ss);
+    for (int q = 0; q < kTq; ++q) {
+      mbar_init(&ms.tq_full[q], 1);
+      mbar_init(&ms.tq_empty[q], 5);  // MMA warp + 4 epilogue warps
+    }
+    for (int b = 0; b < kStages; ++b) mbar_init(&ms.gbar[b], 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ss.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  build_segments<kG1>(mp.g1, ss);
+  if (threadIdx.x == 0) {
+    ms.ntn1 = (mp.g1.N + 127) / 128;
+    ms.ntn2 = (mp.g2.N + kBN - 1) / kBN;
+    ms.nt1 = ss.total_tiles;
+    ms.nt2 = (ms.nt1 / ms.ntn1) * ms.ntn2;
+    ms.total = mp.NG + ms.nt1 + ms.nt2 + mp.NC;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem_base;
+  volatile int* abort = &ss.abort;
+  const int NG = mp.NG, nt1 = ms.nt1, nt2 = ms.nt2, total = ms.total;
+  const int e1 = NG + nt1, e2 = NG + nt1 + nt2;  // ends of the GEMM-1 and GEMM-2 ticket ranges
+  constexpr int kW = 0x0F << 24;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mp.g1.tmA0);
+      tma_prefetch_desc(&mp.g1.tmB0);
+      tma_prefetch_desc(&mp.g2.tmA0);
+      tma_prefetch_desc(&mp.g2.tmB0);
+      ProducerState ps;
+      GatherState gs;
+      int slot = 0;
+      uint32_t tph = 0;
+      while (!*abort) {
+        if (!mbar_wait(&ms.tq_empty[slot], tph ^ 1, abort, err, kW | (1 << 20))) break;
+        const int id = atomicAdd(&mp.ctr[0], 1);
+        ms.tq[slot] = id;
+        mbar_arrive(&ms.tq_full[slot]);
+        if (++slot == kTq) {
+          slot = 0;
+          tph ^= 1;
+        }
+        if (id >= total) break;
+        if (id == mp.skip) continue;
+        const int where = kW | (1 << 20) | (id & 0xFFFFF);
+        if (id < NG) {
+          if (!gather_task(mp, ms, smem, id, gs, abort, where)) break;
+        } else if (id < e1) {
+          const TileInfo t = decode_tile<kG1>(mp.g1, ss, id - NG);
+          if (!t.shared) {  // routed rows come from Xp: wait for their gather blocks
+            const int g0 = t.grow0 / kGatherRows, g1 = (t.grow0 + t.rows - 1) / kGatherRows;
+            bool ok = true;
+            for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], 1, abort, err, where);
+            if (!ok) break;
+            fence_proxy_async_global();
+          }
+          if (!produce_tile<kG1>(mp.g1, t, ss, smem, ps, abort, where)) break;
+        } else if (id < e2) {
+          const int t2 = id - e1;
+          const int mt = t2 / ms.ntn2;
+          if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], 4 * ms.ntn1, abort, err, where)) break;
+          fence_proxy_async_global();
+          if (!produce_tile<kG2>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
+        }
+      }
+      if (*abort) {
+        producer_drain(ss, ps);
+        gather_drain(ms, gs);
+      }
+    }
+  } else if (warp == 1) {
+    MmaState mst;
+    int slot = 0;
+    uint32_t tph = 0;
+    while (true) {
+      if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (2 << 20))) break;
+      const int id = ms.tq[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.tq_empty[slot]);
+      if (++slot == kTq) {
+        slot = 0;
+        tph ^= 1;
+      }
+      if (id >= total) break;
+      if (id == mp.skip) continue;
+      const int where = kW | (2 << 20) | (id & 0xFFFFF);
+      bool ok = true;
+      if (id >= NG && id < e1)
+        ok = mma_tile<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
+      else if (id >= e1 && id < e2)
+        ok = mma_tile<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
+      if (!ok) break;
+    }
+    if (*abort) mma_drain(ss, mst);
+  } else {
+    int it = 0, slot = 0;
+    uint32_t tph = 0;
+    while (true) {
+      if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (3 << 20))) break;
+      const int id = ms.tq[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms.tq_empty[slot]);
+      if (++slot == kTq) {
+        slot = 0;
+        tph ^= 1;
+      }
+      if (id >= total) break;
+      if (id == mp.skip) continue;
+      const int where = kW | (3 << 20) | (id & 0xFFFFF);
+      if (id >= NG && id < e1) {
+        const int t1 = id - NG;
+        if (!epilogue_step<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, t1), ss, tmem, it, abort, where)) break;
+        warp_signal(&mp.ctr[kCtrXp + NG + t1 / ms.ntn1]);
+      } else if (id >= e1 && id < e2) {
+        if (!epilogue_step<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, tmem, it, abort, where)) break;
+        warp_signal(&mp.ctr[1]);
+      } else if (id >= e2) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_counter(&mp.ctr[1], 4 * nt2, abort, err, where);
+          __threadfence();
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+        combine_warp(mp, id - e2);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint16_t* x, const uint16_t* W1,
+                   const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* y, int grid, cudaStream_t s) {
+  GemmArgs a{};
+  a.T = c.T;
+  a.d = c.d_model;
+  a.f = c.d_ff;
+  a.E = c.E;
+  a.k = c.k;
+  a.S = c.n_shared;
+  a.offsets = reinterpret_cast<const int32_t*>(ws + L.offsets);
+  a.row_slot = reinterpret_cast<const int32_t*>(ws + L.row_slot);
+  a.topk_w = topk_w;
+  a.Xp = reinterpret_cast<const uint16_t*>(ws + L.Xp);
+  a.x = x;
+  a.W1 = W1;
+  a.W3 = W3;
+  a.W2 = W2;
+  a.H = reinterpret_cast<const uint16_t*>(ws + L.H);
+  a.H_out = reinterpret_cast<uint16_t*>(ws + L.H);
+  a.AB_out = reinterpret_cast<uint16_t*>(ws + L.AB);
+  a.Op_out = reinterpret_cast<float*>(ws + L.Op);
+  a.err = reinterpret_cast<int*>(ws + L.err);
+  MegaParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  if (!fill_params<kG1>(a, mp.g1) || !fill_params<kG2>(a, mp.g2)) return MOE_ERR_CUDA;
+  const long long R = static_cast<long long>(c.T) * c.k;
+  mp.x = x;
+  mp.row_token = reinterpret_cast<const int32_t*>(ws + L.row_token);
+  mp.dest = reinterpret_cast<const int32_t*>(ws + L.dest);
+  mp.Xp = reinterpret_cast<uint16_t*>(ws + L.Xp);
+  mp.Op = reinterpret_cast<const float*>(ws + L.Op);
+  mp.y = y;
+  mp.ctr = reinterpret_cast<int*>(ws + L.mk);
+  mp.NG = ceil_div(R, kGatherRows);
+  mp.NC = ceil_div(c.T, kCombineTokens);
+  mp.skip = g_skip_ticket;
+  // counters: kCtrXp + NG gather flags + (at most R/128 + E + S*ceil(T/128)) m-tiles
+  const long long need = kCtrXp + mp.NG + R / kBM + c.E + static_cast<long long>(c.n_shared) * ceil_div(c.T, kBM) + 2;
+  if (need > L.mk_ints) return MOE_ERR_SHAPE;
+  if (cudaMemsetAsync(mp.ctr, 0, sizeof(int) * L.mk_ints, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaFuncSetAttribute(mega_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaSmemBytes) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  TraceScope trace_scope(MOE_K_MEGAKERNEL, s);
+  mega_fwd_kernel<<<grid > 0 ? grid : num_sms(), kThreads, kMegaSmemBytes, s>>>(mp);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe
+
+extern "C" int moe_debug_skip_megakernel_task(int ticket) {
+  moe::g_skip_ticket = ticket >= 0 ? ticket : -1;
+  return MOE_OK;
+}

@@ -56,6 +56,7 @@ _SIGS = {
     "moe_get_device_error": ([_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "moe_num_sms": ([], _I),
     "moe_set_grid_limit": ([_I], _I),
+    "moe_debug_skip_megakernel_task": ([_I], _I),
     "moe_trace_enable": ([_I], _I),
     "moe_trace_reset": ([], _I),
     "moe_trace_read": ([_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
@@ -183,6 +184,10 @@ def moe_num_sms() -> int:
 
 def moe_set_grid_limit(n: int):
     _call("moe_set_grid_limit", int(n))
+
+
+def moe_debug_skip_megakernel_task(ticket: int):
+    _call("moe_debug_skip_megakernel_task", int(ticket))
 
 
 def moe_trace_enable(on: bool):

@@ -243,6 +243,14 @@ enum {
   MOE_K_MEGAKERNEL = 16,  /* forward MegaKernel */
   MOE_K_COUNT = 17
 };
+/* Testing aid for failure detection (no device fault involved): the forward
+ * MegaKernel claims task `ticket` but never runs or signals it, so the
+ * tasks that depend on it run into their bounded waits; the kernel then
+ * records MOE_ERR_TIMEOUT in the device error word and returns, and the
+ * CUDA context stays usable.  ticket < 0 disables it (the default).
+ * Process-wide, not thread-safe; never set in normal use. */
+int moe_debug_skip_megakernel_task(int ticket);
+
 int moe_trace_enable(int on);
 int moe_trace_reset(void);
 int moe_trace_read(int kind, double* total_ms, int* launches);

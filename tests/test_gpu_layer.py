@@ -83,6 +83,56 @@ def test_b_and_w_parts_split():
         assert torch.equal(full[k], part[k]), k
 
 
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_megakernel_bitwise_equals_kernel_chain(cfg):
+    """The single-launch forward equals the unfused kernel chain bit for bit
+    (every output and every activation saved for the backward)."""
+    g = to_dev(make_layer_inputs(cfg, seed=15))
+    a, wsa = run_layer(cfg, g, use_megakernel=0)
+    b, wsb = run_layer(cfg, g, use_megakernel=1, fill=float("nan"))
+    assert device_error(wsb) == (0, 0)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    for name in ("Xp", "H", "AB", "Op"):
+        assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
+
+
+def test_megakernel_does_not_depend_on_grid_size():
+    cfg = WIDE
+    g = to_dev(make_layer_inputs(cfg, seed=16))
+    ref = _digest(run_layer(cfg, g, use_megakernel=0)[0])
+    try:
+        for n in (1, 7, 0):
+            moe.moe_set_grid_limit(n)
+            assert _digest(run_layer(cfg, g, use_megakernel=1)[0]) == ref, n
+    finally:
+        moe.moe_set_grid_limit(0)
+
+
+def test_megakernel_wait_timeout_is_reported_and_context_survives():
+    """A task that never completes (set on the host) makes its dependants'
+    bounded waits run out: the kernel returns MOE_ERR_TIMEOUT through the
+    device error word, and the next launches on the same context work."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=17))
+    first_gemm1_ticket = -(-cfg.R // 128)  # gather tasks come first, 128 rows each
+    ws = moe.alloc_workspace(cfg, DEV)
+    out = {k: v for k, v in run_layer(cfg, g, ws=ws, use_megakernel=0)[0].items()}
+    try:
+        moe.moe_debug_skip_megakernel_task(first_gemm1_ticket)
+        moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["topk_idx"],
+                          out["topk_w"], ws, use_megakernel=1)
+        code, info = device_error(ws)
+    finally:
+        moe.moe_debug_skip_megakernel_task(-1)
+    assert code == moe.MOE_ERR_TIMEOUT, (code, info)
+    ref, _ = run_layer(cfg, g, use_megakernel=0)
+    again, ws2 = run_layer(cfg, g, use_megakernel=1)
+    assert device_error(ws2) == (0, 0)
+    for k in ref:
+        assert torch.equal(ref[k], again[k]), k
+
+
 @pytest.mark.slow
 def test_full_size_sampled_parity():
     """The benchmark workload (DeepSeek-V2-Lite-like layer: T=8192, d=2048,
