@@ -52,6 +52,23 @@ def dist_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's `value` (the slowest replica sets the
+    time); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_per_step / 1000.0)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -264,12 +281,8 @@ def run_ours(args):
     clocks = sampler.stop()
     moe.moe_trace_enable(False)
     trace = moe.moe_trace_read()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = cfg.T * world / (ms / 1000.0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    value = job_tokens_per_s(cfg.T, world, ms)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -295,12 +308,8 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": cfg.T * world / (ems / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+        e2e = {"value": job_tokens_per_s(cfg.T, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
     code, info = moe.moe_get_device_error(ws)

@@ -156,6 +156,21 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
   return MOE_OK;
 }
 
+int moe_token_addresses(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* rank_base, int32_t* counts,
+                        int32_t* offsets, int32_t* dest, void* ws, void* stream) {
+  MOE_TRY(check_cfg(cfg));
+  MOE_TRY(check_ptrs({topk_idx, counts, offsets, dest}, {rank_base}, ws));
+  const WsLayout L = ws_layout(*cfg);
+  const moe_cfg& c = *cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* base = at<int32_t>(ws, L.base);
+  MOE_TRY_CUDA(launch_hist(topk_idx, c.T, c.E, c.k, at<int32_t>(ws, L.hist), L.nb_route, at<int>(ws, L.err), s));
+  MOE_TRY_CUDA(launch_scan(at<int32_t>(ws, L.hist), c.E, L.nb_route, c.T * c.k, base, counts, offsets, s));
+  if (rank_base) MOE_TRY_CUDA(launch_rebase(base, offsets, rank_base, c.E, L.nb_route, s));
+  MOE_TRY_CUDA(launch_scatter(topk_idx, base, c.T, c.E, c.k, L.nb_route, dest, nullptr, nullptr, s));
+  return MOE_OK;
+}
+
 int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x, const int32_t* offsets,
                           const int32_t* row_slot, const float* topk_w, const uint16_t* W1, const uint16_t* W3,
                           const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime, void* ws, void* stream) {

@@ -17,6 +17,9 @@ cudaError_t launch_scan(const int32_t* hist, int E, int nb, int R, int32_t* base
                         int32_t* offsets, cudaStream_t s);
 cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, int E, int k, int nb,
                            int32_t* dest, int32_t* row_token, int32_t* row_slot, cudaStream_t s);
+// base[e*nb + b] += rank_base[e] - offsets[e] (multi-rank token mapping).
+cudaError_t launch_rebase(int32_t* base, const int32_t* offsets, const int32_t* rank_base, int E, int nb,
+                          cudaStream_t s);
 // dst[r] = src[idx[r]] for r < nrows, rows of `d` bf16 (zero row if the
 // index is outside [0, nsrc)).
 cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,

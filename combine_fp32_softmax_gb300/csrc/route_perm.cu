@@ -256,10 +256,22 @@ __global__ void __launch_bounds__(256)
     if (valid) {
       const size_t i = slot0 + il;
       dest[i] = r;
-      row_token[r] = static_cast<int>(i / k);
-      row_slot[r] = static_cast<int>(i);
+      if (row_token) {  // inverse tables only when the addresses are local rows
+        row_token[r] = static_cast<int>(i / k);
+        row_slot[r] = static_cast<int>(i);
+      }
     }
   }
+}
+
+// Moves every block base of expert e from the local segment start
+// offsets[e] to the rank's global base rank_base[e] (multi-rank mapping).
+__global__ void rebase_kernel(int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                              const int32_t* __restrict__ rank_base, int E, int nb) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= E * nb) return;
+  const int e = i / nb;
+  base[i] += rank_base[e] - offsets[e];
 }
 
 // dst[r] = src[idx[r]]: one warp per row, 16-byte vectors, 4 in flight per
@@ -440,6 +452,13 @@ cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, 
                            int32_t* row_token, int32_t* row_slot, cudaStream_t s) {
   TraceScope trace_scope(MOE_K_SCATTER, s);
   scatter_kernel<<<nb, 256, 0, s>>>(topk_idx, base, T, E, k, nb, dest, row_token, row_slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rebase(int32_t* base, const int32_t* offsets, const int32_t* rank_base, int E, int nb,
+                          cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_SCAN, s);
+  rebase_kernel<<<ceil_div(static_cast<long long>(E) * nb, 256), 256, 0, s>>>(base, offsets, rank_base, E, nb);
   return cudaGetLastError();
 }
 

@@ -99,6 +99,20 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
                  int32_t* row_token, int32_t* row_slot, uint16_t* Xp,
                  void* ws, void* stream);
 
+/* Multi-rank form of the token mapping (UniEP page, section 2.2,
+ * Algorithm 1): this rank's slots get addresses
+ *   dest[t*k+j] = rank_base[e] + (stable rank of slot t*k+j among this
+ *                 rank's slots routed to e),   e = topk_idx[t*k+j],
+ * where rank_base[e] (device, [E]) is the start of expert e's segment in its
+ * owner's receive buffer plus the slots that lower ranks send to e -- the
+ * prefix sums over the all-gathered per-rank counts.  counts [E] and
+ * offsets [E+1] receive this rank's own counts and their exclusive scan
+ * (the values to all-gather).  rank_base = NULL gives the single-rank
+ * mapping (dest equals moe_dispatch's).  Uses the histogram scratch of ws
+ * only. */
+int moe_token_addresses(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* rank_base,
+                        int32_t* counts, int32_t* offsets, int32_t* dest, void* ws, void* stream);
+
 /* Expert FFN as two grouped GEMMs over the ragged expert segments
  * (UniEP page, section 1.1 "GroupGEMM -> SwiGLU -> GroupGEMM"; padding-free
  * grouped GEMM with per-segment pointer arithmetic, section 2.2).
