@@ -24,8 +24,10 @@ __device__ __forceinline__ void record_error(int* err, int code, int info) {
 }
 #endif
 
-// Router / permutation: tokens per block.
-constexpr int kRouteTokensPerBlock = 256;
+// Router / permutation: tokens per block (8 warps x 4 tokens).  Small blocks
+// give the latency-bound router enough warps; the per-block histogram the
+// scan walks has E * ceil(T / 32) entries.
+constexpr int kRouteTokensPerBlock = 32;
 
 // Grouped GEMM tile: 128 rows x 256 accumulator columns, K staged 64 at a
 // time (one 128-byte swizzle atom of bf16).
@@ -79,7 +81,7 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.dAB = take(2 * Rs * 2 * f);
   L.Hw = take(2 * Rs * f);
   L.dXp = take(4 * Rs * d);
-  L.partial = take(4 * R * L.nt_dh);
+  L.partial = take(4 * R * L.nt_dh * 2);  // one partial dot per (row, column tile, column half)
   L.dw = take(4 * T * k);
   L.mk = take(sizeof(int) * L.mk_ints);
   L.total = o;

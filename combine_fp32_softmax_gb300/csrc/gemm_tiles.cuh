@@ -46,7 +46,8 @@ constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kBoxBytes = 64 * 64 * 2;          // one MN-major box: 64 x 64 bf16
 constexpr int kMaxSeg = 256 + 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two epilogue warps per TMEM lane quadrant, one per half of the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 
 struct GemmParams {
@@ -248,7 +249,8 @@ __device__ __forceinline__ void store_zero_f32x32(float* dst) {
 
 // Epilogue of one tile for the thread owning tile row `row` (TMEM lane).
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, int row, uint32_t tacc) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, int row, int half,
+                                              uint32_t tacc) {
   if constexpr (KIND == kG1) {
     // Columns [0,128) hold a (gate), [128,256) hold b (up) for outputs n0..n0+127.
     const bool ok = row < t.rows;
@@ -256,7 +258,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     uint16_t* H = static_cast<uint16_t*>(p.out0);
     uint16_t* AB = static_cast<uint16_t*>(p.out1);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 2 * half; c < 2 * half + 2; ++c) {
       const int n = t.n0 + 32 * c;
       if (n >= p.f) break;
       uint32_t a[32], b[32];
@@ -301,7 +303,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       if (ok && !t.shared) w = p.topk_w[p.row_slot[grow]];
     float* out = static_cast<float*>(p.out0);
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       const int n = t.n0 + 32 * c;
       if (n >= p.d) break;
       uint32_t v[32];
@@ -318,7 +320,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     uint16_t* Hw = static_cast<uint16_t*>(p.out1);
     float dot = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       const int n = t.n0 + 32 * c;
       if (n >= p.f) break;
       uint32_t g[32];
@@ -364,14 +366,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         }
       }
     }
-    if (ok && !t.shared) p.out_partial[grow * p.nt_dh + t.n0 / kBN] = dot;
+    if (ok && !t.shared) p.out_partial[(grow * p.nt_dh + t.n0 / kBN) * 2 + half] = dot;
   } else if constexpr (KIND == kDW13) {
     // Output row m of the stacked [dW1_e ; dW3_e] (2f rows), columns n (d).
     const int m = t.m0 + row;
     float* out = (m < p.f) ? static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.f + m) * p.d
                            : static_cast<float*>(p.out1) + (static_cast<size_t>(t.seg) * p.f + (m - p.f)) * p.d;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       const int n = t.n0 + 32 * c;
       if (n >= p.d) break;
       if (t.nkb == 0) {
@@ -388,7 +390,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const bool ok = m < p.d;
     float* out = static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.d + m) * p.f;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       const int n = t.n0 + 32 * c;
       if (n >= p.f) break;
       if (t.nkb == 0) {
@@ -449,7 +451,7 @@ __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
   }
   for (int a = 0; a < 2; ++a) {
     mbar_init(&ss.tfull[a], 1);
-    mbar_init(&ss.tempty[a], 4);
+    mbar_init(&ss.tempty[a], kEpiWarps);
   }
   mbar_init(&ss.drain, 1);
   ss.abort = 0;
@@ -566,7 +568,8 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   ++it;
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
   tc_fence_after();
-  epilogue_tile<KIND>(p, t, q * 32 + lane, tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN);
+  const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the accumulator
+  epilogue_tile<KIND>(p, t, q * 32 + lane, half, tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN);
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&ss.tempty[acc]);

@@ -1,14 +1,16 @@
 // Persistent grouped GEMM over ragged expert segments on tcgen05 tensor cores
 // (one kernel per GEMM kind; the tile machinery is in gemm_tiles.cuh).
 //
-// Design (one CTA per SM, 192 threads):
+// Design (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //               (256 x 64) into a 4-stage shared-memory ring (48 KB/stage).
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma
 //               (M=128, N=256, K=16, bf16 -> fp32) from one lane, commits
 //               to mbarriers; a ragged-K tail is zeroed in shared memory.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
-//               thread = one output row), fused elementwise work, stores.
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
+//               thread = one output row; two warps per lane quadrant, each
+//               owning half of the 256 columns), fused elementwise work,
+//               stores.
 //   The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 //   epilogue of tile i overlaps the main loop of tile i+1.
 // Tiles are taken in a static round-robin over CTAs; every output element is

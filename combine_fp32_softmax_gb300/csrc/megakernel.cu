@@ -169,8 +169,8 @@ __device__ void combine_warp(const MegaParams& mp, int c) {
   const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R;
   const int nr = k + S, nvec = mp.g1.d / 4;
   const float4* rows = reinterpret_cast<const float4*>(mp.Op);
-  for (int i = 0; i < kCombineTokens / 4; ++i) {
-    const int t = c * kCombineTokens + ew * (kCombineTokens / 4) + i;
+  for (int i = 0; i < kCombineTokens / kEpiWarps; ++i) {
+    const int t = c * kCombineTokens + ew * (kCombineTokens / kEpiWarps) + i;
     if (t >= T) break;
     long long myrow = 0;
     if (lane < k)
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
     init_gemm_barriers(ss);
     for (int q = 0; q < kTq; ++q) {
       mbar_init(&ms.tq_full[q], 1);
-      mbar_init(&ms.tq_empty[q], 5);  // MMA warp + 4 epilogue warps
+      mbar_init(&ms.tq_empty[q], 1 + kEpiWarps);  // MMA warp + epilogue warps
     }
     for (int b = 0; b < kStages; ++b) mbar_init(&ms.gbar[b], 1);
     fence_mbar_init();
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
         } else if (id < e2) {
           const int t2 = id - e1;
           const int mt = t2 / ms.ntn2;
-          if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], 4 * ms.ntn1, abort, err, where)) break;
+          if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kEpiWarps * ms.ntn1, abort, err, where)) break;
           fence_proxy_async_global();
           if (!produce_tile<kG2>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
         }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       } else if (id >= e2) {
         bool ok = true;
         if (lane == 0) {
-          ok = wait_counter(&mp.ctr[1], 4 * nt2, abort, err, where);
+          ok = wait_counter(&mp.ctr[1], kEpiWarps * nt2, abort, err, where);
           __threadfence();
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;

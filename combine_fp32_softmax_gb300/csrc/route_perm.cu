@@ -209,11 +209,13 @@ __global__ void __launch_bounds__(1024)
   if (tid == 0) offsets[E] = R;
 }
 
-// Stable in-block ranks.  Warp w owns tokens [32w, 32w+32) of the block, i.e.
-// a contiguous run of 32*k flat slots, visited in k rounds of 32.  Pass 1
+// Stable in-block ranks.  Warp w owns tokens [TPW*w, TPW*w+TPW) of the block,
+// i.e. a contiguous run of TPW*k flat slots, visited in rounds of 32.  Pass 1
 // counts per (warp, expert); a prefix over warps (starting at the block's
 // global base) gives each warp's first address per expert; pass 2 ranks each
 // slot among equal-expert lanes of its round (match mask) and advances.
+constexpr int kScatterTPW = kRouteTokensPerBlock / 8;  // tokens per warp
+
 __global__ void __launch_bounds__(256)
     scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, int T, int E, int k,
                    int nb, int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
@@ -224,10 +226,12 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   const size_t slot0 = static_cast<size_t>(b) * kRouteTokensPerBlock * k;
   const int nslot = (min(T, (b + 1) * kRouteTokensPerBlock) - b * kRouteTokensPerBlock) * k;
-  const int wslot0 = w * 32 * k;
-  for (int rnd = 0; rnd < k; ++rnd) {
+  const int wslots = kScatterTPW * k;
+  const int wslot0 = w * wslots;
+  const int rounds = (wslots + 31) / 32;
+  for (int rnd = 0; rnd < rounds; ++rnd) {
     const int il = wslot0 + rnd * 32 + lane;
-    const bool valid = il < nslot;
+    const bool valid = rnd * 32 + lane < wslots && il < nslot;
     const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     if (valid && lane == __ffs(peers) - 1) wrun[w][e] += __popc(peers);
@@ -244,9 +248,9 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
-  for (int rnd = 0; rnd < k; ++rnd) {
+  for (int rnd = 0; rnd < rounds; ++rnd) {
     const int il = wslot0 + rnd * 32 + lane;
-    const bool valid = il < nslot;
+    const bool valid = rnd * 32 + lane < wslots && il < nslot;
     const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int r = valid ? wrun[w][e] + __popc(peers & lt) : 0;
