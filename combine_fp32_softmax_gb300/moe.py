@@ -46,6 +46,7 @@ _SIGS = {
     "moe_route": ([_CFG, _P, _P, _P, _P, _P], _I),
     "moe_dispatch": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_token_addresses": ([_CFG] + [_P] * 7, _I),
+    "moe_dispatch_noalloc": ([_CFG] + [_P] * 9, _I),
     "moe_group_gemm_swiglu": ([_CFG] + [_P] * 13, _I),
     "moe_combine": ([_CFG, _P, _P, _P, _P, _P], _I),
     "moe_layer_fwd": ([_CFG] + [_P] * 9 + [_I, _P], _I),
@@ -129,6 +130,11 @@ def moe_route(cfg, logits, topk_idx, topk_w, ws, stream=None):
 def moe_dispatch(cfg, topk_idx, x, counts, offsets, dest, row_token, row_slot, Xp, ws, stream=None):
     _call("moe_dispatch", _cfg(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(dest),
           _ptr(row_token), _ptr(row_slot), _ptr(Xp), _ptr(ws), _stream(stream))
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, counts, offsets, dest, row_token, row_slot, Xp, stream=None):
+    _call("moe_dispatch_noalloc", _cfg(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(dest),
+          _ptr(row_token), _ptr(row_slot), _ptr(Xp), _stream(stream))
 
 
 def moe_token_addresses(cfg, topk_idx, rank_base, counts, offsets, dest, ws, stream=None):

@@ -99,6 +99,30 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
                  int32_t* row_token, int32_t* row_slot, uint16_t* Xp,
                  void* ws, void* stream);
 
+/* moe_dispatch for callers that cannot provide a workspace (no counterpart
+ * on the pages: a deployment variant of moe_dispatch).  Some callers may not
+ * allocate device memory while they run -- e.g. a framework operator
+ * registered with a zero-byte workspace, or code whose device memory a host
+ * framework planned in advance -- so they cannot give the library `ws`.
+ * This entry point computes exactly what moe_dispatch computes (same
+ * arguments minus ws; Xp gathered when x and Xp are both non-NULL), but
+ * keeps its scratch (expert histogram, block bases, error word) in a 4 MiB
+ * array inside the library, held by every GPU that loads it until exit.
+ * It allocates nothing and calls no allocating routine.
+ *  - Limit: E * ceil(T / 32) <= 524,256 (e.g. 64 experts and 262,144
+ *    tokens); larger shapes return MOE_ERR_SHAPE before any work.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents:
+ *    two calls whose work can overlap on the GPU (e.g. issued on different
+ *    streams with no ordering between them) race and produce wrong tables;
+ *    order them on one stream or with events.
+ *  - Out-of-range expert indices are clamped as in moe_dispatch; the error
+ *    record stays inside the array (there is no workspace to read it from). */
+int moe_dispatch_noalloc(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
+                         int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* row_token,
+                         int32_t* row_slot, uint16_t* Xp, void* stream);
+
 /* Multi-rank form of the token mapping (UniEP page, section 2.2,
  * Algorithm 1): this rank's slots get addresses
  *   dest[t*k+j] = rank_base[e] + (stable rank of slot t*k+j among this
