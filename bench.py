@@ -238,14 +238,24 @@ def run_ours(args):
                dW1=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
                dW3=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
                dW2=torch.empty(nexp, cfg.d, cfg.f, dtype=f32, device=dev))
-    mk = args.megakernel
-    if mk < 0:  # probe: the MegaKernel is used when the library provides it
-        try:
+    def fwd_ms(use_mk, iters=5):
+        """Device time of the forward alone (kernel chain or MegaKernel)."""
+        for _ in range(2):
             moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
-                              ws, use_megakernel=1)
-            mk = 1
-        except moe.MoeError:
-            mk = 0
+                              ws, use_megakernel=use_mk)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
+                              ws, use_megakernel=use_mk)
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / iters
+
+    fwd_times = {"chain": fwd_ms(0), "megakernel": fwd_ms(1)}
+    mk = args.megakernel
+    if mk < 0:  # the faster forward of the two (same bits either way)
+        mk = 1 if fwd_times["megakernel"] < fwd_times["chain"] else 0
 
     def step(src=g):
         moe.moe_layer_fwd(cfg, src["logits"], src["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
@@ -346,7 +356,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg, mk),
             "e2e": e2e, "gpu_launches": int(sum(v[1] for v in trace.values())),
             "roofline": roof, "clocks": clocks,
-            "gemm_tflops_all": all_gemm_tflops, "kernels": kernels}
+            "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "kernels": kernels}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)

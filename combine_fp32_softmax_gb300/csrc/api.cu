@@ -264,7 +264,7 @@ int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint1
   a.dW2_out = dW2;
   if (which & 1) {
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
-    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, c.T * c.k, 2 * L.nt_dh, dw, s));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, c.T * c.k, L.nt_dh, dw, s));
     MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
   }
   if (which & 2) {
@@ -338,7 +338,7 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
   if (which & 1) {  // B part: input gradients (critical path)
     MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, R, c.d_model, G, MOE_K_COMBINE_BWD, s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
-    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, 2 * L.nt_dh, dw, s));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
     MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
     MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
     MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, s));

@@ -81,7 +81,7 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.dAB = take(2 * Rs * 2 * f);
   L.Hw = take(2 * Rs * f);
   L.dXp = take(4 * Rs * d);
-  L.partial = take(4 * R * L.nt_dh * 2);  // one partial dot per (row, column tile, column half)
+  L.partial = take(4 * R * L.nt_dh);  // one partial dot per (row, 256-column tile)
   L.dw = take(4 * T * k);
   L.mk = take(sizeof(int) * L.mk_ints);
   L.total = o;

@@ -1,6 +1,7 @@
 #pragma once
-// Tile machinery shared by the persistent grouped GEMM and the forward MegaKernel:
-// persistent grouped GEMM over ragged expert segments on tcgen05 tensor cores.
+// Tile machinery shared by the persistent grouped GEMM kernels and the
+// forward MegaKernel: grouped GEMM over ragged expert segments on tcgen05
+// tensor cores.
 //
 // The expert FFN of the MoE layer runs as GroupGEMM -> SwiGLU -> GroupGEMM
 // (UniEP page, "Unified Expert-Parallel MoE MegaKernel for LLM Training",
@@ -15,12 +16,18 @@
 //
 // Design (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
-//               (256 x 64) into a 4-stage shared-memory ring (48 KB/stage).
+//               (256 x 64) into a 3- or 4-stage shared-memory ring
+//               (48 KB/stage).
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma
 //               (M=128, N=256, K=16, bf16 -> fp32) from one lane, commits
 //               to mbarriers; a ragged-K tail is zeroed in shared memory.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
-//               thread = one output row), fused elementwise work, stores.
+//               thread = one output row), fused elementwise work, results
+//               staged through swizzled shared memory and written with TMA
+//               tensor stores (coalesced, asynchronous).  Warps whose 32
+//               rows are not all valid (a segment's last m-tile) store
+//               their valid rows directly.  The dH epilogue TMA-loads its
+//               elementwise inputs ([a|b], H) per warp, double-buffered.
 //   The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 //   epilogue of tile i overlaps the main loop of tile i+1.
 // Tiles are taken in a static round-robin over CTAs; every output element is
@@ -40,28 +47,30 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kBoxBytes = 64 * 64 * 2;          // one MN-major box: 64 x 64 bf16
 constexpr int kMaxSeg = 256 + 4;
-constexpr int kEpiWarps = 8;  // two epilogue warps per TMEM lane quadrant, one per half of the columns
+constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
+constexpr int kChunkBytes = 32 * 64;  // one staged chunk: 32 rows x 64 bytes (SW64)
 
 struct GemmParams {
-  CUtensorMap tmA0, tmA1, tmB0, tmB1;
+  CUtensorMap tmA0, tmA1, tmB0, tmB1;  // operands
+  CUtensorMap tmO0, tmO1;              // outputs written with TMA stores
+  CUtensorMap tmX0, tmX1;              // dH epilogue inputs: [a|b] and H
   int T, d, f, E, k, S, R;
-  int N;      // output columns per expert
-  int Mw;     // ragged-K kinds: output rows per expert
-  int K;      // ragged-M kinds: reduction length
-  int nt_dh;  // dH: column tiles per row (number of partial dot products)
+  int N;       // output columns per expert
+  int Mw;      // ragged-K kinds: output rows per expert
+  int K;       // ragged-M kinds: reduction length
+  int nt_dh;   // dH: column tiles per row (number of partial dot products)
+  int has_ab;  // GEMM 1: save [a|b]
   const int32_t* offsets;
   const int32_t* row_slot;
   const float* topk_w;
-  const uint16_t* aux_ab;
-  const uint16_t* aux_h;
   void* out0;
   void* out1;
   float* out_partial;
@@ -74,10 +83,16 @@ struct Traits {
   static constexpr bool B_MN = (KIND == kDH || KIND == kDX || KIND == kDW13 || KIND == kDW2);
   static constexpr bool RAGGED_K = (KIND == kDW13 || KIND == kDW2);
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
+  static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
+  // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two input buffers
+  // ([a, b, H] chunks) plus one output chunk of dA, dB, Hw; fp32 kinds two
+  // output chunks.
+  static constexpr int EPI_BYTES = (KIND == kG1) ? 3 * kChunkBytes : (KIND == kDH) ? 9 * kChunkBytes : 2 * kChunkBytes;
 };
 
 struct SharedState {
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
+  uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain;
+  uint64_t aux[kEpiWarps][2];  // dH epilogue input buffers of each warp
   uint32_t tmem_base;
   int abort;
   int nseg;
@@ -87,7 +102,11 @@ struct SharedState {
   int prefix[kMaxSeg + 1];
 };
 
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + static_cast<int>(sizeof(SharedState));
+template <int KIND>
+constexpr int smem_bytes() {
+  return 1024 + Traits<KIND>::STAGES * kStageBytes + kEpiWarps * Traits<KIND>::EPI_BYTES +
+         static_cast<int>(sizeof(SharedState));
+}
 
 struct TileInfo {
   int seg, m0, n0, rows, grow0, nkb;
@@ -234,218 +253,311 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&v)[32], float scale) {
-  float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    d4[i] = make_float4(scale * __uint_as_float(v[4 * i]), scale * __uint_as_float(v[4 * i + 1]),
-                        scale * __uint_as_float(v[4 * i + 2]), scale * __uint_as_float(v[4 * i + 3]));
-}
-__device__ __forceinline__ void store_zero_f32x32(float* dst) {
-  float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) d4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+__device__ __forceinline__ void tmem_ld_32x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
-// Epilogue of one tile for the thread owning tile row `row` (TMEM lane).
+// One row of a 32-row x 64-byte staging chunk in the TMA 64-byte swizzle
+// layout: 16-byte piece c of row r sits at piece c ^ ((r >> 1) & 3).  A
+// warp writing or reading one row per lane touches every bank once per
+// eight lanes (no bank conflicts).
+__device__ __forceinline__ void stage_row64(uint8_t* buf, int row, const uint32_t* w) {
+  const int sw = (row >> 1) & 3;
+  uint4* r = reinterpret_cast<uint4*>(buf + row * 64);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) r[c ^ sw] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+__device__ __forceinline__ void load_row64(const uint8_t* buf, int row, uint32_t* w) {
+  const int sw = (row >> 1) & 3;
+  const uint4* r = reinterpret_cast<const uint4*>(buf + row * 64);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = r[c ^ sw];
+    w[4 * c] = v.x;
+    w[4 * c + 1] = v.y;
+    w[4 * c + 2] = v.z;
+    w[4 * c + 3] = v.w;
+  }
+}
+// Direct (unstaged) store of 16 words: the fallback for rows of warps that
+// are only partly inside the segment.
+__device__ __forceinline__ void store_words16(void* dst, const uint32_t* w) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+// Per-epilogue-warp state carried across tiles.
+struct EpiState {
+  int it = 0;             // tiles done (TMEM buffer / phase)
+  uint32_t chunks = 0;    // staged chunks issued in the current tile
+  uint32_t auxn = 0;      // dH input chunks loaded so far (buffer = auxn & 1)
+  uint32_t auxpar = 0;    // next wait parity of each dH input buffer
+  uint32_t auxpend = 0;   // dH input buffers with a load in flight
+};
+
+// Staging helper: lane 0 waits until earlier chunks stopped reading the
+// buffer about to be rewritten.
+template <int MAX_PENDING>
+__device__ __forceinline__ void staging_reuse_wait(uint32_t chunks) {
+  if (chunks > MAX_PENDING) {
+    if ((threadIdx.x & 31) == 0) bulk_wait_read<MAX_PENDING>();
+    __syncwarp();
+  }
+}
+__device__ __forceinline__ void staging_publish() {
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// fp32 outputs (GEMM 2, dX, dW1/dW3, dW2): 16-column chunks, double-buffered.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, int row, int half,
-                                              uint32_t tacc) {
-  if constexpr (KIND == kG1) {
-    // Columns [0,128) hold a (gate), [128,256) hold b (up) for outputs n0..n0+127.
-    const bool ok = row < t.rows;
-    const size_t grow = static_cast<size_t>(t.grow0) + row;
-    uint16_t* H = static_cast<uint16_t*>(p.out0);
-    uint16_t* AB = static_cast<uint16_t*>(p.out1);
-#pragma unroll 1
-    for (int c = 2 * half; c < 2 * half + 2; ++c) {
-      const int n = t.n0 + 32 * c;
-      if (n >= p.f) break;
-      uint32_t a[32], b[32];
-      tmem_ld_32x32(tacc + 32 * c, a);
-      tmem_ld_32x32(tacc + 128 + 32 * c, b);
-      tmem_ld_wait();
-      if (ok) {
-        uint32_t hp[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a0 = __uint_as_float(a[2 * i]), a1 = __uint_as_float(a[2 * i + 1]);
-          const float b0 = __uint_as_float(b[2 * i]), b1 = __uint_as_float(b[2 * i + 1]);
-          const float h0 = a0 / (1.f + expf(-a0)) * b0;
-          const float h1 = a1 / (1.f + expf(-a1)) * b1;
-          hp[i] = pack_bf16(h0, h1);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(H + grow * p.f + n);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hp[4 * i], hp[4 * i + 1], hp[4 * i + 2], hp[4 * i + 3]);
-        if (AB) {
-          uint4* da = reinterpret_cast<uint4*>(AB + grow * 2 * p.f + n);
-          uint4* db = reinterpret_cast<uint4*>(AB + grow * 2 * p.f + p.f + n);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            da[i] = make_uint4(pack_bf16(__uint_as_float(a[8 * i]), __uint_as_float(a[8 * i + 1])),
-                               pack_bf16(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3])),
-                               pack_bf16(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5])),
-                               pack_bf16(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7])));
-            db[i] = make_uint4(pack_bf16(__uint_as_float(b[8 * i]), __uint_as_float(b[8 * i + 1])),
-                               pack_bf16(__uint_as_float(b[8 * i + 2]), __uint_as_float(b[8 * i + 3])),
-                               pack_bf16(__uint_as_float(b[8 * i + 4]), __uint_as_float(b[8 * i + 5])),
-                               pack_bf16(__uint_as_float(b[8 * i + 6]), __uint_as_float(b[8 * i + 7])));
-          }
-        }
-      }
-    }
-  } else if constexpr (KIND == kG2 || KIND == kDX) {
-    const bool ok = row < t.rows;
-    const size_t grow = static_cast<size_t>(t.grow0) + row;
-    float w = 1.f;
+__device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
+                                             uint8_t* stg, EpiState& es) {
+  const int lane = threadIdx.x & 31;
+  const int r = 32 * q + lane;  // tile row of this lane
+  const CUtensorMap* map = &p.tmO0;
+  int orow0;                    // tensor-map row of the warp's first row
+  float* optr;                  // this lane's output row (fallback path)
+  bool full, rowok;
+  float scale = 1.f;
+  int N;
+  if constexpr (KIND == kG2 || KIND == kDX) {
+    N = p.d;
+    rowok = r < t.rows;
+    full = t.rows >= 32 * q + 32;
+    const size_t grow = static_cast<size_t>(t.grow0) + r;
+    orow0 = t.grow0 + 32 * q;
+    optr = static_cast<float*>(p.out0) + grow * N;
     if constexpr (KIND == kG2)
-      if (ok && !t.shared) w = p.topk_w[p.row_slot[grow]];
-    float* out = static_cast<float*>(p.out0);
-#pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-      const int n = t.n0 + 32 * c;
-      if (n >= p.d) break;
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + 32 * c, v);
-      tmem_ld_wait();
-      if (ok) store_f32x32(out + grow * p.d + n, v, w);
-    }
-  } else if constexpr (KIND == kDH) {
-    const bool ok = row < t.rows;
-    const size_t grow = static_cast<size_t>(t.grow0) + row;
-    float w = 1.f;
-    if (ok && !t.shared) w = p.topk_w[p.row_slot[grow]];
-    uint16_t* dAB = static_cast<uint16_t*>(p.out0);
-    uint16_t* Hw = static_cast<uint16_t*>(p.out1);
-    float dot = 0.f;
-#pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-      const int n = t.n0 + 32 * c;
-      if (n >= p.f) break;
-      uint32_t g[32];
-      tmem_ld_32x32(tacc + 32 * c, g);
-      tmem_ld_wait();
-      if (ok) {
-        const uint4* pa = reinterpret_cast<const uint4*>(p.aux_ab + grow * 2 * p.f + n);
-        const uint4* pb = reinterpret_cast<const uint4*>(p.aux_ab + grow * 2 * p.f + p.f + n);
-        const uint4* ph = reinterpret_cast<const uint4*>(p.aux_h + grow * p.f + n);
-        uint4* oa = reinterpret_cast<uint4*>(dAB + grow * 2 * p.f + n);
-        uint4* ob = reinterpret_cast<uint4*>(dAB + grow * 2 * p.f + p.f + n);
-        uint4* oh = reinterpret_cast<uint4*>(Hw + grow * p.f + n);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 av = __ldg(pa + q), bv = __ldg(pb + q), hv = __ldg(ph + q);
-          const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-          const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-          uint32_t ra[4], rb[4], rh[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float dA2[2], dB2[2], hw2[2];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const float a = half ? bf16_hi(aw[u]) : bf16_lo(aw[u]);
-              const float b = half ? bf16_hi(bw[u]) : bf16_lo(bw[u]);
-              const float h = half ? bf16_hi(hw[u]) : bf16_lo(hw[u]);
-              const float graw = __uint_as_float(g[8 * q + 2 * u + half]);
-              dot += graw * h;
-              const float dH = w * graw;
-              const float s = 1.f / (1.f + expf(-a));
-              dA2[half] = dH * b * s * (1.f + a * (1.f - s));
-              dB2[half] = dH * (a * s);
-              hw2[half] = w * h;
-            }
-            ra[u] = pack_bf16(dA2[0], dA2[1]);
-            rb[u] = pack_bf16(dB2[0], dB2[1]);
-            rh[u] = pack_bf16(hw2[0], hw2[1]);
-          }
-          oa[q] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
-          ob[q] = make_uint4(rb[0], rb[1], rb[2], rb[3]);
-          oh[q] = make_uint4(rh[0], rh[1], rh[2], rh[3]);
-        }
-      }
-    }
-    if (ok && !t.shared) p.out_partial[(grow * p.nt_dh + t.n0 / kBN) * 2 + half] = dot;
+      if (rowok && !t.shared) scale = p.topk_w[p.row_slot[grow]];
   } else if constexpr (KIND == kDW13) {
-    // Output row m of the stacked [dW1_e ; dW3_e] (2f rows), columns n (d).
-    const int m = t.m0 + row;
-    float* out = (m < p.f) ? static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.f + m) * p.d
-                           : static_cast<float*>(p.out1) + (static_cast<size_t>(t.seg) * p.f + (m - p.f)) * p.d;
+    N = p.d;
+    const int mw0 = t.m0 + 32 * q;  // the warp's 32 rows all sit in dW1 or all in dW3 (f % 32 == 0)
+    const bool second = mw0 >= p.f;
+    map = second ? &p.tmO1 : &p.tmO0;
+    orow0 = t.seg * p.f + (second ? mw0 - p.f : mw0);
+    optr = static_cast<float*>(second ? p.out1 : p.out0) + (static_cast<size_t>(orow0) + lane) * N;
+    rowok = full = true;
+  } else {  // kDW2
+    N = p.f;
+    const int m = t.m0 + r;
+    rowok = m < p.d;
+    full = t.m0 + 32 * q + 32 <= p.d;
+    orow0 = t.seg * p.d + t.m0 + 32 * q;
+    optr = static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.d + m) * N;
+  }
+  const bool zero = Traits<KIND>::RAGGED_K && t.nkb == 0;  // empty expert: exact zeros
+  es.chunks = 0;
 #pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-      const int n = t.n0 + 32 * c;
-      if (n >= p.d) break;
-      if (t.nkb == 0) {
-        store_zero_f32x32(out + n);
-        continue;
-      }
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + 32 * c, v);
+  for (int j = 0; j < 16; ++j) {
+    const int n = t.n0 + 16 * j;
+    if (n >= N) break;
+    uint32_t v[16];
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0u;
+    } else {
+      tmem_ld_32x16(tacc + 16 * j, v);
       tmem_ld_wait();
-      store_f32x32(out + n, v, 1.f);
+      if constexpr (KIND == kG2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(scale * __uint_as_float(v[i]));
+      }
     }
-  } else {  // kDW2: output row m (d) of dW2_e, columns n (f)
-    const int m = t.m0 + row;
-    const bool ok = m < p.d;
-    float* out = static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.d + m) * p.f;
-#pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-      const int n = t.n0 + 32 * c;
-      if (n >= p.f) break;
-      if (t.nkb == 0) {
-        if (ok) store_zero_f32x32(out + n);
-        continue;
+    if (full) {
+      uint8_t* buf = stg + (es.chunks & 1) * kChunkBytes;
+      staging_reuse_wait<1>(es.chunks);
+      stage_row64(buf, lane, v);
+      staging_publish();
+      if (lane == 0) {
+        tma_store_2d(map, buf, n, orow0);
+        bulk_commit();
       }
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + 32 * c, v);
-      tmem_ld_wait();
-      if (ok) store_f32x32(out + n, v, 1.f);
+      ++es.chunks;
+    } else if (rowok) {
+      store_words16(optr + n, v);
     }
   }
 }
 
-// ------------------------------------------------------------------ host
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+// GEMM 1: columns [0,128) of the accumulator hold a (gate), [128,256) hold b
+// (up) for outputs n0..n0+127; H = bf16(silu(a) * b), optionally [a|b].
+__device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
+                                            uint8_t* stg, EpiState& es) {
+  const int lane = threadIdx.x & 31;
+  const int r = 32 * q + lane;
+  const bool rowok = r < t.rows, full = t.rows >= 32 * q + 32;
+  const size_t grow = static_cast<size_t>(t.grow0) + r;
+  const int orow0 = t.grow0 + 32 * q;
+  uint16_t* H = static_cast<uint16_t*>(p.out0);
+  uint16_t* AB = static_cast<uint16_t*>(p.out1);
+  es.chunks = 0;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    const int n = t.n0 + 32 * c;
+    if (n >= p.f) break;
+    uint32_t a[32], b[32];
+    tmem_ld_32x32(tacc + 32 * c, a);
+    tmem_ld_32x32(tacc + 128 + 32 * c, b);
+    tmem_ld_wait();
+    uint32_t hp[16], ap[16], bp[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float a0 = __uint_as_float(a[2 * i]), a1 = __uint_as_float(a[2 * i + 1]);
+      const float b0 = __uint_as_float(b[2 * i]), b1 = __uint_as_float(b[2 * i + 1]);
+      hp[i] = pack_bf16(a0 / (1.f + expf(-a0)) * b0, a1 / (1.f + expf(-a1)) * b1);
+      ap[i] = pack_bf16(a0, a1);
+      bp[i] = pack_bf16(b0, b1);
+    }
+    if (full) {
+      staging_reuse_wait<0>(es.chunks);
+      stage_row64(stg, lane, hp);
+      if (p.has_ab) {
+        stage_row64(stg + kChunkBytes, lane, ap);
+        stage_row64(stg + 2 * kChunkBytes, lane, bp);
+      }
+      staging_publish();
+      if (lane == 0) {
+        tma_store_2d(&p.tmO0, stg, n, orow0);
+        if (p.has_ab) {
+          tma_store_2d(&p.tmO1, stg + kChunkBytes, n, orow0);
+          tma_store_2d(&p.tmO1, stg + 2 * kChunkBytes, p.f + n, orow0);
+        }
+        bulk_commit();
+      }
+      ++es.chunks;
+    } else if (rowok) {
+      store_words16(H + grow * p.f + n, hp);
+      if (p.has_ab) {
+        store_words16(AB + grow * 2 * p.f + n, ap);
+        store_words16(AB + grow * 2 * p.f + p.f + n, bp);
+      }
+    }
   }
-  return fn;
 }
 
-// Row-major bf16 matrix [outer, inner] seen as 2D tiles of box_outer rows x
-// box_inner (= 64, one 128-byte swizzle span) columns; out-of-range reads
-// fill zeros.
-bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-           uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || !base || inner == 0 || outer == 0) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// dH: inputs a, b, H of the tile's 32-column chunks are TMA-loaded per warp
+// into two buffers (3 chunks of 2 KB each); outputs dA, dB, Hw are staged
+// in a third.
+__device__ __forceinline__ int dh_chunks(const GemmParams& p, const TileInfo& t) {
+  return min(8, (p.f - t.n0 + 31) / 32);
+}
+__device__ __forceinline__ void dh_issue_inputs(const GemmParams& p, const TileInfo& t, int q, int c, uint8_t* stg,
+                                                SharedState& ss, EpiState& es) {
+  const int buf = es.auxn & 1;
+  ++es.auxn;
+  if ((threadIdx.x & 31) == 0) {
+    uint8_t* in = stg + buf * 3 * kChunkBytes;
+    uint64_t* bar = &ss.aux[q][buf];
+    const int n = t.n0 + 32 * c, row0 = t.grow0 + 32 * q;
+    mbar_arrive_expect_tx(bar, 3 * kChunkBytes);
+    tma_load_2d(in, &p.tmX0, bar, n, row0);                    // a
+    tma_load_2d(in + kChunkBytes, &p.tmX0, bar, p.f + n, row0);  // b
+    tma_load_2d(in + 2 * kChunkBytes, &p.tmX1, bar, n, row0);  // H
+  }
+  es.auxpend |= 1u << buf;
+}
+// Issued before the tile's accumulator is ready so the loads overlap the wait.
+__device__ __forceinline__ void dh_prefetch(const GemmParams& p, const TileInfo& t, int q, uint8_t* stg,
+                                            SharedState& ss, EpiState& es) {
+  const int nch = dh_chunks(p, t);
+  dh_issue_inputs(p, t, q, 0, stg, ss, es);
+  if (nch > 1) dh_issue_inputs(p, t, q, 1, stg, ss, es);
 }
 
+__device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
+                                            uint8_t* stg, SharedState& ss, EpiState& es, volatile int* abort,
+                                            int where) {
+  const int lane = threadIdx.x & 31;
+  const int r = 32 * q + lane;
+  const bool rowok = r < t.rows, full = t.rows >= 32 * q + 32;
+  const size_t grow = static_cast<size_t>(t.grow0) + r;
+  const int orow0 = t.grow0 + 32 * q;
+  float w = 1.f;
+  if (rowok && !t.shared) w = p.topk_w[p.row_slot[grow]];
+  uint16_t* dAB = static_cast<uint16_t*>(p.out0);
+  uint16_t* Hw = static_cast<uint16_t*>(p.out1);
+  uint8_t* out = stg + 6 * kChunkBytes;
+  const int nch = dh_chunks(p, t);
+  const uint32_t first = es.auxn - (nch > 1 ? 2 : 1);  // input chunk index of chunk 0
+  float dot = 0.f;
+  es.chunks = 0;
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const int n = t.n0 + 32 * c;
+    const int buf = (first + c) & 1;
+    if (!mbar_wait(&ss.aux[q][buf], (es.auxpar >> buf) & 1, abort, p.err, where)) return false;
+    es.auxpar ^= 1u << buf;
+    es.auxpend &= ~(1u << buf);
+    uint32_t g[32];
+    tmem_ld_32x32(tacc + 32 * c, g);
+    tmem_ld_wait();
+    const uint8_t* in = stg + buf * 3 * kChunkBytes;
+    uint32_t aw[16], bw[16], hw[16];
+    load_row64(in, lane, aw);
+    load_row64(in + kChunkBytes, lane, bw);
+    load_row64(in + 2 * kChunkBytes, lane, hw);
+    // the buffer is free again: every lane has its row in registers
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (c + 2 < nch) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
+    uint32_t ra[16], rb[16], rh[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      float dA2[2], dB2[2], hw2[2];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float a = half ? bf16_hi(aw[u]) : bf16_lo(aw[u]);
+        const float b = half ? bf16_hi(bw[u]) : bf16_lo(bw[u]);
+        const float h = half ? bf16_hi(hw[u]) : bf16_lo(hw[u]);
+        const float graw = __uint_as_float(g[2 * u + half]);
+        dot += graw * h;
+        const float dH = w * graw;
+        const float s = 1.f / (1.f + expf(-a));
+        dA2[half] = dH * b * s * (1.f + a * (1.f - s));
+        dB2[half] = dH * (a * s);
+        hw2[half] = w * h;
+      }
+      ra[u] = pack_bf16(dA2[0], dA2[1]);
+      rb[u] = pack_bf16(dB2[0], dB2[1]);
+      rh[u] = pack_bf16(hw2[0], hw2[1]);
+    }
+    if (full) {
+      staging_reuse_wait<0>(es.chunks);
+      stage_row64(out, lane, ra);
+      stage_row64(out + kChunkBytes, lane, rb);
+      stage_row64(out + 2 * kChunkBytes, lane, rh);
+      staging_publish();
+      if (lane == 0) {
+        tma_store_2d(&p.tmO0, out, n, orow0);
+        tma_store_2d(&p.tmO0, out + kChunkBytes, p.f + n, orow0);
+        tma_store_2d(&p.tmO1, out + 2 * kChunkBytes, n, orow0);
+        bulk_commit();
+      }
+      ++es.chunks;
+    } else if (rowok) {
+      store_words16(dAB + grow * 2 * p.f + n, ra);
+      store_words16(dAB + grow * 2 * p.f + p.f + n, rb);
+      store_words16(Hw + grow * p.f + n, rh);
+    }
+  }
+  if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + t.n0 / kBN] = dot;
+  return true;
+}
 
 // ---------------------------------------------------------- per-tile roles
-// Shared by the grouped GEMM kernel and the MegaKernel, so a tile's MMA
+// Shared by the grouped GEMM kernels and the MegaKernel, so a tile's MMA
 // sequence and epilogue arithmetic are the same code in both.
 
 __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
-  for (int s = 0; s < kStages; ++s) {
+  for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&ss.full[s], 1);
     mbar_init(&ss.empty[s], 1);
   }
@@ -453,17 +565,21 @@ __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
     mbar_init(&ss.tfull[a], 1);
     mbar_init(&ss.tempty[a], kEpiWarps);
   }
+  for (int w = 0; w < kEpiWarps; ++w) {
+    mbar_init(&ss.aux[w][0], 1);
+    mbar_init(&ss.aux[w][1], 1);
+  }
   mbar_init(&ss.drain, 1);
   ss.abort = 0;
 }
 
-// Producer lane: every K block of one tile through the stage ring.
+// Producer lane: every K block of one tile through the NST-stage ring.
 struct ProducerState {
   int stage = 0;
   uint32_t phase = 0, filled = 0, fill_par = 0;
 };
 
-template <int KIND>
+template <int KIND, int NST>
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
                                              ProducerState& ps, volatile int* abort, int where) {
   for (int kb = 0; kb < t.nkb; ++kb) {
@@ -473,7 +589,7 @@ __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo
     issue_loads<KIND>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage]);
     ps.filled |= 1u << ps.stage;
     ps.fill_par = (ps.fill_par & ~(1u << ps.stage)) | (ps.phase << ps.stage);
-    if (++ps.stage == kStages) {
+    if (++ps.stage == NST) {
       ps.stage = 0;
       ps.phase ^= 1;
     }
@@ -483,18 +599,18 @@ __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo
 
 // Lets every copy the producer issued land before the CTA may exit.
 __device__ __forceinline__ void producer_drain(SharedState& ss, const ProducerState& ps) {
-  for (int s = 0; s < kStages; ++s)
+  for (int s = 0; s < kMaxStages; ++s)
     if (ps.filled & (1u << s)) mbar_wait_drain(&ss.full[s], (ps.fill_par >> s) & 1);
 }
 
-// MMA warp: one tile into TMEM accumulator buffer `acc`; lane 0 issues.
+// MMA warp: one tile into TMEM accumulator buffer `it & 1`; lane 0 issues.
 struct MmaState {
   int stage = 0, it = 0;
   uint32_t phase = 0;
   bool issued = false;
 };
 
-template <int KIND>
+template <int KIND, int NST>
 __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
                                          uint32_t tmem, MmaState& ms, volatile int* abort, int where) {
   using Tr = Traits<KIND>;
@@ -538,7 +654,7 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
       ms.issued = true;
     }
     __syncwarp();
-    if (++ms.stage == kStages) {
+    if (++ms.stage == NST) {
       ms.stage = 0;
       ms.phase ^= 1;
     }
@@ -557,23 +673,92 @@ __device__ __forceinline__ void mma_drain(SharedState& ss, const MmaState& ms) {
   __syncwarp();
 }
 
-// Epilogue warps (2..5): one tile out of TMEM buffer `it & 1`.
+// Epilogue warp (2..5): one tile out of TMEM buffer `es.it & 1`.  `stg` is
+// this warp's staging memory.  The TMEM buffer is released as soon as the
+// last accumulator load is done; the staged stores drain in the background
+// and are waited for (read side) before the staging memory is reused.
 template <int KIND>
 __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInfo& t, SharedState& ss, uint32_t tmem,
-                                              int& it, volatile int* abort, int where) {
+                                              uint8_t* stg, EpiState& es, volatile int* abort, int where) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are reachable from this warp
-  const int acc = it & 1;
-  const uint32_t aph = (it >> 1) & 1;
-  ++it;
+  const int acc = es.it & 1;
+  const uint32_t aph = (es.it >> 1) & 1;
+  ++es.it;
+  if constexpr (KIND == kDH) dh_prefetch(p, t, q, stg, ss, es);
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
   tc_fence_after();
-  const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the accumulator
-  epilogue_tile<KIND>(p, t, q * 32 + lane, half, tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN);
+  const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+  bool ok = true;
+  if constexpr (KIND == kG1)
+    epilogue_g1(p, t, q, tacc, stg, es);
+  else if constexpr (KIND == kDH)
+    ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where);
+  else
+    epilogue_f32<KIND>(p, t, q, tacc, stg, es);
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&ss.tempty[acc]);
-  return true;
+  if (ok && lane == 0) mbar_arrive(&ss.tempty[acc]);
+  if (lane == 0) bulk_wait_read<0>();  // staging memory free for the next tile
+  __syncwarp();
+  return ok;
+}
+
+// Before an epilogue warp may leave: its TMA stores complete and its
+// in-flight input loads landed.
+__device__ __forceinline__ void epilogue_drain(SharedState& ss, const EpiState& es) {
+  const int q = (threadIdx.x >> 5) & 3;
+  if ((threadIdx.x & 31) == 0) {
+    bulk_wait_all();
+    for (int b = 0; b < 2; ++b)
+      if (es.auxpend & (1u << b)) mbar_wait_drain(&ss.aux[q][b], (es.auxpar >> b) & 1);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ host
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Row-major matrix [outer, inner] of bf16 (esize 2) or fp32 (esize 4) seen
+// as 2D boxes of box_outer rows x box_inner elements; out-of-range reads
+// fill zeros and out-of-range parts of a stored box are skipped.
+bool map2d_any(CUtensorMap* m, const void* base, int esize, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base || inner == 0 || outer == 0) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * esize};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// Operand tiles: bf16, 64-element (128-byte) swizzled rows.
+bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  return map2d_any(m, base, 2, inner, outer, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Epilogue chunks: 32 rows x 64 bytes (32 bf16 or 16 fp32), 64-byte swizzle.
+bool map_chunk_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  return map2d_any(m, base, 2, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+bool map_chunk_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  return map2d_any(m, base, 4, inner, outer, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Tensor maps and pointers of one GEMM kind.
@@ -600,6 +785,9 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA1, alt(a.x, a.Xp), d, a.x ? T : R, 64, 128);
     ok &= map2d(&p.tmB0, a.W1, d, nexp * f, 64, 128);
     ok &= map2d(&p.tmB1, a.W3, d, nexp * f, 64, 128);
+    ok &= map_chunk_bf16(&p.tmO0, a.H_out, f, Rs);
+    p.has_ab = a.AB_out != nullptr;
+    if (p.has_ab) ok &= map_chunk_bf16(&p.tmO1, a.AB_out, 2 * f, Rs);
     p.N = a.f;
     p.K = a.d;
     p.out0 = a.H_out;
@@ -607,6 +795,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
   } else if constexpr (KIND == kG2) {
     ok &= map2d(&p.tmA0, a.H, f, Rs, 64, 128);
     ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 256);
+    ok &= map_chunk_f32(&p.tmO0, a.Op_out, d, Rs);
     p.N = a.d;
     p.K = a.f;
     p.out0 = a.Op_out;
@@ -614,10 +803,12 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA0, a.G, d, R, 64, 128);
     ok &= map2d(&p.tmA1, a.dy, d, T, 64, 128);
     ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 64);
+    ok &= map_chunk_bf16(&p.tmO0, a.dAB_out, 2 * f, Rs);
+    ok &= map_chunk_bf16(&p.tmO1, a.Hw_out, f, Rs);
+    ok &= map_chunk_bf16(&p.tmX0, a.AB, 2 * f, Rs);
+    ok &= map_chunk_bf16(&p.tmX1, a.H, f, Rs);
     p.N = a.f;
     p.K = a.d;
-    p.aux_ab = a.AB;
-    p.aux_h = a.H;
     p.out0 = a.dAB_out;
     p.out1 = a.Hw_out;
     p.out_partial = a.partial_out;
@@ -625,6 +816,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA0, a.dAB, 2 * f, Rs, 64, 128);
     ok &= map2d(&p.tmB0, a.W1, d, nexp * f, 64, 64);
     ok &= map2d(&p.tmB1, a.W3, d, nexp * f, 64, 64);
+    ok &= map_chunk_f32(&p.tmO0, a.dXp_out, d, Rs);
     p.N = a.d;
     p.K = 2 * a.f;
     p.out0 = a.dXp_out;
@@ -632,6 +824,8 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA0, a.dAB, 2 * f, Rs, 64, 64);
     ok &= map2d(&p.tmB0, a.Xp, d, R, 64, 64);
     ok &= map2d(&p.tmB1, alt(a.x, a.Xp), d, a.x ? T : R, 64, 64);
+    ok &= map_chunk_f32(&p.tmO0, a.dW1_out, d, nexp * f);
+    ok &= map_chunk_f32(&p.tmO1, a.dW3_out, d, nexp * f);
     p.Mw = 2 * a.f;
     p.N = a.d;
     p.out0 = a.dW1_out;
@@ -640,11 +834,13 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA0, a.G, d, R, 64, 64);
     ok &= map2d(&p.tmA1, a.dy, d, T, 64, 64);
     ok &= map2d(&p.tmB0, a.Hw, f, Rs, 64, 64);
+    ok &= map_chunk_f32(&p.tmO0, a.dW2_out, f, nexp * d);
     p.Mw = a.d;
     p.N = a.f;
     p.out0 = a.dW2_out;
   }
   return ok;
 }
+
 }  // namespace
 }  // namespace moe

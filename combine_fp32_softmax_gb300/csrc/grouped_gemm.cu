@@ -1,20 +1,10 @@
 // Persistent grouped GEMM over ragged expert segments on tcgen05 tensor cores
 // (one kernel per GEMM kind; the tile machinery is in gemm_tiles.cuh).
 //
-// Design (one CTA per SM, 320 threads):
-//   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
-//               (256 x 64) into a 4-stage shared-memory ring (48 KB/stage).
-//   warp 1      allocates 512 TMEM columns, issues tcgen05.mma
-//               (M=128, N=256, K=16, bf16 -> fp32) from one lane, commits
-//               to mbarriers; a ragged-K tail is zeroed in shared memory.
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
-//               thread = one output row; two warps per lane quadrant, each
-//               owning half of the 256 columns), fused elementwise work,
-//               stores.
-//   The accumulator is double-buffered in TMEM (2 x 256 columns) so the
-//   epilogue of tile i overlaps the main loop of tile i+1.
-// Tiles are taken in a static round-robin over CTAs; every output element is
-// produced by exactly one tile with a fixed K order.
+// Warp roles, shared-memory ring, TMEM double buffering and the staged TMA
+// epilogues are described in gemm_tiles.cuh.  Tiles are taken in a static
+// round-robin over CTAs; every output element is produced by exactly one
+// tile with a fixed K order.
 #include "gemm_tiles.cuh"
 
 namespace moe {
@@ -22,9 +12,12 @@ namespace {
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Tr = Traits<KIND>;
+  constexpr int NST = Tr::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  SharedState& ss = *reinterpret_cast<SharedState*>(smem + kStages * kStageBytes);
+  uint8_t* stg_base = smem + NST * kStageBytes;  // epilogue staging, Tr::EPI_BYTES per epilogue warp
+  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + kEpiWarps * Tr::EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -50,20 +43,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tma_prefetch_desc(&p.tmB0);
       ProducerState ps;
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-        if (!produce_tile<KIND>(p, decode_tile<KIND>(p, ss, tile), ss, smem, ps, abort, where0 | tile)) break;
+        if (!produce_tile<KIND, NST>(p, decode_tile<KIND>(p, ss, tile), ss, smem, ps, abort, where0 | tile)) break;
       if (*abort) producer_drain(ss, ps);
     }
   } else if (warp == 1) {
     MmaState ms;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-      if (!mma_tile<KIND>(p, decode_tile<KIND>(p, ss, tile), ss, smem, tmem, ms, abort, where0 | (2 << 20) | tile))
+      if (!mma_tile<KIND, NST>(p, decode_tile<KIND>(p, ss, tile), ss, smem, tmem, ms, abort,
+                               where0 | (2 << 20) | tile))
         break;
     if (*abort) mma_drain(ss, ms);
   } else {
-    int it = 0;
+    EpiState es;
+    uint8_t* stg = stg_base + (warp & 3) * Tr::EPI_BYTES;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-      if (!epilogue_step<KIND>(p, decode_tile<KIND>(p, ss, tile), ss, tmem, it, abort, where0 | (4 << 20) | tile))
+      if (!epilogue_step<KIND>(p, decode_tile<KIND>(p, ss, tile), ss, tmem, stg, es, abort,
+                               where0 | (4 << 20) | tile))
         break;
+    epilogue_drain(ss, es);
   }
 
   tc_fence_before();
@@ -76,13 +73,15 @@ template <int KIND>
 int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
   GemmParams p;
   if (!fill_params<KIND>(a, p)) return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+  constexpr int kSmem = smem_bytes<KIND>();
+  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int grid = grid_override > 0 ? grid_override : num_sms();
   constexpr int kTrace[6] = {MOE_K_GEMM1, MOE_K_GEMM2, MOE_K_GEMM_DH, MOE_K_GEMM_DX, MOE_K_GEMM_DW13, MOE_K_GEMM_DW2};
   TraceScope trace_scope(kTrace[KIND], s);
-  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, s>>>(p);
+  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

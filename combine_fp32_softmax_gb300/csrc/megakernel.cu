@@ -48,33 +48,21 @@ struct MegaParams {
 
 int g_skip_ticket = -1;
 
+constexpr int kMegaStages = 4;
+// epilogue staging per warp: the larger of GEMM 1's and GEMM 2's
+constexpr int kMegaEpiBytes =
+    Traits<kG1>::EPI_BYTES > Traits<kG2>::EPI_BYTES ? Traits<kG1>::EPI_BYTES : Traits<kG2>::EPI_BYTES;
+
 struct MegaShared {
   SharedState g;
-  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kStages];
+  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kMegaStages];
   int tq[kTq];
   int ntn1, ntn2, nt1, nt2, total;
 };
 
-constexpr int kMegaSmemBytes = 1024 + kStages * kStageBytes + static_cast<int>(sizeof(MegaShared));
-
-// ------------------------------------------------------ bulk copies (1D)
-__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst_smem)),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-               "r"(smem_u32(src_smem)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+constexpr int kMegaSmemBytes =
+    1024 + kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes + static_cast<int>(sizeof(MegaShared));
+static_assert(kMegaSmemBytes <= 232448, "shared memory budget of one CTA");
 
 // Bounded acquire-spin until *c >= target.
 __device__ bool wait_counter(const int* c, int target, volatile int* abort, int* err, int where) {
@@ -92,9 +80,11 @@ __device__ bool wait_counter(const int* c, int target, volatile int* abort, int*
   return true;
 }
 
-// Publishes this warp's global stores (generic and to the async proxy that
-// TMA reads through), then lane 0 adds one to the readiness counter.
+// Publishes this warp's global stores -- its TMA stores (completed first)
+// and any direct stores -- to other CTAs, including their TMA reads, then
+// lane 0 adds one to the readiness counter.
 __device__ __forceinline__ void warp_signal(int* counter) {
+  if ((threadIdx.x & 31) == 0) bulk_wait_all();
   fence_proxy_async_global();
   __threadfence();
   __syncwarp();
@@ -119,8 +109,8 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
   const int nchunk = (nrows + rps - 1) / rps;
   for (int c = 0; c <= nchunk; ++c) {
     if (c < nchunk) {
-      const int b = c % kStages;
-      if (c >= kStages) bulk_wait_read<kStages - 2>();  // chunk c-4 finished reading buffer b
+      const int b = c % kMegaStages;
+      if (c >= kMegaStages) bulk_wait_read<kMegaStages - 2>();  // chunk c-4 finished reading buffer b
       const int n = min(rps, nrows - c * rps);
       uint8_t* buf = smem + b * kStageBytes;
       mbar_arrive_expect_tx(&ms.gbar[b], n * rb);
@@ -131,7 +121,7 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
       gs.pending |= 1u << b;
     }
     if (c > 0) {
-      const int pc = c - 1, b = pc % kStages;
+      const int pc = c - 1, b = pc % kMegaStages;
       if (!mbar_wait(&ms.gbar[b], (gs.par >> b) & 1, abort, mp.g1.err, where)) return false;
       gs.par ^= 1u << b;
       gs.pending &= ~(1u << b);
@@ -149,7 +139,7 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
 
 __device__ void gather_drain(MegaShared& ms, const GatherState& gs) {
   bulk_wait_all();
-  for (int b = 0; b < kStages; ++b)
+  for (int b = 0; b < kMegaStages; ++b)
     if (gs.pending & (1u << b)) mbar_wait_drain(&ms.gbar[b], (gs.par >> b) & 1);
 }
 
@@ -181,12 +171,18 @@ __device__ void combine_warp(const MegaParams& mp, int c) {
 #pragma unroll
     for (int j = 0; j < kMaxTokRows; ++j) base[j] = rows + static_cast<size_t>(__shfl_sync(0xffffffffu, myrow, j)) * nvec;
     float4* o = reinterpret_cast<float4*>(mp.y) + static_cast<size_t>(t) * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-      float4 val[kMaxTokRows];
+    // two vectors per lane per step: twice the loads in flight for the few
+    // warps that run combine tasks; each element is summed in slot order.
+    for (int v = lane; v < nvec; v += 64) {
+      const bool two = v + 32 < nvec;
+      float4 val[kMaxTokRows], val2[kMaxTokRows];
 #pragma unroll
       for (int j = 0; j < kMaxTokRows; ++j)
-        if (j < nr) val[j] = base[j][v];
-      float4 acc = val[0];
+        if (j < nr) {
+          val[j] = base[j][v];
+          if (two) val2[j] = base[j][v + 32];
+        }
+      float4 acc = val[0], acc2 = val2[0];
 #pragma unroll
       for (int j = 1; j < kMaxTokRows; ++j)
         if (j < nr) {
@@ -194,8 +190,13 @@ __device__ void combine_warp(const MegaParams& mp, int c) {
           acc.y += val[j].y;
           acc.z += val[j].z;
           acc.w += val[j].w;
+          acc2.x += val2[j].x;
+          acc2.y += val2[j].y;
+          acc2.z += val2[j].z;
+          acc2.w += val2[j].w;
         }
       o[v] = acc;
+      if (two) o[v + 32] = acc2;
     }
   }
 }
@@ -203,7 +204,7 @@ __device__ void combine_warp(const MegaParams& mp, int c) {
 __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_constant__ MegaParams mp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + kStages * kStageBytes);
+  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes);
   SharedState& ss = ms.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = mp.g1.err;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       mbar_init(&ms.tq_full[q], 1);
       mbar_init(&ms.tq_empty[q], 1 + kEpiWarps);  // MMA warp + epilogue warps
     }
-    for (int b = 0; b < kStages; ++b) mbar_init(&ms.gbar[b], 1);
+    for (int b = 0; b < kMegaStages; ++b) mbar_init(&ms.gbar[b], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -271,13 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
             if (!ok) break;
             fence_proxy_async_global();
           }
-          if (!produce_tile<kG1>(mp.g1, t, ss, smem, ps, abort, where)) break;
+          if (!produce_tile<kG1, kMegaStages>(mp.g1, t, ss, smem, ps, abort, where)) break;
         } else if (id < e2) {
           const int t2 = id - e1;
           const int mt = t2 / ms.ntn2;
           if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kEpiWarps * ms.ntn1, abort, err, where)) break;
           fence_proxy_async_global();
-          if (!produce_tile<kG2>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
+          if (!produce_tile<kG2, kMegaStages>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
         }
       }
       if (*abort) {
@@ -303,14 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       const int where = kW | (2 << 20) | (id & 0xFFFFF);
       bool ok = true;
       if (id >= NG && id < e1)
-        ok = mma_tile<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<kG1, kMegaStages>(mp.g1, decode_tile<kG1>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
       else if (id >= e1 && id < e2)
-        ok = mma_tile<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<kG2, kMegaStages>(mp.g2, decode_g2(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
       if (!ok) break;
     }
     if (*abort) mma_drain(ss, mst);
   } else {
-    int it = 0, slot = 0;
+    EpiState es;
+    uint8_t* stg = smem + kMegaStages * kStageBytes + (warp & 3) * kMegaEpiBytes;
+    int slot = 0;
     uint32_t tph = 0;
     while (true) {
       if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (3 << 20))) break;
@@ -326,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       const int where = kW | (3 << 20) | (id & 0xFFFFF);
       if (id >= NG && id < e1) {
         const int t1 = id - NG;
-        if (!epilogue_step<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, t1), ss, tmem, it, abort, where)) break;
+        if (!epilogue_step<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, t1), ss, tmem, stg, es, abort, where)) break;
         warp_signal(&mp.ctr[kCtrXp + NG + t1 / ms.ntn1]);
       } else if (id >= e1 && id < e2) {
-        if (!epilogue_step<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, tmem, it, abort, where)) break;
+        if (!epilogue_step<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, tmem, stg, es, abort, where)) break;
         warp_signal(&mp.ctr[1]);
       } else if (id >= e2) {
         bool ok = true;
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
         combine_warp(mp, id - e2);
       }
     }
+    epilogue_drain(ss, es);
   }
 
   tc_fence_before();

@@ -241,7 +241,7 @@ def ws_offsets(cfg: MoEConfig) -> dict:
                          ("offsets", 4 * (E + 1)), ("dest", 4 * R), ("row_token", 4 * R),
                          ("row_slot", 4 * R), ("Xp", 2 * R * d), ("AB", 4 * Rs * f), ("H", 2 * Rs * f),
                          ("Op", 4 * Rs * d), ("G", 2 * R * d), ("dAB", 4 * Rs * f), ("Hw", 2 * Rs * f),
-                         ("dXp", 4 * Rs * d), ("partial", 8 * R * nt), ("dw", 4 * T * k)]:
+                         ("dXp", 4 * Rs * d), ("partial", 4 * R * nt), ("dw", 4 * T * k)]:
         take(name, nbytes)
     out["_mk"] = o
     return out
