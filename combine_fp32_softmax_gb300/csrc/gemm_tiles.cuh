@@ -84,10 +84,15 @@ struct Traits {
   static constexpr bool RAGGED_K = (KIND == kDW13 || KIND == kDW2);
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
   static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
+  // fp32 kinds: 16-column chunks, two staging buffers in flight.
+  static constexpr int F32_CPR = 1;
+  static constexpr int F32_ROUNDS = 2;
   // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two input buffers
-  // ([a, b, H] chunks) plus one output chunk of dA, dB, Hw; fp32 kinds two
-  // output chunks.
-  static constexpr int EPI_BYTES = (KIND == kG1) ? 3 * kChunkBytes : (KIND == kDH) ? 9 * kChunkBytes : 2 * kChunkBytes;
+  // ([a, b, H] chunks) plus one output chunk of dA, dB, Hw; fp32 kinds
+  // F32_ROUNDS x F32_CPR output chunks.
+  static constexpr int EPI_BYTES = (KIND == kG1)   ? 3 * kChunkBytes
+                                   : (KIND == kDH) ? 9 * kChunkBytes
+                                                   : F32_ROUNDS * F32_CPR * kChunkBytes;
 };
 
 struct SharedState {
@@ -100,6 +105,7 @@ struct SharedState {
   int seg_row0[kMaxSeg];
   int seg_rows[kMaxSeg];
   int prefix[kMaxSeg + 1];
+  int order[kMaxSeg];  // ragged-K kinds: segments by descending rows (largest first)
 };
 
 template <int KIND>
@@ -150,6 +156,21 @@ __device__ void build_segments(const GemmParams& p, SharedState& ss) {
     ss.seg_rows[s] = n;
   }
   __syncthreads();
+  if constexpr (Traits<KIND>::RAGGED_K) {
+    // Longest segments first: their tiles (K = their rows) are spread over
+    // the CTAs before the short ones fill in, so no long tile ends the
+    // launch alone.  Stable rank: more rows first, then lower index.
+    for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+      const int n = ss.seg_rows[s];
+      int rank = 0;
+      for (int u = 0; u < nseg; ++u) {
+        const int m = ss.seg_rows[u];
+        rank += (m > n || (m == n && u < s)) ? 1 : 0;
+      }
+      ss.order[rank] = s;
+    }
+    __syncthreads();
+  }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (nseg + 31) / 32;
@@ -180,17 +201,21 @@ template <int KIND>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const SharedState& ss, int tile) {
   using Tr = Traits<KIND>;
   int lo = 0, hi = ss.nseg;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (ss.prefix[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid;
+  if constexpr (Tr::RAGGED_K) {  // equal tile counts per segment, taken in ss.order
+    lo = ss.order[tile / ss.prefix[1]];
+  } else {
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ss.prefix[mid] <= tile)
+        lo = mid;
+      else
+        hi = mid;
+    }
   }
   TileInfo t;
   t.seg = lo;
   t.shared = lo >= p.E;
-  const int local = tile - ss.prefix[lo];
+  const int local = Tr::RAGGED_K ? tile % ss.prefix[1] : tile - ss.prefix[lo];
   const int ntn = (p.N + Tr::BNE - 1) / Tr::BNE;
   const int mb = local / ntn, nb = local - mb * ntn;
   t.m0 = mb * kBM;
@@ -354,27 +379,32 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
     optr = static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.d + m) * N;
   }
   const bool zero = Traits<KIND>::RAGGED_K && t.nkb == 0;  // empty expert: exact zeros
+  constexpr int NR = Traits<KIND>::F32_ROUNDS;
+  const int nchunks = min(16, (N - t.n0 + 15) / 16);
   es.chunks = 0;
+  // Software pipeline: chunk j+1's TMEM load is in flight while chunk j is
+  // staged and its TMA store issued.
+  uint32_t cur[16], nxt[16];
+  if (zero) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) cur[i] = 0u;
+  } else {
+    tmem_ld_32x16(tacc, cur);
+    tmem_ld_wait();
+  }
 #pragma unroll 1
-  for (int j = 0; j < 16; ++j) {
-    const int n = t.n0 + 16 * j;
-    if (n >= N) break;
-    uint32_t v[16];
-    if (zero) {
+  for (int j = 0; j < nchunks; ++j) {
+    const bool more = j + 1 < nchunks;
+    if (more && !zero) tmem_ld_32x16(tacc + 16 * (j + 1), nxt);
+    if constexpr (KIND == kG2) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0u;
-    } else {
-      tmem_ld_32x16(tacc + 16 * j, v);
-      tmem_ld_wait();
-      if constexpr (KIND == kG2) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(scale * __uint_as_float(v[i]));
-      }
+      for (int i = 0; i < 16; ++i) cur[i] = __float_as_uint(scale * __uint_as_float(cur[i]));
     }
+    const int n = t.n0 + 16 * j;
     if (full) {
-      uint8_t* buf = stg + (es.chunks & 1) * kChunkBytes;
-      staging_reuse_wait<1>(es.chunks);
-      stage_row64(buf, lane, v);
+      uint8_t* buf = stg + (es.chunks % NR) * kChunkBytes;
+      staging_reuse_wait<NR - 1>(es.chunks);
+      stage_row64(buf, lane, cur);
       staging_publish();
       if (lane == 0) {
         tma_store_2d(map, buf, n, orow0);
@@ -382,7 +412,12 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
       }
       ++es.chunks;
     } else if (rowok) {
-      store_words16(optr + n, v);
+      store_words16(optr + n, cur);
+    }
+    if (more) {
+      if (!zero) tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cur[i] = zero ? 0u : nxt[i];
     }
   }
 }
@@ -412,7 +447,7 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
     for (int i = 0; i < 16; ++i) {
       const float a0 = __uint_as_float(a[2 * i]), a1 = __uint_as_float(a[2 * i + 1]);
       const float b0 = __uint_as_float(b[2 * i]), b1 = __uint_as_float(b[2 * i + 1]);
-      hp[i] = pack_bf16(a0 / (1.f + expf(-a0)) * b0, a1 / (1.f + expf(-a1)) * b1);
+      hp[i] = pack_bf16(__fdividef(a0, 1.f + __expf(-a0)) * b0, __fdividef(a1, 1.f + __expf(-a1)) * b1);
       ap[i] = pack_bf16(a0, a1);
       bp[i] = pack_bf16(b0, b1);
     }
@@ -520,7 +555,7 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
         const float graw = __uint_as_float(g[2 * u + half]);
         dot += graw * h;
         const float dH = w * graw;
-        const float s = 1.f / (1.f + expf(-a));
+        const float s = __fdividef(1.f, 1.f + __expf(-a));
         dA2[half] = dH * b * s * (1.f + a * (1.f - s));
         dB2[half] = dH * (a * s);
         hw2[half] = w * h;

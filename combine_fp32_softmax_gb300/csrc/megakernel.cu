@@ -11,6 +11,8 @@
 // a set of readiness counters:
 //   ctr[0]                   ticket cursor
 //   ctr[1]                   GEMM-2 warp-tiles finished (combine waits on all)
+//   ctr[2]                   combine cursor: after the last ticket every warp of
+//                            every CTA claims tokens one at a time from it
 //   ctr[kCtrXp + g]          Xp row block g (128 rows) gathered
 //   ctr[kCtrXp + NG + mt]    GEMM-1 warp-tiles finished of m-tile mt
 //                            (GEMM-2 tiles of mt wait for all of them)
@@ -29,7 +31,6 @@ namespace {
 
 constexpr int kTq = 4;              // depth of the producer -> consumer task FIFO
 constexpr int kGatherRows = 128;    // Xp rows per gather task
-constexpr int kCombineTokens = 32;  // tokens per combine task (8 per epilogue warp)
 constexpr int kCtrXp = 8;
 constexpr int kMaxTokRows = 12;     // k <= 8 routed + S <= 4 shared rows per token
 
@@ -42,11 +43,31 @@ struct MegaParams {
   const float* Op;
   float* y;
   int* ctr;
-  int NG, NC;
+  int NG;
   int skip;  // testing aid: ticket treated as never done (-1: none)
+  // optional per-task timeline: records_per_cta records of 3 x u64
+  // (ticket | role << 32 | cta << 40, start ns, end ns) per CTA, the first
+  // half for the producer, the second for the first epilogue warp
+  unsigned long long* trace;
+  int trace_per_cta;
 };
 
 int g_skip_ticket = -1;
+unsigned long long* g_trace_buf = nullptr;
+int g_trace_per_cta = 0;
+
+__device__ __forceinline__ void trace_record(const MegaParams& mp, int role, int& n, int id, uint64_t t0) {
+  if (!mp.trace) return;
+  const int half = mp.trace_per_cta / 2;
+  if (n >= half) return;
+  unsigned long long* r =
+      mp.trace + 3ull * (static_cast<size_t>(blockIdx.x) * mp.trace_per_cta + static_cast<size_t>(role) * half + n);
+  r[0] = static_cast<unsigned long long>(static_cast<unsigned>(id)) | (static_cast<unsigned long long>(role) << 32) |
+         (static_cast<unsigned long long>(blockIdx.x) << 40);
+  r[1] = t0;
+  r[2] = globaltimer_ns();
+  ++n;
+}
 
 constexpr int kMegaStages = 4;
 // epilogue staging per warp: the larger of GEMM 1's and GEMM 2's
@@ -152,16 +173,14 @@ __device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaSh
   return t;
 }
 
-// Combine task (one epilogue warp, 8 tokens): the same fp32 sum, in the same
-// order, as the stand-alone combine kernel.
-__device__ void combine_warp(const MegaParams& mp, int c) {
-  const int lane = threadIdx.x & 31, ew = (threadIdx.x >> 5) - 2;
+// Combine of one token by one warp: the same fp32 sum, in the same order, as
+// the stand-alone combine kernel.
+__device__ void combine_token(const MegaParams& mp, int t) {
+  const int lane = threadIdx.x & 31;
   const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R;
   const int nr = k + S, nvec = mp.g1.d / 4;
   const float4* rows = reinterpret_cast<const float4*>(mp.Op);
-  for (int i = 0; i < kCombineTokens / kEpiWarps; ++i) {
-    const int t = c * kCombineTokens + ew * (kCombineTokens / kEpiWarps) + i;
-    if (t >= T) break;
+  {
     long long myrow = 0;
     if (lane < k)
       myrow = mp.dest[static_cast<size_t>(t) * k + lane];
@@ -201,6 +220,27 @@ __device__ void combine_warp(const MegaParams& mp, int c) {
   }
 }
 
+// Combine phase, run by every warp of every CTA once its part of the ticket
+// space is done: after all GEMM-2 tiles are published, warps claim single
+// tokens from their own cursor (ctr[2]) until none are left, so the work
+// balances across all warps whatever the tickets each CTA ended up with.
+__device__ void combine_phase(const MegaParams& mp, int nt2, volatile int* abort, int* err) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    ok = wait_counter(&mp.ctr[1], kEpiWarps * nt2, abort, err, (0x0F << 24) | (5 << 20)) ? 1 : 0;
+    __threadfence();
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  while (true) {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(&mp.ctr[2], 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t >= mp.g1.T) break;
+    combine_token(mp, t);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_constant__ MegaParams mp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -228,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
     ms.ntn2 = (mp.g2.N + kBN - 1) / kBN;
     ms.nt1 = ss.total_tiles;
     ms.nt2 = (ms.nt1 / ms.ntn1) * ms.ntn2;
-    ms.total = mp.NG + ms.nt1 + ms.nt2 + mp.NC;
+    ms.total = mp.NG + ms.nt1 + ms.nt2;  // combine is claimed per token afterwards
   }
   tc_fence_before();
   __syncthreads();
@@ -247,11 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       tma_prefetch_desc(&mp.g2.tmB0);
       ProducerState ps;
       GatherState gs;
-      int slot = 0;
+      int slot = 0, tn = 0;
       uint32_t tph = 0;
       while (!*abort) {
         if (!mbar_wait(&ms.tq_empty[slot], tph ^ 1, abort, err, kW | (1 << 20))) break;
         const int id = atomicAdd(&mp.ctr[0], 1);
+        const uint64_t t_claim = globaltimer_ns();
         ms.tq[slot] = id;
         mbar_arrive(&ms.tq_full[slot]);
         if (++slot == kTq) {
@@ -280,12 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
           fence_proxy_async_global();
           if (!produce_tile<kG2, kMegaStages>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
         }
+        trace_record(mp, 0, tn, id, t_claim);
       }
       if (*abort) {
         producer_drain(ss, ps);
         gather_drain(ms, gs);
       }
     }
+    __syncwarp();
+    if (!*abort) combine_phase(mp, nt2, abort, err);
   } else if (warp == 1) {
     MmaState mst;
     int slot = 0;
@@ -310,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       if (!ok) break;
     }
     if (*abort) mma_drain(ss, mst);
+    if (!*abort) combine_phase(mp, nt2, abort, err);
   } else {
     EpiState es;
     uint8_t* stg = smem + kMegaStages * kStageBytes + (warp & 3) * kMegaEpiBytes;
-    int slot = 0;
+    int slot = 0, tn = 0;
     uint32_t tph = 0;
     while (true) {
       if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (3 << 20))) break;
       const int id = ms.tq[slot];
+      const uint64_t t_pop = globaltimer_ns();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.tq_empty[slot]);
       if (++slot == kTq) {
@@ -334,17 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       } else if (id >= e1 && id < e2) {
         if (!epilogue_step<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, tmem, stg, es, abort, where)) break;
         warp_signal(&mp.ctr[1]);
-      } else if (id >= e2) {
-        bool ok = true;
-        if (lane == 0) {
-          ok = wait_counter(&mp.ctr[1], kEpiWarps * nt2, abort, err, where);
-          __threadfence();
-        }
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-        combine_warp(mp, id - e2);
       }
+      if (warp == 2 && lane == 0) trace_record(mp, 1, tn, id, t_pop);
     }
     epilogue_drain(ss, es);
+    if (!*abort) combine_phase(mp, nt2, abort, err);
   }
 
   tc_fence_before();
@@ -389,8 +429,9 @@ int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint1
   mp.y = y;
   mp.ctr = reinterpret_cast<int*>(ws + L.mk);
   mp.NG = ceil_div(R, kGatherRows);
-  mp.NC = ceil_div(c.T, kCombineTokens);
   mp.skip = g_skip_ticket;
+  mp.trace = g_trace_buf;
+  mp.trace_per_cta = g_trace_per_cta;
   // counters: kCtrXp + NG gather flags + (at most R/128 + E + S*ceil(T/128)) m-tiles
   const long long need = kCtrXp + mp.NG + R / kBM + c.E + static_cast<long long>(c.n_shared) * ceil_div(c.T, kBM) + 2;
   if (need > L.mk_ints) return MOE_ERR_SHAPE;
@@ -407,5 +448,12 @@ int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint1
 
 extern "C" int moe_debug_skip_megakernel_task(int ticket) {
   moe::g_skip_ticket = ticket >= 0 ? ticket : -1;
+  return MOE_OK;
+}
+
+extern "C" int moe_debug_megakernel_trace(void* buf, int records_per_cta) {
+  if (buf && (records_per_cta < 2 || (reinterpret_cast<uintptr_t>(buf) & 15u))) return MOE_ERR_ARG;
+  moe::g_trace_buf = static_cast<unsigned long long*>(buf);
+  moe::g_trace_per_cta = buf ? records_per_cta : 0;
   return MOE_OK;
 }

@@ -59,6 +59,7 @@ _SIGS = {
     "moe_num_sms": ([], _I),
     "moe_set_grid_limit": ([_I], _I),
     "moe_debug_skip_megakernel_task": ([_I], _I),
+    "moe_debug_megakernel_trace": ([_P, _I], _I),
     "moe_trace_enable": ([_I], _I),
     "moe_trace_reset": ([], _I),
     "moe_trace_read": ([_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
@@ -200,6 +201,23 @@ def moe_set_grid_limit(n: int):
 
 def moe_debug_skip_megakernel_task(ticket: int):
     _call("moe_debug_skip_megakernel_task", int(ticket))
+
+
+def moe_debug_megakernel_trace(buf, records_per_cta: int = 0):
+    """buf: int64 CUDA tensor of >= grid * records_per_cta * 3 elements, or None."""
+    _call("moe_debug_megakernel_trace", _ptr(buf), int(records_per_cta))
+
+
+def megakernel_timeline(buf, records_per_cta: int):
+    """Decodes a MegaKernel trace buffer into (cta, role, ticket, start_ns, end_ns) rows, start-sorted."""
+    rec = buf.view(-1, 3).cpu().tolist()
+    out = []
+    for meta, t0, t1 in rec:
+        if t1 <= 0 or t1 < t0:
+            continue
+        meta &= (1 << 64) - 1
+        out.append(((meta >> 40) & 0xFFFFFF, (meta >> 32) & 0xFF, meta & 0xFFFFFFFF, t0, t1))
+    return sorted(out, key=lambda r: r[3])
 
 
 def moe_trace_enable(on: bool):

@@ -289,6 +289,17 @@ enum {
  * Process-wide, not thread-safe; never set in normal use. */
 int moe_debug_skip_megakernel_task(int ticket);
 
+/* Profiling aid: per-task timeline of the forward MegaKernel.  While `buf`
+ * (device memory, 16-byte aligned, at least grid * records_per_cta * 24
+ * bytes; grid = moe_num_sms() unless capped) is set, every MegaKernel launch
+ * writes, per CTA, up to records_per_cta/2 records for its producer and as
+ * many for its first epilogue warp: three u64 each,
+ *   [ticket | role << 32 | cta << 40, start ns, end ns]  (%globaltimer),
+ * role 0 = producer (claim .. loads issued / gather done), role 1 =
+ * epilogue (task popped .. results published).  Unused records keep their
+ * previous contents.  buf = NULL turns it off.  Process-wide. */
+int moe_debug_megakernel_trace(void* buf, int records_per_cta);
+
 int moe_trace_enable(int on);
 int moe_trace_reset(void);
 int moe_trace_read(int kind, double* total_ms, int* launches);

@@ -310,43 +310,47 @@ def tokens_fwd_bwd(x, logits, W1, W3, W2, dy, k: int, S: int, renorm: int, token
     tokens = np.asarray(tokens, dtype=np.int64)
     xs = take_rows(x, tokens)
     dys = take_rows(dy, tokens)
-    W1, W3, W2 = f64(W1), f64(W3), f64(W2)
     E = np.asarray(logits).shape[1]
     routing = route(f64(logits)[tokens], k, renorm)
     n, d = xs.shape
     y = np.zeros((n, d)); dx = np.zeros((n, d)); dw = np.zeros((n, k))
-    experts = [(j, e) for j in range(k) for e in range(E)] + [(None, E + s) for s in range(S)]
-    for j, e in experts:
-        if j is None:
-            idx = np.arange(n); wgt = np.ones(n)
-        else:
-            idx = np.nonzero(routing.sel[:, j] == e)[0]
+    # one pass per expert (only the experts the sampled tokens use, each
+    # expert's weights widened once); a token picks an expert at most once
+    for e in range(E + S):
+        if e < E:
+            idx, slot = np.nonzero(routing.sel == e)
             if len(idx) == 0:
                 continue
-            wgt = routing.w[idx, j]
-        a, b, h, o = swiglu_expert(xs[idx], W1[e], W3[e], W2[e])
+            wgt = routing.w[idx, slot]
+        else:
+            idx, slot, wgt = np.arange(n), None, np.ones(n)
+        W1e, W3e, W2e = f64(W1[e]), f64(W3[e]), f64(W2[e])
+        a, b, h, o = swiglu_expert(xs[idx], W1e, W3e, W2e)
         y[idx] += wgt[:, None] * o
         g = dys[idx]
-        if j is not None:
-            dw[idx, j] = (g * o).sum(axis=1)
-        dh = (wgt[:, None] * g) @ W2[e]
+        if slot is not None:
+            dw[idx, slot] = (g * o).sum(axis=1)
+        dh = (wgt[:, None] * g) @ W2e
         dA = dh * b * dsilu(a); dB = dh * silu(a)
-        dx[idx] += dA @ W1[e] + dB @ W3[e]
+        dx[idx] += dA @ W1e + dB @ W3e
     dlogits = route_bwd(routing, dw, renorm)
     return routing, y, dx, dlogits, dw
 
 
 def dW_entries(x, logits, W1, W3, W2, dy, k: int, S: int, renorm: int,
-               which: str, expert: int, rows, cols):
+               which: str, expert: int, rows, cols, routing: Routing = None, perm: Permutation = None):
     """Selected entries of dW1/dW3 ([expert, n, c]) or dW2 ([expert, c, n]),
     each summed over the expert's whole segment.  ``rows``/``cols`` index the
-    weight matrix of that expert."""
+    weight matrix of that expert.  ``routing``/``perm`` may be passed in when
+    already computed for these logits."""
     W1e, W3e, W2e = f64(W1[expert]), f64(W3[expert]), f64(W2[expert])
     T = x.shape[0]
     E = np.asarray(logits).shape[1]
     if expert < E:
-        routing = route(logits, k, renorm)
-        perm = permute(routing.sel, E)
+        if routing is None:
+            routing = route(logits, k, renorm)
+        if perm is None:
+            perm = permute(routing.sel, E)
         r = np.arange(perm.offsets[expert], perm.offsets[expert + 1])
         tok = perm.row_token[r]
         wgt = routing.w.reshape(-1)[perm.row_slot[r]]

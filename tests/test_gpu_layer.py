@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from combine_fp32_softmax_gb300 import moe
-from combine_fp32_softmax_gb300.configs import DSV2_LITE, TINY, MoEConfig
+from combine_fp32_softmax_gb300.configs import DSV2_LITE, LONG128K, MIXTRAL, SKEWED, TINY, MoEConfig
 from combine_fp32_softmax_gb300.inputs import make_layer_inputs
 from oracle import moe_oracle as O
 from tests.gpu_util import (DEV, assert_grad_close, assert_layer_close, device_error, np64, run_layer,
@@ -134,13 +134,13 @@ def test_megakernel_wait_timeout_is_reported_and_context_survives():
 
 
 @pytest.mark.slow
-def test_full_size_sampled_parity():
-    """The benchmark workload (DeepSeek-V2-Lite-like layer: T=8192, d=2048,
-    f=1408, 64 experts top-6, 2 shared) in the benchmark's launch
-    configuration: routing and the permutation in full, y / dx / dlogits on
-    256 seeded tokens, and weight-gradient entries of several experts summed
-    over their whole segments."""
-    cfg = DSV2_LITE
+@pytest.mark.parametrize("cfg", [DSV2_LITE, MIXTRAL, SKEWED, LONG128K], ids=lambda c: c.name)
+def test_full_size_sampled_parity(cfg):
+    """Every workload at full size, in the benchmark's launch configuration:
+    routing and the permutation in full, y / dx / dlogits on 256 seeded
+    tokens (128 for the widest layers), and weight-gradient entries of
+    several experts (largest, smallest, a middle one, the shared ones)
+    summed over their whole segments; empty experts' gradients exactly 0."""
     inp = make_layer_inputs(cfg, seed=0)
     out, ws = run_layer(cfg, to_dev(inp))
     assert device_error(ws) == (0, 0)
@@ -150,20 +150,26 @@ def test_full_size_sampled_parity():
     for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
         assert np.array_equal(moe.ws_view(ws, cfg, name).cpu().numpy(), getattr(perm, name)), name
     rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(cfg.T, 256, replace=False))
+    ntok = 128 if cfg.f * cfg.d > 8e6 else 256
+    toks = np.sort(rng.choice(cfg.T, ntok, replace=False))
     _, y, dx, dz, _ = O.tokens_fwd_bwd(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
                                        cfg.renorm, toks)
     assert_layer_close("y", np64(out["y"])[toks], y)
     assert_grad_close("dx", np64(out["dx"])[toks], dx)
     assert_grad_close("dlogits", np64(out["dlogits"])[toks], dz)
     counts = perm.counts
-    experts = [int(np.argmax(counts)), int(np.argmin(counts)), 7, cfg.E, cfg.E + 1]
+    nonempty = np.nonzero(counts)[0]
+    experts = [int(np.argmax(counts)), int(nonempty[np.argmin(counts[nonempty])]), int(nonempty[len(nonempty) // 2])]
+    experts += [cfg.E + s for s in range(cfg.S)]
+    for e in np.nonzero(counts == 0)[0][:4]:  # empty experts: exact zeros
+        for gpu in (out["dW1"], out["dW3"], out["dW2"]):
+            assert torch.count_nonzero(gpu[int(e)]) == 0
     for which, gpu in (("W1", out["dW1"]), ("W3", out["dW3"]), ("W2", out["dW2"])):
         for e in experts:
             nr, nc = gpu.shape[1], gpu.shape[2]
             rows, cols = rng.integers(0, nr, 64), rng.integers(0, nc, 64)
             ref = O.dW_entries(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
-                               cfg.renorm, which, e, rows, cols)
+                               cfg.renorm, which, e, rows, cols, routing=routing, perm=perm)
             got = np64(gpu[e])[rows, cols]
             if counts[e] == 0 if e < cfg.E else False:
                 assert np.all(got == 0)
