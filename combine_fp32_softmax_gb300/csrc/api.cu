@@ -133,6 +133,13 @@ int moe_set_grid_limit(int n) {
   return MOE_OK;
 }
 
+int moe_set_gemm_pair_kinds(int mask) { return set_gemm_pair_kinds(mask); }
+
+int moe_gemm_pair_capacity(int kind) {
+  if (kind < kG1 || kind > kDW2) return 0;
+  return gemm_pair_capacity(static_cast<GemmKind>(kind));
+}
+
 int moe_route(const moe_cfg* cfg, const float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({logits, topk_idx, topk_w}, {}, ws));

@@ -51,4 +51,11 @@ struct GemmArgs {
 // Returns MOE_OK or a negative MOE_ERR_* (tensor-map encoding or launch).
 int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_override = 0);
 
+// Bit k set: kind k runs on CTA pairs (256-row tiles); clear: one CTA per
+// 128-row tile.  Returns the previous mask.
+int set_gemm_pair_kinds(int mask);
+
+// CTA pairs of `kind` that fit on the device at once (0 on error).
+int gemm_pair_capacity(GemmKind kind);
+
 }  // namespace moe

@@ -47,10 +47,10 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB (one CTA per tile)
 constexpr int kBoxBytes = 64 * 64 * 2;          // one MN-major box: 64 x 64 bf16
 constexpr int kMaxSeg = 256 + 4;
 constexpr int kEpiWarps = 4;
@@ -85,38 +85,63 @@ struct Traits {
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
   static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
   // fp32 kinds: 16-column chunks, two staging buffers in flight.
-  static constexpr int F32_CPR = 1;
   static constexpr int F32_ROUNDS = 2;
   // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two input buffers
   // ([a, b, H] chunks) plus one output chunk of dA, dB, Hw; fp32 kinds
-  // F32_ROUNDS x F32_CPR output chunks.
+  // F32_ROUNDS output chunks.
   static constexpr int EPI_BYTES = (KIND == kG1)   ? 3 * kChunkBytes
                                    : (KIND == kDH) ? 9 * kChunkBytes
-                                                   : F32_ROUNDS * F32_CPR * kChunkBytes;
+                                                   : F32_ROUNDS * kChunkBytes;
+};
+
+// Shared-memory pipeline of one kind.  CG = 1: one CTA per 128 x 256 tile,
+// 48 KB stages.  CG = 2: a CTA pair per 256 x 256 tile (tcgen05 CTA group of
+// two): each CTA stages its 128 rows of A and its half of B's 256 columns,
+// 32 KB a stage, so more stages fit and B is fetched once per 256 rows.
+template <int KIND, int CG>
+struct Pipe {
+  static constexpr int TILE_M = kBM * CG;  // output rows per (pair) tile
+  static constexpr int B_BYTES = kBBytes / CG;
+  static constexpr int B_BOXES = 4 / CG;  // MN-major B: 64-column boxes per CTA
+  static constexpr int STAGE_BYTES = kABytes + B_BYTES;
+  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 4 : 6);
 };
 
 struct SharedState {
   uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain;
+  uint64_t ready[kMaxStages];  // CG = 2, even CTA: the odd CTA's stage has landed
   uint64_t aux[kEpiWarps][2];  // dH epilogue input buffers of each warp
   uint32_t tmem_base;
   int abort;
   int nseg;
   int total_tiles;
+  int tiles_per_seg;  // ragged-K kinds: every segment has the same tile count
   int seg_row0[kMaxSeg];
-  int seg_rows[kMaxSeg];
-  int prefix[kMaxSeg + 1];
-  int order[kMaxSeg];  // ragged-K kinds: segments by descending rows (largest first)
+  union {
+    int prefix[kMaxSeg + 1];  // ragged-M kinds: tiles before each segment
+    int order[kMaxSeg];       // ragged-K kinds: segments by descending rows
+  };
 };
 
-template <int KIND>
+// Rows of segment s: routed expert s owns [offsets[s], offsets[s+1]); the
+// shared experts own T rows each.
+__device__ __forceinline__ int seg_rows(const GemmParams& p, const SharedState& ss, int s) {
+  if (s >= p.E) return p.T;
+  return (s + 1 < p.E ? ss.seg_row0[s + 1] : p.R) - ss.seg_row0[s];
+}
+
+template <int KIND, int CG = 1>
 constexpr int smem_bytes() {
-  return 1024 + Traits<KIND>::STAGES * kStageBytes + kEpiWarps * Traits<KIND>::EPI_BYTES +
+  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + kEpiWarps * Traits<KIND>::EPI_BYTES +
          static_cast<int>(sizeof(SharedState));
 }
 
+// One CTA's part of a tile.  m0 and rows are this CTA's: in a pair the odd
+// CTA's part starts 128 rows further and may hold no valid row (`active`
+// false: it still takes part in the main loop, and writes nothing).
 struct TileInfo {
   int seg, m0, n0, rows, grow0, nkb;
-  bool shared;
+  bool shared, active;
 };
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
@@ -128,55 +153,49 @@ __device__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <int KIND>
+template <int KIND, int CG>
 __device__ __forceinline__ int tiles_of(const GemmParams& p, int rows) {
   using Tr = Traits<KIND>;
+  constexpr int TM = Pipe<KIND, CG>::TILE_M;
   const int ntn = (p.N + Tr::BNE - 1) / Tr::BNE;
   if constexpr (Tr::RAGGED_K)
-    return ((p.Mw + kBM - 1) / kBM) * ntn;
+    return ((p.Mw + TM - 1) / TM) * ntn;
   else
-    return ((rows + kBM - 1) / kBM) * ntn;
+    return ((rows + TM - 1) / TM) * ntn;
 }
 
 // Segment table: routed expert e owns GEMM rows [offsets[e], offsets[e+1]);
 // shared expert s owns [R + s*T, R + (s+1)*T).  prefix[] counts tiles.
-template <int KIND>
+template <int KIND, int CG = 1>
 __device__ void build_segments(const GemmParams& p, SharedState& ss) {
   const int nseg = p.E + p.S;
-  for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
-    int r0, n;
-    if (s < p.E) {
-      r0 = p.offsets[s];
-      n = p.offsets[s + 1] - r0;
-    } else {
-      r0 = p.R + (s - p.E) * p.T;
-      n = p.T;
-    }
-    ss.seg_row0[s] = r0;
-    ss.seg_rows[s] = n;
-  }
+  for (int s = threadIdx.x; s < nseg; s += blockDim.x)
+    ss.seg_row0[s] = (s < p.E) ? p.offsets[s] : p.R + (s - p.E) * p.T;
   __syncthreads();
   if constexpr (Traits<KIND>::RAGGED_K) {
     // Longest segments first: their tiles (K = their rows) are spread over
     // the CTAs before the short ones fill in, so no long tile ends the
     // launch alone.  Stable rank: more rows first, then lower index.
     for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
-      const int n = ss.seg_rows[s];
+      const int n = seg_rows(p, ss, s);
       int rank = 0;
       for (int u = 0; u < nseg; ++u) {
-        const int m = ss.seg_rows[u];
+        const int m = seg_rows(p, ss, u);
         rank += (m > n || (m == n && u < s)) ? 1 : 0;
       }
       ss.order[rank] = s;
     }
-    __syncthreads();
-  }
-  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
+      ss.tiles_per_seg = tiles_of<KIND, CG>(p, 0);
+      ss.total_tiles = ss.tiles_per_seg * nseg;
+      ss.nseg = nseg;
+    }
+  } else if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (nseg + 31) / 32;
     const int lo = min(nseg, lane * per), hi = min(nseg, lo + per);
     int local = 0;
-    for (int s = lo; s < hi; ++s) local += tiles_of<KIND>(p, ss.seg_rows[s]);
+    for (int s = lo; s < hi; ++s) local += tiles_of<KIND, CG>(p, seg_rows(p, ss, s));
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -186,7 +205,7 @@ __device__ void build_segments(const GemmParams& p, SharedState& ss) {
     int run = incl - local;
     for (int s = lo; s < hi; ++s) {
       ss.prefix[s] = run;
-      run += tiles_of<KIND>(p, ss.seg_rows[s]);
+      run += tiles_of<KIND, CG>(p, seg_rows(p, ss, s));
     }
     if (lane == 31) {
       ss.prefix[nseg] = incl;
@@ -197,12 +216,13 @@ __device__ void build_segments(const GemmParams& p, SharedState& ss) {
   __syncthreads();
 }
 
-template <int KIND>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const SharedState& ss, int tile) {
+template <int KIND, int CG = 1>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const SharedState& ss, int tile,
+                                                int rank = 0) {
   using Tr = Traits<KIND>;
   int lo = 0, hi = ss.nseg;
   if constexpr (Tr::RAGGED_K) {  // equal tile counts per segment, taken in ss.order
-    lo = ss.order[tile / ss.prefix[1]];
+    lo = ss.order[tile / ss.tiles_per_seg];
   } else {
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -215,60 +235,67 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
   TileInfo t;
   t.seg = lo;
   t.shared = lo >= p.E;
-  const int local = Tr::RAGGED_K ? tile % ss.prefix[1] : tile - ss.prefix[lo];
+  const int local = Tr::RAGGED_K ? tile % ss.tiles_per_seg : tile - ss.prefix[lo];
   const int ntn = (p.N + Tr::BNE - 1) / Tr::BNE;
   const int mb = local / ntn, nb = local - mb * ntn;
-  t.m0 = mb * kBM;
+  t.m0 = mb * Pipe<KIND, CG>::TILE_M + rank * kBM;
   t.n0 = nb * Tr::BNE;
   if constexpr (Tr::RAGGED_K) {
-    t.rows = ss.seg_rows[lo];
+    t.rows = seg_rows(p, ss, lo);
     t.grow0 = ss.seg_row0[lo];
     t.nkb = (t.rows + kBK - 1) / kBK;
+    t.active = t.m0 < p.Mw;
   } else {
-    t.rows = min(kBM, ss.seg_rows[lo] - t.m0);
+    t.rows = min(kBM, seg_rows(p, ss, lo) - t.m0);
     t.grow0 = ss.seg_row0[lo] + t.m0;
     t.nkb = p.K / kBK;
+    t.active = t.rows > 0;
   }
   return t;
 }
 
-// One stage of TMA loads (48 KB in every kind).
-template <int KIND>
+// One stage of TMA loads: A (this CTA's 128 rows) and this CTA's part of B
+// (all 256 columns for CG = 1; columns [128 rank, 128 rank + 128) for
+// CG = 2).  Boxes that fall outside a tensor are zero-filled.
+template <int KIND, int CG = 1>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& t, int kb, uint8_t* sA,
-                                            uint8_t* sB, uint64_t* bar) {
+                                            uint8_t* sB, uint64_t* bar, int rank = 0) {
+  constexpr int NB = Pipe<KIND, CG>::B_BOXES;
   const int kk = kb * kBK;
+  const int bn0 = t.n0 + 128 * rank;  // first B column this CTA stages
   if constexpr (KIND == kG1) {
+    // accumulator columns [0,128) = gate rows of W1, [128,256) = up rows of W3
     tma_load_2d(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, kk, t.shared ? t.m0 : t.grow0);
-    tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.f + t.n0);
-    tma_load_2d(sB + kBBytes / 2, &p.tmB1, bar, kk, t.seg * p.f + t.n0);
+    if (CG == 1 || rank == 0) tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.f + t.n0);
+    if (CG == 1 || rank == 1) tma_load_2d(sB + (CG == 1 ? kBBytes / 2 : 0), &p.tmB1, bar, kk, t.seg * p.f + t.n0);
   } else if constexpr (KIND == kG2) {
     tma_load_2d(sA, &p.tmA0, bar, kk, t.grow0);
-    tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.d + t.n0);
+    tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.d + bn0);
   } else if constexpr (KIND == kDH) {
     tma_load_2d(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, kk, t.shared ? t.m0 : t.grow0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, t.n0 + 64 * i, t.seg * p.d + kk);
+    for (int i = 0; i < NB; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, bn0 + 64 * i, t.seg * p.d + kk);
   } else if constexpr (KIND == kDX) {
     tma_load_2d(sA, &p.tmA0, bar, kk, t.grow0);
     const bool second = kk >= p.f;
     const int krow = t.seg * p.f + (second ? kk - p.f : kk);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_2d(sB + i * kBoxBytes, second ? &p.tmB1 : &p.tmB0, bar, t.n0 + 64 * i, krow);
+    for (int i = 0; i < NB; ++i)
+      tma_load_2d(sB + i * kBoxBytes, second ? &p.tmB1 : &p.tmB0, bar, bn0 + 64 * i, krow);
   } else if constexpr (KIND == kDW13) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) tma_load_2d(sA + i * kBoxBytes, &p.tmA0, bar, t.m0 + 64 * i, t.grow0 + kk);
     const int brow = t.shared ? kk : t.grow0 + kk;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_2d(sB + i * kBoxBytes, t.shared ? &p.tmB1 : &p.tmB0, bar, t.n0 + 64 * i, brow);
+    for (int i = 0; i < NB; ++i)
+      tma_load_2d(sB + i * kBoxBytes, t.shared ? &p.tmB1 : &p.tmB0, bar, bn0 + 64 * i, brow);
   } else {  // kDW2
     const int arow = t.shared ? kk : t.grow0 + kk;
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       tma_load_2d(sA + i * kBoxBytes, t.shared ? &p.tmA1 : &p.tmA0, bar, t.m0 + 64 * i, arow);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, t.n0 + 64 * i, t.grow0 + kk);
+    for (int i = 0; i < NB; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, bn0 + 64 * i, t.grow0 + kk);
   }
 }
 
@@ -591,14 +618,18 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
 // Shared by the grouped GEMM kernels and the MegaKernel, so a tile's MMA
 // sequence and epilogue arithmetic are the same code in both.
 
+// CG = 2: the even CTA's tempty barriers count the epilogue warps of both
+// CTAs; ready[s] takes the odd CTA's word that its part of stage s landed.
+template <int CG = 1>
 __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&ss.full[s], 1);
     mbar_init(&ss.empty[s], 1);
+    mbar_init(&ss.ready[s], 1);
   }
   for (int a = 0; a < 2; ++a) {
     mbar_init(&ss.tfull[a], 1);
-    mbar_init(&ss.tempty[a], kEpiWarps);
+    mbar_init(&ss.tempty[a], kEpiWarps * CG);
   }
   for (int w = 0; w < kEpiWarps; ++w) {
     mbar_init(&ss.aux[w][0], 1);
@@ -614,14 +645,15 @@ struct ProducerState {
   uint32_t phase = 0, filled = 0, fill_par = 0;
 };
 
-template <int KIND, int NST>
+template <int KIND, int NST, int CG = 1>
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
-                                             ProducerState& ps, volatile int* abort, int where) {
+                                             ProducerState& ps, volatile int* abort, int where, int rank = 0) {
+  constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
   for (int kb = 0; kb < t.nkb; ++kb) {
     if (!mbar_wait(&ss.empty[ps.stage], ps.phase ^ 1, abort, p.err, where)) return false;
-    uint8_t* sA = smem + ps.stage * kStageBytes;
-    mbar_arrive_expect_tx(&ss.full[ps.stage], kStageBytes);
-    issue_loads<KIND>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage]);
+    uint8_t* sA = smem + ps.stage * SB;
+    mbar_arrive_expect_tx(&ss.full[ps.stage], SB);
+    issue_loads<KIND, CG>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage], rank);
     ps.filled |= 1u << ps.stage;
     ps.fill_par = (ps.fill_par & ~(1u << ps.stage)) | (ps.phase << ps.stage);
     if (++ps.stage == NST) {
@@ -645,36 +677,67 @@ struct MmaState {
   bool issued = false;
 };
 
-template <int KIND, int NST>
-__device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
-                                         uint32_t tmem, MmaState& ms, volatile int* abort, int where) {
-  using Tr = Traits<KIND>;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
+// Ragged-K tail: the rows of a stage past the segment's end are zeroed in
+// shared memory (they hold the next segment's rows) so they add nothing.
+template <int KIND, int CG>
+__device__ __forceinline__ void zero_k_tail(const TileInfo& t, int kb, uint8_t* sA, uint8_t* sB) {
+  const int kvalid = t.rows - kb * kBK;
+  if (kvalid >= kBK) return;
   const int lane = threadIdx.x & 31;
+  const int per_box = (kBK - kvalid) * 8;
+  constexpr int NBOX = 2 + Pipe<KIND, CG>::B_BOXES;
+  for (int idx = lane; idx < NBOX * per_box; idx += 32) {
+    const int box = idx / per_box, rem = idx - box * per_box;
+    uint8_t* bb = (box < 2) ? sA + box * kBoxBytes : sB + (box - 2) * kBoxBytes;
+    reinterpret_cast<uint4*>(bb + (kvalid + rem / 8) * 128)[rem & 7] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// MMA warp, one tile.  CG = 1, or the even CTA of a pair: waits for the
+// accumulator buffer, then per stage for its data (and, in a pair, for the
+// odd CTA's word that its part landed), issues the MMAs from lane 0 and
+// commits: stage release to the producers (both CTAs of a pair), and the
+// finished accumulator to the epilogues (both CTAs).  The odd CTA of a pair
+// only relays: waits for its own stage, zeroes its ragged-K tail and tells
+// the even CTA.
+template <int KIND, int NST, int CG = 1>
+__device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
+                                         uint32_t tmem, MmaState& ms, volatile int* abort, int where,
+                                         int rank = 0) {
+  using Tr = Traits<KIND>;
+  constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
+  const int lane = threadIdx.x & 31;
+  if (CG == 2 && rank == 1) {
+    for (int kb = 0; kb < t.nkb; ++kb) {
+      if (!mbar_wait(&ss.full[ms.stage], ms.phase, abort, p.err, where | (1 << 20))) return false;
+      uint8_t* sA = smem + ms.stage * SB;
+      if constexpr (Tr::RAGGED_K) zero_k_tail<KIND, CG>(t, kb, sA, sA + kABytes);
+      if (lane == 0) mbar_arrive_rank(&ss.ready[ms.stage], 0);
+      __syncwarp();
+      if (++ms.stage == NST) {
+        ms.stage = 0;
+        ms.phase ^= 1;
+      }
+    }
+    return true;
+  }
   const int acc = ms.it & 1;
   const uint32_t aph = (ms.it >> 1) & 1;
   ++ms.it;
-  if (!mbar_wait(&ss.tempty[acc], aph ^ 1, abort, p.err, where)) return false;
+  if (!mbar_wait<CG == 2>(&ss.tempty[acc], aph ^ 1, abort, p.err, where)) return false;
   tc_fence_after();
   const uint32_t dtm = tmem + acc * kBN;
   for (int kb = 0; kb < t.nkb; ++kb) {
     if (!mbar_wait(&ss.full[ms.stage], ms.phase, abort, p.err, where | (1 << 20))) return false;
-    tc_fence_after();
-    uint8_t* sA = smem + ms.stage * kStageBytes;
+    uint8_t* sA = smem + ms.stage * SB;
     uint8_t* sB = sA + kABytes;
-    if constexpr (Tr::RAGGED_K) {
-      const int kvalid = t.rows - kb * kBK;
-      if (kvalid < kBK) {  // rows past the segment end must not contribute
-        const int per_box = (kBK - kvalid) * 8;
-        for (int idx = lane; idx < 6 * per_box; idx += 32) {
-          const int box = idx / per_box, rem = idx - box * per_box;
-          uint8_t* bb = (box < 2) ? sA + box * kBoxBytes : sB + (box - 2) * kBoxBytes;
-          reinterpret_cast<uint4*>(bb + (kvalid + rem / 8) * 128)[rem & 7] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-    }
+    if constexpr (Tr::RAGGED_K) zero_k_tail<KIND, CG>(t, kb, sA, sB);
+    if constexpr (CG == 2)
+      if (!mbar_wait<true>(&ss.ready[ms.stage], ms.phase, abort, p.err, where | (3 << 20))) return false;
+    tc_fence_after();
     if (lane == 0) {
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
@@ -683,9 +746,12 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
                                      : smem_desc_sw128(a0 + k4 * 32, 16, 1024);
         const uint64_t bd = Tr::B_MN ? smem_desc_sw128(b0 + k4 * 2048, kBoxBytes, 1024)
                                      : smem_desc_sw128(b0 + k4 * 32, 16, 1024);
-        umma_bf16(dtm, ad, bd, kIdesc, (kb | k4) != 0 ? 1u : 0u);
+        umma_bf16<CG>(dtm, ad, bd, kIdesc, (kb | k4) != 0 ? 1u : 0u);
       }
-      umma_commit(&ss.empty[ms.stage]);
+      if constexpr (CG == 2)
+        umma_commit_pair(&ss.empty[ms.stage]);
+      else
+        umma_commit(&ss.empty[ms.stage]);
       ms.issued = true;
     }
     __syncwarp();
@@ -694,15 +760,21 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
       ms.phase ^= 1;
     }
   }
-  if (lane == 0) umma_commit(&ss.tfull[acc]);
+  if (lane == 0) {
+    if constexpr (CG == 2)
+      umma_commit_pair(&ss.tfull[acc]);
+    else
+      umma_commit(&ss.tfull[acc]);
+  }
   __syncwarp();
   return true;
 }
 
 // Waits for the tensor core before TMEM is released on an aborted run.
+template <int CG = 1>
 __device__ __forceinline__ void mma_drain(SharedState& ss, const MmaState& ms) {
   if ((threadIdx.x & 31) == 0 && ms.issued) {
-    umma_commit(&ss.drain);
+    umma_commit<CG>(&ss.drain);
     mbar_wait_drain(&ss.drain, 0);
   }
   __syncwarp();
@@ -712,20 +784,26 @@ __device__ __forceinline__ void mma_drain(SharedState& ss, const MmaState& ms) {
 // this warp's staging memory.  The TMEM buffer is released as soon as the
 // last accumulator load is done; the staged stores drain in the background
 // and are waited for (read side) before the staging memory is reused.
-template <int KIND>
+// In a pair the odd CTA's warps release the buffer on the even CTA's
+// barrier.  A part with no valid row still waits for the accumulator, so its
+// release cannot count toward an earlier phase of the barrier.
+template <int KIND, int CG = 1>
 __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInfo& t, SharedState& ss, uint32_t tmem,
-                                              uint8_t* stg, EpiState& es, volatile int* abort, int where) {
+                                              uint8_t* stg, EpiState& es, volatile int* abort, int where,
+                                              int rank = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are reachable from this warp
   const int acc = es.it & 1;
   const uint32_t aph = (es.it >> 1) & 1;
   ++es.it;
-  if constexpr (KIND == kDH) dh_prefetch(p, t, q, stg, ss, es);
+  if constexpr (KIND == kDH)
+    if (t.active) dh_prefetch(p, t, q, stg, ss, es);
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
   tc_fence_after();
   const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
   bool ok = true;
-  if constexpr (KIND == kG1)
+  if (!t.active) {
+  } else if constexpr (KIND == kG1)
     epilogue_g1(p, t, q, tacc, stg, es);
   else if constexpr (KIND == kDH)
     ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where);
@@ -733,7 +811,12 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
     epilogue_f32<KIND>(p, t, q, tacc, stg, es);
   tc_fence_before();
   __syncwarp();
-  if (ok && lane == 0) mbar_arrive(&ss.tempty[acc]);
+  if (ok && lane == 0) {
+    if (CG == 2 && rank == 1)
+      mbar_arrive_rank(&ss.tempty[acc], 0);
+    else
+      mbar_arrive(&ss.tempty[acc]);
+  }
   if (lane == 0) bulk_wait_read<0>();  // staging memory free for the next tile
   __syncwarp();
   return ok;
@@ -796,8 +879,8 @@ bool map_chunk_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
   return map2d_any(m, base, 4, inner, outer, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// Tensor maps and pointers of one GEMM kind.
-template <int KIND>
+// Tensor maps and pointers of one GEMM kind (CG: CTAs per tile).
+template <int KIND, int CG = 1>
 bool fill_params(const GemmArgs& a, GemmParams& p) {
   std::memset(&p, 0, sizeof(p));
   const uint64_t T = a.T, d = a.d, f = a.f, nexp = a.E + a.S, R = uint64_t(a.T) * a.k, Rs = R + uint64_t(a.S) * a.T;
@@ -829,7 +912,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     p.out1 = a.AB_out;
   } else if constexpr (KIND == kG2) {
     ok &= map2d(&p.tmA0, a.H, f, Rs, 64, 128);
-    ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 256);
+    ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 256 / CG);
     ok &= map_chunk_f32(&p.tmO0, a.Op_out, d, Rs);
     p.N = a.d;
     p.K = a.f;

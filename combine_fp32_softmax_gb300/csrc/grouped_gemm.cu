@@ -5,98 +5,194 @@
 // epilogues are described in gemm_tiles.cuh.  Tiles are taken in a static
 // round-robin over CTAs; every output element is produced by exactly one
 // tile with a fixed K order.
+#include <algorithm>
+
 #include "gemm_tiles.cuh"
 
 namespace moe {
 namespace {
 
-template <int KIND>
+// CG = 1: one CTA per SM and tile.  CG = 2: CTA pairs (clusters of two), one
+// 256-row tile per pair; the even CTA issues the MMAs for both.
+template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Tr = Traits<KIND>;
-  constexpr int NST = Tr::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* stg_base = smem + NST * kStageBytes;  // epilogue staging, Tr::EPI_BYTES per epilogue warp
-  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + kEpiWarps * Tr::EPI_BYTES);
+  constexpr int NST = Pipe<KIND, CG>::STAGES;
+  constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The 128-byte-swizzled stages need a 1024-byte-aligned base; the dynamic
+  // shared window of a kernel without static shared memory starts there.
+  // Checked rather than padded (the padding would cost a pipeline stage's
+  // worth of headroom): a misaligned base is reported, never computed on.
+  // The offset is the same in every CTA, so both CTAs of a pair return here.
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) record_error(p.err, MOE_ERR_CUDA, 0x5A11);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint8_t* stg_base = smem + NST * SB;  // epilogue staging, Traits::EPI_BYTES per epilogue warp
+  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + kEpiWarps * Traits<KIND>::EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int first = CG == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int step = CG == 2 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    init_gemm_barriers(ss);
+    init_gemm_barriers<CG>(ss);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ss.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(&ss.tmem_base, kTmemCols);
+    tmem_relinquish<CG>();
   }
-  build_segments<KIND>(p, ss);
+  build_segments<KIND, CG>(p, ss);
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anything arrives on them
   tc_fence_after();
   const uint32_t tmem = ss.tmem_base;
   const int total = ss.total_tiles;
   volatile int* abort = &ss.abort;
-  const int where0 = (KIND + 1) << 24;
+  const int where0 = (KIND + 1) << 24 | rank << 23;
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&p.tmA0);
       tma_prefetch_desc(&p.tmB0);
       ProducerState ps;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-        if (!produce_tile<KIND, NST>(p, decode_tile<KIND>(p, ss, tile), ss, smem, ps, abort, where0 | tile)) break;
+      for (int tile = first; tile < total && !*abort; tile += step)
+        if (!produce_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
+                                         where0 | tile, rank))
+          break;
       if (*abort) producer_drain(ss, ps);
     }
   } else if (warp == 1) {
     MmaState ms;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-      if (!mma_tile<KIND, NST>(p, decode_tile<KIND>(p, ss, tile), ss, smem, tmem, ms, abort,
-                               where0 | (2 << 20) | tile))
+    for (int tile = first; tile < total && !*abort; tile += step)
+      if (!mma_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, tmem, ms, abort,
+                                   where0 | (2 << 20) | tile, rank))
         break;
-    if (*abort) mma_drain(ss, ms);
+    if (*abort) mma_drain<CG>(ss, ms);
   } else {
     EpiState es;
-    uint8_t* stg = stg_base + (warp & 3) * Tr::EPI_BYTES;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x)
-      if (!epilogue_step<KIND>(p, decode_tile<KIND>(p, ss, tile), ss, tmem, stg, es, abort,
-                               where0 | (4 << 20) | tile))
+    uint8_t* stg = stg_base + (warp & 3) * Traits<KIND>::EPI_BYTES;
+    for (int tile = first; tile < total && !*abort; tile += step)
+      if (!epilogue_step<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, tmem, stg, es, abort,
+                                   where0 | (4 << 20) | tile, rank))
         break;
     epilogue_drain(ss, es);
   }
 
   tc_fence_before();
   __syncthreads();
+  // No CTA of a pair leaves (or frees TMEM) while the other may still arrive
+  // on its barriers or have MMAs read its shared memory.
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
+}
+
+int g_pair_kinds = 0;  // kinds that run on CTA pairs (bit = GemmKind)
+
+// Launch configuration of one kind; CG = 2 adds the cluster dimension.
+template <int KIND, int CG>
+void launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t s) {
+  cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<KIND, CG>();
+  cfg.stream = s;
+  if constexpr (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+}
+
+// Number of CTA pairs of kind KIND that can be resident at once (cached).
+template <int KIND>
+int pair_capacity() {
+  static int cached = 0;
+  if (cached == 0) {
+    auto kern = grouped_gemm_kernel<KIND, 2>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<KIND, 2>()) !=
+        cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    launch_config<KIND, 2>(cfg, attr, nullptr);
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return 0;
+    cached = n;
+  }
+  return cached;
+}
+
+template <int KIND, int CG>
+int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
+  GemmParams p;
+  if (!fill_params<KIND, CG>(a, p)) return MOE_ERR_CUDA;
+  constexpr int kSmem = smem_bytes<KIND, CG>();
+  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
+  auto kern = grouped_gemm_kernel<KIND, CG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int grid = grid_override > 0 ? grid_override : num_sms();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  launch_config<KIND, CG>(cfg, attr, s);
+  if constexpr (CG == 2) {
+    // Persistent: only as many pairs as can be resident at once (an SM
+    // left without a partner stays idle rather than adding a second wave).
+    const int max_pairs = pair_capacity<KIND>();
+    if (max_pairs <= 0) return MOE_ERR_CUDA;
+    grid = 2 * std::max(1, std::min(max_pairs, grid / 2));
+  }
+  cfg.gridDim = dim3(grid);
+  constexpr int kTrace[6] = {MOE_K_GEMM1, MOE_K_GEMM2, MOE_K_GEMM_DH, MOE_K_GEMM_DX, MOE_K_GEMM_DW13, MOE_K_GEMM_DW2};
+  TraceScope trace_scope(kTrace[KIND], s);
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <int KIND>
-int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
-  GemmParams p;
-  if (!fill_params<KIND>(a, p)) return MOE_ERR_CUDA;
-  constexpr int kSmem = smem_bytes<KIND>();
-  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  const int grid = grid_override > 0 ? grid_override : num_sms();
-  constexpr int kTrace[6] = {MOE_K_GEMM1, MOE_K_GEMM2, MOE_K_GEMM_DH, MOE_K_GEMM_DX, MOE_K_GEMM_DW13, MOE_K_GEMM_DW2};
-  TraceScope trace_scope(kTrace[KIND], s);
-  grouped_gemm_kernel<KIND><<<grid, kThreads, kSmem, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+int launch_any(const GemmArgs& a, cudaStream_t s, int grid_override) {
+  return (g_pair_kinds >> KIND) & 1 ? launch_kind<KIND, 2>(a, s, grid_override)
+                                    : launch_kind<KIND, 1>(a, s, grid_override);
 }
 
 }  // namespace
 
 int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_override) {
   switch (kind) {
-    case kG1: return launch_kind<kG1>(a, s, grid_override);
-    case kG2: return launch_kind<kG2>(a, s, grid_override);
-    case kDH: return launch_kind<kDH>(a, s, grid_override);
-    case kDX: return launch_kind<kDX>(a, s, grid_override);
-    case kDW13: return launch_kind<kDW13>(a, s, grid_override);
-    case kDW2: return launch_kind<kDW2>(a, s, grid_override);
+    case kG1: return launch_any<kG1>(a, s, grid_override);
+    case kG2: return launch_any<kG2>(a, s, grid_override);
+    case kDH: return launch_any<kDH>(a, s, grid_override);
+    case kDX: return launch_any<kDX>(a, s, grid_override);
+    case kDW13: return launch_any<kDW13>(a, s, grid_override);
+    case kDW2: return launch_any<kDW2>(a, s, grid_override);
   }
   return MOE_ERR_ARG;
+}
+
+int gemm_pair_capacity(GemmKind kind) {
+  switch (kind) {
+    case kG1: return pair_capacity<kG1>();
+    case kG2: return pair_capacity<kG2>();
+    case kDH: return pair_capacity<kDH>();
+    case kDX: return pair_capacity<kDX>();
+    case kDW13: return pair_capacity<kDW13>();
+    case kDW2: return pair_capacity<kDW2>();
+  }
+  return 0;
+}
+
+int set_gemm_pair_kinds(int mask) {
+  const int prev = g_pair_kinds;
+  g_pair_kinds = mask & ((1 << 6) - 1);
+  return prev;
 }
 
 }  // namespace moe

@@ -82,7 +82,7 @@ struct MegaShared {
 };
 
 constexpr int kMegaSmemBytes =
-    1024 + kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes + static_cast<int>(sizeof(MegaShared));
+    kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes + static_cast<int>(sizeof(MegaShared));
 static_assert(kMegaSmemBytes <= 232448, "shared memory budget of one CTA");
 
 // Bounded acquire-spin until *c >= target.
@@ -242,8 +242,12 @@ __device__ void combine_phase(const MegaParams& mp, int nt2, volatile int* abort
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_constant__ MegaParams mp) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023) {  // see grouped_gemm_kernel: checked, not padded
+    if (threadIdx.x == 0) record_error(mp.g1.err, MOE_ERR_CUDA, 0x5A11);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes);
   SharedState& ss = ms.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

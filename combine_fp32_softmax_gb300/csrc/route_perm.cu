@@ -303,7 +303,11 @@ __global__ void __launch_bounds__(256)
 }
 
 // out[t] = ((rows[sel[t*k]] + rows[sel[t*k+1]]) + ...) + rows[R + t] + ...
-// in exactly that order, fp32, float4 per lane, one warp per token.
+// in exactly that order, fp32, one warp per token.  NR = k + S rows per
+// token is a template parameter so the loads of every row (two float4 per
+// lane per step) are in registers with no spare slots, which keeps enough
+// warps resident to stream at HBM rate.
+template <int NR>
 __global__ void __launch_bounds__(256)
     sum_rows_f32_kernel(const float4* __restrict__ rows, const int32_t* __restrict__ sel, int T, int k, int S,
                         int nvec, float4* __restrict__ out) {
@@ -311,35 +315,40 @@ __global__ void __launch_bounds__(256)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const long long R = static_cast<long long>(T) * k;
   const long long nrows = R + static_cast<long long>(S) * T;
-  const int nr = k + S;
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
     long long myrow = 0;
     if (lane < k) {
       myrow = sel[static_cast<size_t>(t) * k + lane];
       if (myrow < 0 || myrow >= nrows) myrow = 0;
-    } else if (lane < nr) {
+    } else if (lane < NR) {
       myrow = R + static_cast<long long>(lane - k) * T + t;
     }
-    const float4* base[kMaxRowsPerToken];
+    const float4* base[NR];
 #pragma unroll
-    for (int j = 0; j < kMaxRowsPerToken; ++j)
-      base[j] = rows + static_cast<size_t>(__shfl_sync(kFull, myrow, j)) * nvec;
+    for (int j = 0; j < NR; ++j) base[j] = rows + static_cast<size_t>(__shfl_sync(kFull, myrow, j)) * nvec;
     float4* o = out + static_cast<size_t>(t) * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-      float4 val[kMaxRowsPerToken];
+    for (int v = lane; v < nvec; v += 64) {
+      const bool two = v + 32 < nvec;
+      float4 val[NR], val2[NR];
 #pragma unroll
-      for (int j = 0; j < kMaxRowsPerToken; ++j)
-        if (j < nr) val[j] = __ldg(base[j] + v);
-      float4 acc = val[0];
+      for (int j = 0; j < NR; ++j) {
+        val[j] = __ldg(base[j] + v);
+        val2[j] = two ? __ldg(base[j] + v + 32) : val[j];
+      }
+      float4 acc = val[0], acc2 = val2[0];
 #pragma unroll
-      for (int j = 1; j < kMaxRowsPerToken; ++j)
-        if (j < nr) {
-          acc.x += val[j].x;
-          acc.y += val[j].y;
-          acc.z += val[j].z;
-          acc.w += val[j].w;
-        }
+      for (int j = 1; j < NR; ++j) {
+        acc.x += val[j].x;
+        acc.y += val[j].y;
+        acc.z += val[j].z;
+        acc.w += val[j].w;
+        acc2.x += val2[j].x;
+        acc2.y += val2[j].y;
+        acc2.z += val2[j].z;
+        acc2.w += val2[j].w;
+      }
       o[v] = acc;
+      if (two) o[v + 32] = acc2;
     }
   }
 }
@@ -480,8 +489,27 @@ cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, in
                                 int trace_kind, cudaStream_t s) {
   TraceScope trace_scope(trace_kind, s);
   const int blocks = min(ceil_div(T, 8), num_sms() * 8);
-  sum_rows_f32_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(rows), sel, T, k, S, d / 4,
-                                             reinterpret_cast<float4*>(out));
+  const float4* r4 = reinterpret_cast<const float4*>(rows);
+  float4* o4 = reinterpret_cast<float4*>(out);
+  switch (k + S) {
+#define MOE_SUM_ROWS_CASE(N) \
+  case N: sum_rows_f32_kernel<N><<<blocks, 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4); break;
+    MOE_SUM_ROWS_CASE(1)
+    MOE_SUM_ROWS_CASE(2)
+    MOE_SUM_ROWS_CASE(3)
+    MOE_SUM_ROWS_CASE(4)
+    MOE_SUM_ROWS_CASE(5)
+    MOE_SUM_ROWS_CASE(6)
+    MOE_SUM_ROWS_CASE(7)
+    MOE_SUM_ROWS_CASE(8)
+    MOE_SUM_ROWS_CASE(9)
+    MOE_SUM_ROWS_CASE(10)
+    MOE_SUM_ROWS_CASE(11)
+    MOE_SUM_ROWS_CASE(12)
+#undef MOE_SUM_ROWS_CASE
+    static_assert(12 == kMaxRowsPerToken, "one instantiation per row count");
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -58,6 +58,8 @@ _SIGS = {
     "moe_get_device_error": ([_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "moe_num_sms": ([], _I),
     "moe_set_grid_limit": ([_I], _I),
+    "moe_set_gemm_pair_kinds": ([_I], _I),
+    "moe_gemm_pair_capacity": ([_I], _I),
     "moe_debug_skip_megakernel_task": ([_I], _I),
     "moe_debug_megakernel_trace": ([_P, _I], _I),
     "moe_trace_enable": ([_I], _I),
@@ -197,6 +199,20 @@ def moe_num_sms() -> int:
 
 def moe_set_grid_limit(n: int):
     _call("moe_set_grid_limit", int(n))
+
+
+GEMM_KINDS = ("gemm1", "gemm2", "dh", "dx", "dw13", "dw2")
+ALL_PAIR_KINDS = (1 << len(GEMM_KINDS)) - 1
+
+
+def moe_set_gemm_pair_kinds(mask: int) -> int:
+    """Bit k: grouped-GEMM kind GEMM_KINDS[k] on CTA pairs. Returns the previous mask."""
+    return int(lib().moe_set_gemm_pair_kinds(int(mask)))
+
+
+def moe_gemm_pair_capacity(kind: int) -> int:
+    """CTA pairs of grouped-GEMM kind `kind` resident at once on the current device."""
+    return int(lib().moe_gemm_pair_capacity(int(kind)))
 
 
 def moe_debug_skip_megakernel_task(ticket: int):

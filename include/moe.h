@@ -254,6 +254,22 @@ int moe_num_sms(void);
  * it exists to test exactly that.  Process-wide, not thread-safe. */
 int moe_set_grid_limit(int n);
 
+/* Selects, per grouped-GEMM kind, the tile shape: bit k of `mask` set runs
+ * kind k on CTA pairs (thread-block clusters of two; the pair computes a
+ * 256 x 256 tile with tcgen05 MMAs of the CTA group of two, each CTA holding
+ * half of A and half of B); clear runs it one CTA per 128 x 256 tile.  Bits:
+ * 0 GEMM 1 (gate/up), 1 GEMM 2 (down), 2 dH, 3 dX, 4 dW1/dW3, 5 dW2.  The
+ * default is none.  Results are the same bits either way: every output
+ * element is the same fp32 sum over K in the same order.  Returns the
+ * previous mask.  Process-wide, not thread-safe. */
+int moe_set_gemm_pair_kinds(int mask);
+
+/* Number of CTA pairs of grouped-GEMM kind `kind` (numbered as above) that
+ * the current device holds at once; the pair-mode launches use that many
+ * pairs (fewer under moe_set_grid_limit).  Returns 0 for an unknown kind or
+ * when the query fails. */
+int moe_gemm_pair_capacity(int kind);
+
 /* ------------------------------------------------------- kernel timing
  * Optional profiling aid.  While enabled, every kernel launch the library
  * makes is bracketed by a pair of CUDA events recorded on the launching

@@ -23,6 +23,15 @@ EK = MoEConfig("ek_T200_d128_f128_E4_k4_renorm", 200, 128, 128, 4, 4, renorm=1)
 GEMM_CFGS = [TINY, MID, D192, SKEW, EK]
 
 
+@pytest.fixture(params=["pair", "single"])
+def gemm_mode(request):
+    """Runs a GEMM test with every kind on CTA pairs (256-row tiles) and
+    again with one CTA per 128-row tile."""
+    prev = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS if request.param == "pair" else 0)
+    yield request.param
+    moe.moe_set_gemm_pair_kinds(prev)
+
+
 def _route(cfg, logits_dev):
     ws = moe.alloc_workspace(cfg, DEV)
     idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=DEV)
@@ -169,7 +178,7 @@ def _fwd_pieces(cfg, seed=5):
 
 
 @pytest.mark.parametrize("cfg", GEMM_CFGS, ids=lambda c: c.name)
-def test_gemm_fwd_matches_oracle(cfg):
+def test_gemm_fwd_matches_oracle(cfg, gemm_mode):
     inp, g, idx, w, ws, t, Xp, H, AB, Op, fw = _fwd_pieces(cfg)
     assert device_error(ws) == (0, 0)
     assert_bf16_rounding_close("a", AB[:, :cfg.f], fw.a)
@@ -181,7 +190,7 @@ def test_gemm_fwd_matches_oracle(cfg):
 
 
 @pytest.mark.parametrize("cfg", GEMM_CFGS, ids=lambda c: c.name)
-def test_gemm_bwd_matches_oracle(cfg):
+def test_gemm_bwd_matches_oracle(cfg, gemm_mode):
     inp, g, idx, w, ws, t, Xp, H, AB, Op, fw = _fwd_pieces(cfg)
     bw = O.layer_bwd(fw, inp.dy, inp.x, inp.W1, inp.W3, inp.W2, renorm=cfg.renorm)
     G = torch.empty(cfg.R, cfg.d, dtype=torch.bfloat16, device=DEV)

@@ -70,6 +70,28 @@ def test_results_do_not_depend_on_grid_size():
     assert len(digests) == 1
 
 
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_cta_pair_tiles_equal_single_cta_tiles_bitwise(cfg):
+    """Every grouped GEMM on CTA pairs (256-row tiles, tcgen05 CTA group of
+    two) gives the same bits as one CTA per 128-row tile: each output element
+    is the same fp32 sum over K in the same order.  The configurations cover
+    segments that end inside the pair's first half (an odd CTA with no valid
+    row) and weight-gradient row counts that are not multiples of 256."""
+    g = to_dev(make_layer_inputs(cfg, seed=18))
+    prev = moe.moe_set_gemm_pair_kinds(0)
+    try:
+        a, wsa = run_layer(cfg, g)
+        moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
+        b, wsb = run_layer(cfg, g, fill=float("nan"))
+    finally:
+        moe.moe_set_gemm_pair_kinds(prev)
+    assert device_error(wsa) == (0, 0) and device_error(wsb) == (0, 0)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    for name in ("H", "AB", "Op", "dAB", "Hw"):
+        assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
+
+
 def test_b_and_w_parts_split():
     """which=1 then which=2 gives the same bits as which=3."""
     cfg = MID
