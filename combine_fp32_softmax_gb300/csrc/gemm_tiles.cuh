@@ -254,12 +254,26 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
   return t;
 }
 
+// Ragged-K kinds: the last K block of a tile whose segment length is not a
+// multiple of kBK (its rows past the segment end are zeroed in shared memory).
+template <int KIND>
+__device__ __forceinline__ bool is_k_tail(const TileInfo& t, int kb) {
+  return Traits<KIND>::RAGGED_K && kb == t.nkb - 1 && (t.rows & (kBK - 1)) != 0;
+}
+
 // One stage of TMA loads: A (this CTA's 128 rows) and this CTA's part of B
 // (all 256 columns for CG = 1; columns [128 rank, 128 rank + 128) for
-// CG = 2).  Boxes that fall outside a tensor are zero-filled.
+// CG = 2).  Boxes that fall outside a tensor are zero-filled.  `to_even`:
+// completion is counted on the pair's even CTA's barrier.
 template <int KIND, int CG = 1>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& t, int kb, uint8_t* sA,
-                                            uint8_t* sB, uint64_t* bar, int rank = 0) {
+                                            uint8_t* sB, uint64_t* bar, int rank = 0, bool to_even = false) {
+  auto tma_load_2d = [&](void* dst, const CUtensorMap* map, uint64_t* b, int c0, int c1) {
+    if (CG == 2 && to_even)
+      tma_load_2d_to_even(dst, map, b, c0, c1);
+    else
+      moe::tma_load_2d(dst, map, b, c0, c1);
+  };
   constexpr int NB = Pipe<KIND, CG>::B_BOXES;
   const int kk = kb * kBK;
   const int bn0 = t.n0 + 128 * rank;  // first B column this CTA stages
@@ -640,11 +654,19 @@ __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
 }
 
 // Producer lane: every K block of one tile through the NST-stage ring.
+// filled / fill_par: stages with a load counted on this CTA's own barrier,
+// and the parity of the phase it completes (for the drain on abort).
 struct ProducerState {
   int stage = 0;
   uint32_t phase = 0, filled = 0, fill_par = 0;
+  uint32_t tail_par = 0;  // CG = 2, odd CTA: phase parity of its own full[s] (turns on K tails only)
 };
 
+// CG = 2: both CTAs' loads of a stage are counted on the even CTA's full[s]
+// (the even CTA expects both CTAs' bytes), so no thread stands between the
+// odd CTA's data and the MMA.  A ragged-K tail is the exception: each CTA's
+// loads complete on its own full[s], each zeroes its own rows past the
+// segment end, and the odd CTA then arrives on the even CTA's ready[s].
 template <int KIND, int NST, int CG = 1>
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
                                              ProducerState& ps, volatile int* abort, int where, int rank = 0) {
@@ -652,10 +674,18 @@ __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo
   for (int kb = 0; kb < t.nkb; ++kb) {
     if (!mbar_wait(&ss.empty[ps.stage], ps.phase ^ 1, abort, p.err, where)) return false;
     uint8_t* sA = smem + ps.stage * SB;
-    mbar_arrive_expect_tx(&ss.full[ps.stage], SB);
-    issue_loads<KIND, CG>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage], rank);
-    ps.filled |= 1u << ps.stage;
-    ps.fill_par = (ps.fill_par & ~(1u << ps.stage)) | (ps.phase << ps.stage);
+    const uint32_t bit = 1u << ps.stage;
+    const bool tail = CG == 2 && is_k_tail<KIND>(t, kb);
+    if (CG == 1 || rank == 0 || tail) mbar_arrive_expect_tx(&ss.full[ps.stage], CG == 2 && !tail ? 2 * SB : SB);
+    issue_loads<KIND, CG>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage], rank, CG == 2 && rank == 1 && !tail);
+    if (CG == 1 || rank == 0) {
+      ps.filled |= bit;
+      ps.fill_par = (ps.fill_par & ~bit) | (ps.phase << ps.stage);
+    } else if (tail) {
+      ps.filled |= bit;
+      ps.fill_par = (ps.fill_par & ~bit) | (ps.tail_par & bit);
+      ps.tail_par ^= bit;
+    }
     if (++ps.stage == NST) {
       ps.stage = 0;
       ps.phase ^= 1;
@@ -674,6 +704,7 @@ __device__ __forceinline__ void producer_drain(SharedState& ss, const ProducerSt
 struct MmaState {
   int stage = 0, it = 0;
   uint32_t phase = 0;
+  uint32_t tail_par = 0;  // CG = 2: parity of ready[s] (even CTA) / own full[s] (odd CTA) on K tails
   bool issued = false;
 };
 
@@ -696,12 +727,12 @@ __device__ __forceinline__ void zero_k_tail(const TileInfo& t, int kb, uint8_t* 
 }
 
 // MMA warp, one tile.  CG = 1, or the even CTA of a pair: waits for the
-// accumulator buffer, then per stage for its data (and, in a pair, for the
-// odd CTA's word that its part landed), issues the MMAs from lane 0 and
-// commits: stage release to the producers (both CTAs of a pair), and the
-// finished accumulator to the epilogues (both CTAs).  The odd CTA of a pair
-// only relays: waits for its own stage, zeroes its ragged-K tail and tells
-// the even CTA.
+// accumulator buffer, then per stage for its data (on a pair's ragged-K
+// tail also for the odd CTA's word that its zeroed part is ready), issues
+// the MMAs from lane 0 and commits: stage release to the producers (both
+// CTAs of a pair), and the finished accumulator to the epilogues (both
+// CTAs).  The odd CTA's MMA warp only handles ragged-K tails: waits for its
+// own stage, zeroes its rows past the segment end and tells the even CTA.
 template <int KIND, int NST, int CG = 1>
 __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
                                          uint32_t tmem, MmaState& ms, volatile int* abort, int where,
@@ -711,15 +742,22 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
   const int lane = threadIdx.x & 31;
   if (CG == 2 && rank == 1) {
-    for (int kb = 0; kb < t.nkb; ++kb) {
-      if (!mbar_wait(&ss.full[ms.stage], ms.phase, abort, p.err, where | (1 << 20))) return false;
-      uint8_t* sA = smem + ms.stage * SB;
-      if constexpr (Tr::RAGGED_K) zero_k_tail<KIND, CG>(t, kb, sA, sA + kABytes);
-      if (lane == 0) mbar_arrive_rank(&ss.ready[ms.stage], 0);
-      __syncwarp();
-      if (++ms.stage == NST) {
-        ms.stage = 0;
-        ms.phase ^= 1;
+    if constexpr (Tr::RAGGED_K) {
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (is_k_tail<KIND>(t, kb)) {
+          const uint32_t bit = 1u << ms.stage;
+          if (!mbar_wait(&ss.full[ms.stage], (ms.tail_par & bit) ? 1u : 0u, abort, p.err, where | (1 << 20)))
+            return false;
+          ms.tail_par ^= bit;
+          uint8_t* sA = smem + ms.stage * SB;
+          zero_k_tail<KIND, CG>(t, kb, sA, sA + kABytes);
+          if (lane == 0) mbar_arrive_rank(&ss.ready[ms.stage], 0);
+          __syncwarp();
+        }
+        if (++ms.stage == NST) {
+          ms.stage = 0;
+          ms.phase ^= 1;
+        }
       }
     }
     return true;
@@ -735,8 +773,15 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
     uint8_t* sA = smem + ms.stage * SB;
     uint8_t* sB = sA + kABytes;
     if constexpr (Tr::RAGGED_K) zero_k_tail<KIND, CG>(t, kb, sA, sB);
-    if constexpr (CG == 2)
-      if (!mbar_wait<true>(&ss.ready[ms.stage], ms.phase, abort, p.err, where | (3 << 20))) return false;
+    if constexpr (CG == 2 && Tr::RAGGED_K) {
+      if (is_k_tail<KIND>(t, kb)) {
+        const uint32_t bit = 1u << ms.stage;
+        if (!mbar_wait<true>(&ss.ready[ms.stage], (ms.tail_par & bit) ? 1u : 0u, abort, p.err,
+                             where | (3 << 20)))
+          return false;
+        ms.tail_par ^= bit;
+      }
+    }
     tc_fence_after();
     if (lane == 0) {
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);

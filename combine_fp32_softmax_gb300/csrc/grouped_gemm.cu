@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
 }
 
-int g_pair_kinds = 0;  // kinds that run on CTA pairs (bit = GemmKind)
+int g_pair_kinds = (1 << 6) - 1;  // kinds that run on CTA pairs (bit = GemmKind)
 
 // Launch configuration of one kind; CG = 2 adds the cluster dimension.
 template <int KIND, int CG>

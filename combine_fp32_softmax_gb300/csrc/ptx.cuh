@@ -133,6 +133,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// CTA pair (tcgen05 CTA group of two): 2D tiled load into this CTA's shared
+// memory whose completion is counted on the barrier at `bar`'s offset in
+// the pair's even CTA, where the MMAs that read both CTAs' tiles are issued.
+__device__ __forceinline__ void tma_load_2d_to_even(void* dst, const void* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "{\n\t.reg .b32 rb;\n\t"
+      "mapa.shared::cluster.u32 rb, %2, 0;\n\t"
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%3, %4}], [rb];\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
 // 2D tiled store of one box from shared memory (bulk-group completion).
 // Parts of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* map, const void* src_smem, int c0, int c1) {

@@ -259,7 +259,7 @@ int moe_set_grid_limit(int n);
  * 256 x 256 tile with tcgen05 MMAs of the CTA group of two, each CTA holding
  * half of A and half of B); clear runs it one CTA per 128 x 256 tile.  Bits:
  * 0 GEMM 1 (gate/up), 1 GEMM 2 (down), 2 dH, 3 dX, 4 dW1/dW3, 5 dW2.  The
- * default is none.  Results are the same bits either way: every output
+ * default is all six.  Results are the same bits either way: every output
  * element is the same fp32 sum over K in the same order.  Returns the
  * previous mask.  Process-wide, not thread-safe. */
 int moe_set_gemm_pair_kinds(int mask);
