@@ -255,10 +255,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
 }
 
 // Ragged-K kinds: the last K block of a tile whose segment length is not a
-// multiple of kBK (its rows past the segment end are zeroed in shared memory).
+// multiple of 16 (the MMA's K step).  Its rows from the segment end up to the
+// next multiple of 16 are zeroed in shared memory; K steps wholly past the
+// end are not issued.
 template <int KIND>
 __device__ __forceinline__ bool is_k_tail(const TileInfo& t, int kb) {
-  return Traits<KIND>::RAGGED_K && kb == t.nkb - 1 && (t.rows & (kBK - 1)) != 0;
+  return Traits<KIND>::RAGGED_K && kb == t.nkb - 1 && (t.rows & 15) != 0;
+}
+// K steps (16 rows each) of block kb that hold rows of the segment.
+template <int KIND>
+__device__ __forceinline__ int k_steps(const TileInfo& t, int kb) {
+  if constexpr (Traits<KIND>::RAGGED_K)
+    return min(kBK / 16, (t.rows - kb * kBK + 15) >> 4);
+  else
+    return kBK / 16;
 }
 
 // One stage of TMA loads: A (this CTA's 128 rows) and this CTA's part of B
@@ -708,19 +718,24 @@ struct MmaState {
   bool issued = false;
 };
 
-// Ragged-K tail: the rows of a stage past the segment's end are zeroed in
-// shared memory (they hold the next segment's rows) so they add nothing.
+// Ragged-K tail: in the last K step that holds rows of the segment, the
+// rows past the segment's end (they hold the next segment's rows) are
+// zeroed in shared memory, in every box of A and B, so they add nothing.
+// Both operands are zeroed so that a non-finite value of another expert's
+// rows cannot reach this expert's sums.  MN-major boxes hold one K row per
+// 128 bytes; all 8 pieces of a row are cleared, so the swizzle is moot.
 template <int KIND, int CG>
 __device__ __forceinline__ void zero_k_tail(const TileInfo& t, int kb, uint8_t* sA, uint8_t* sB) {
+  if (!is_k_tail<KIND>(t, kb)) return;
   const int kvalid = t.rows - kb * kBK;
-  if (kvalid >= kBK) return;
+  const int n = (((kvalid + 15) & ~15) - kvalid) * 8;  // 16-byte pieces per box, < 128
   const int lane = threadIdx.x & 31;
-  const int per_box = (kBK - kvalid) * 8;
   constexpr int NBOX = 2 + Pipe<KIND, CG>::B_BOXES;
-  for (int idx = lane; idx < NBOX * per_box; idx += 32) {
-    const int box = idx / per_box, rem = idx - box * per_box;
+#pragma unroll
+  for (int box = 0; box < NBOX; ++box) {
     uint8_t* bb = (box < 2) ? sA + box * kBoxBytes : sB + (box - 2) * kBoxBytes;
-    reinterpret_cast<uint4*>(bb + (kvalid + rem / 8) * 128)[rem & 7] = make_uint4(0, 0, 0, 0);
+    for (int idx = lane; idx < n; idx += 32)
+      reinterpret_cast<uint4*>(bb + (kvalid + (idx >> 3)) * 128)[idx & 7] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
   __syncwarp();
@@ -785,8 +800,10 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
     tc_fence_after();
     if (lane == 0) {
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      const int nk4 = k_steps<KIND>(t, kb);
 #pragma unroll
       for (int k4 = 0; k4 < kBK / 16; ++k4) {
+        if (k4 >= nk4) break;
         const uint64_t ad = Tr::A_MN ? smem_desc_sw128(a0 + k4 * 2048, kBoxBytes, 1024)
                                      : smem_desc_sw128(a0 + k4 * 32, 16, 1024);
         const uint64_t bd = Tr::B_MN ? smem_desc_sw128(b0 + k4 * 2048, kBoxBytes, 1024)
