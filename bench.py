@@ -47,6 +47,10 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller captures for profiling)")
     ap.add_argument("--gemm-pair-kinds", type=int, default=-1,
                     help="bit mask of grouped-GEMM kinds run on CTA pairs (-1: the library default)")
+    ap.add_argument("--no-bwd-overlap", action="store_true",
+                    help="run the backward's weight-gradient GEMMs on the caller's stream (no B/W overlap)")
+    ap.add_argument("--no-autotune", action="store_true",
+                    help="skip the library's measured GEMM autotuner (run during set-up, untimed)")
     return ap.parse_args()
 
 
@@ -148,17 +152,23 @@ def gemm_flops_per_launch(cfg):
             "gemm_dw13": 2 * dfr, "gemm_dw2": dfr}
 
 
-def traffic_from_profiles(kernel, workload):
-    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, or None."""
+def traffic_from_profiles(kernel, workload, cta_group=None):
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, or None.
+    A line `traffic_bytes_per_launch[cta_group=N]: B` is specific to one tile
+    shape of a grouped GEMM (N = 1 or 2 CTAs per tile) and is preferred when
+    that shape ran; `traffic_bytes_per_launch: B` holds for any."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
-    for line in open(path):
-        if line.strip().startswith("traffic_bytes_per_launch:"):
-            try:
-                return float(line.split(":", 1)[1].strip().split()[0])
-            except ValueError:
-                return None
+    keys = ([f"traffic_bytes_per_launch[cta_group={cta_group}]:"] if cta_group else []) + ["traffic_bytes_per_launch:"]
+    lines = [ln.strip() for ln in open(path)]
+    for key in keys:
+        for line in lines:
+            if line.startswith(key):
+                try:
+                    return float(line.split(":", 1)[1].strip().split()[0])
+                except ValueError:
+                    return None
     return None
 
 
@@ -206,9 +216,9 @@ def run_reference(args):
     return 0
 
 
-def config_dict(cfg, megakernel, pair_kinds=None):
+def config_dict(cfg, megakernel):
     return {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E, "k": cfg.k,
-            "n_shared": cfg.S, "renorm": cfg.renorm, "megakernel": megakernel, "gemm_pair_kinds": pair_kinds,
+            "n_shared": cfg.S, "renorm": cfg.renorm, "megakernel": megakernel,
             "l2": "inputs larger than L2 (no flush): weights 1.15 GB + activations per step",
             "parallelism": "replicas"}
 
@@ -232,8 +242,8 @@ def run_ours(args):
     ws = moe.alloc_workspace(cfg, dev)
     if args.gemm_pair_kinds >= 0:
         moe.moe_set_gemm_pair_kinds(args.gemm_pair_kinds)
-    pair_kinds = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
-    moe.moe_set_gemm_pair_kinds(pair_kinds)
+    if args.no_bwd_overlap:
+        moe.moe_set_bwd_overlap(False)
     f32 = torch.float32
     nexp = cfg.E + cfg.S
     out = dict(y=torch.empty(cfg.T, cfg.d, dtype=f32, device=dev),
@@ -257,6 +267,16 @@ def run_ours(args):
         b.record()
         b.synchronize()
         return a.elapsed_time(b) / iters
+
+    # Set-up, untimed: the library's measured autotuner picks each grouped
+    # GEMM's tile shape and L2 prefetch depth on this very layer.
+    tuning = None
+    if not args.no_autotune:
+        tuning = moe.moe_autotune(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], g["dy"], out["y"], out["idx"],
+                                  out["w"], out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], ws)
+        tuning = {k: {"pair": v[0], "prefetch_kb": v[1], "us": round(v[2], 1)} for k, v in tuning.items()}
+    pair_kinds = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
+    moe.moe_set_gemm_pair_kinds(pair_kinds)
 
     fwd_times = {"chain": fwd_ms(0), "megakernel": fwd_ms(1)}
     mk = args.megakernel
@@ -283,8 +303,6 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
-    moe.moe_trace_reset()
-    moe.moe_trace_enable(True)
     sampler.start()
     time.sleep(0.3)
     barrier()
@@ -295,10 +313,23 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     clocks = sampler.stop()
-    moe.moe_trace_enable(False)
-    trace = moe.moe_trace_read()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     value = job_tokens_per_s(cfg.T, world, ms)
+
+    # ---- per-kernel times: the library's CUDA events around each launch, on
+    # the stream it is launched on, over as many more steps.  The backward's
+    # B/W overlap is switched off for this pass: with it on, the events of a
+    # weight-gradient GEMM on the second stream would also span its wait for
+    # the SMs that dX holds.  Nothing else differs from the timed steps.
+    overlap = moe.moe_set_bwd_overlap(False)
+    moe.moe_trace_reset()
+    moe.moe_trace_enable(True)
+    for _ in range(args.steps):
+        step()
+    barrier()
+    moe.moe_trace_enable(False)
+    trace = moe.moe_trace_read()
+    moe.moe_set_bwd_overlap(overlap)
 
     # ---- end to end through the C ABI with host buffers: every step uploads
     # its inputs (x, logits, dy) from pinned host memory and reads its
@@ -389,7 +420,11 @@ def run_ours(args):
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
                 "frac": None, "peak_source": peak_src}
-    roof["traffic"] = traffic_from_profiles(dom, cfg.name)
+    gemm_kind = {"gemm1_swiglu": 0, "gemm2_scale": 1, "gemm_dh": 2, "gemm_dx": 3, "gemm_dw13": 4, "gemm_dw2": 5}
+    cta_group = 1 + ((pair_kinds >> gemm_kind[dom]) & 1) if dom in gemm_kind else None
+    roof["traffic"] = traffic_from_profiles(dom, cfg.name, cta_group)
+    if cta_group:
+        roof["cta_group"] = cta_group
     roof["share"] = trace[dom][0] / total_ms
     kernels = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1], "share": v[0] / total_ms} for k, v in trace.items()}
     gemm_ms = sum(trace[k][0] for k in flops if k in trace) / args.steps
@@ -397,10 +432,13 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg, mk, pair_kinds),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg, mk),
             "e2e": e2e, "gpu_launches": int(sum(v[1] for v in trace.values())),
             "roofline": roof, "clocks": clocks,
-            "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "kernels": kernels}
+            "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "kernels": kernels,
+            "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap},
+            "kernel_timing": "per-launch CUDA events on the launching stream over --steps further steps run with "
+                             "the backward's B/W overlap off (the timed steps run with it on)"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -20,6 +21,32 @@ using namespace moe;
 namespace {
 
 int g_grid_limit = 0;
+int g_bwd_overlap = 1;
+
+// Per device: a second stream and two events for the backward's fork/join
+// (weight gradients beside the input-gradient tail).  Created on first use,
+// kept until exit.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mu;
+
+const SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return ss.s = nullptr, nullptr;
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+  }
+  return &ss;
+}
 
 int persistent_grid() {
   const int n = num_sms();
@@ -134,6 +161,17 @@ int moe_set_grid_limit(int n) {
 }
 
 int moe_set_gemm_pair_kinds(int mask) { return set_gemm_pair_kinds(mask); }
+
+int moe_set_bwd_overlap(int on) {
+  const int prev = g_bwd_overlap;
+  g_bwd_overlap = on != 0;
+  return prev;
+}
+
+int moe_set_gemm_prefetch(int kind, int kblocks) {
+  if (kind < kG1 || kind > kDW2) return MOE_ERR_ARG;
+  return set_gemm_prefetch(static_cast<GemmKind>(kind), kblocks);
+}
 
 int moe_gemm_pair_capacity(int kind) {
   if (kind < kG1 || kind > kDW2) return 0;
@@ -342,9 +380,31 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
   a.dW1_out = dW1;
   a.dW3_out = dW3;
   a.dW2_out = dW2;
+  // B/W split (GraphPP page, section 2: the backward splits into its
+  // input-gradient part B and its deferrable weight-gradient part W): the W
+  // GEMMs need only dH's outputs, so with which == 3 they run on a second
+  // stream forked after dH and fill the SMs that dX's tail frees and that
+  // the memory-bound dx sum and router backward leave idle.  The streams
+  // join before return; no arithmetic moves, so the bits are unchanged.
+  const SideStream* side = (which == 3 && g_bwd_overlap) ? side_stream() : nullptr;
+  if (which == 3 && g_bwd_overlap && !side) return MOE_ERR_CUDA;
   if (which & 1) {  // B part: input gradients (critical path)
     MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, R, c.d_model, G, MOE_K_COMBINE_BWD, s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
+    if (side) {
+      MOE_TRY_CUDA(cudaEventRecord(side->fork, s));
+      MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));  // queued first: it has the SMs first
+      MOE_TRY_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+      MOE_TRY(launch_gemm(kDW13, a, side->s, persistent_grid()));
+      MOE_TRY(launch_gemm(kDW2, a, side->s, persistent_grid()));
+      MOE_TRY_CUDA(cudaEventRecord(side->join, side->s));
+      MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
+      MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+      MOE_TRY_CUDA(
+          launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, s));
+      MOE_TRY_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+      return MOE_OK;
+    }
     MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
     MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
     MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));

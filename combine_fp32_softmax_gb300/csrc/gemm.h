@@ -55,6 +55,11 @@ int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_overr
 // 128-row tile.  Returns the previous mask.
 int set_gemm_pair_kinds(int mask);
 
+// K blocks of each CTA's next tile that kind `kind` prefetches into L2 while
+// loading the current one (0 = none, at most 64).  Returns the previous
+// value, or -1 for an unknown kind.
+int set_gemm_prefetch(GemmKind kind, int kblocks);
+
 // CTA pairs of `kind` that fit on the device at once (0 on error).
 int gemm_pair_capacity(GemmKind kind);
 

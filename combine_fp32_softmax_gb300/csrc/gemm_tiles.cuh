@@ -68,6 +68,7 @@ struct GemmParams {
   int K;       // ragged-M kinds: reduction length
   int nt_dh;   // dH: column tiles per row (number of partial dot products)
   int has_ab;  // GEMM 1: save [a|b]
+  int prefetch_kb;  // K blocks of a CTA's next tile brought into L2 ahead of its loads
   const int32_t* offsets;
   const int32_t* row_slot;
   const float* topk_w;
@@ -275,11 +276,14 @@ __device__ __forceinline__ int k_steps(const TileInfo& t, int kb) {
 // (all 256 columns for CG = 1; columns [128 rank, 128 rank + 128) for
 // CG = 2).  Boxes that fall outside a tensor are zero-filled.  `to_even`:
 // completion is counted on the pair's even CTA's barrier.
-template <int KIND, int CG = 1>
+// PREFETCH: the same boxes are only brought into L2.
+template <int KIND, int CG = 1, bool PREFETCH = false>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& t, int kb, uint8_t* sA,
                                             uint8_t* sB, uint64_t* bar, int rank = 0, bool to_even = false) {
   auto tma_load_2d = [&](void* dst, const CUtensorMap* map, uint64_t* b, int c0, int c1) {
-    if (CG == 2 && to_even)
+    if constexpr (PREFETCH)
+      tma_prefetch_2d(map, c0, c1);
+    else if (CG == 2 && to_even)
       tma_load_2d_to_even(dst, map, b, c0, c1);
     else
       moe::tma_load_2d(dst, map, b, c0, c1);
@@ -702,6 +706,15 @@ __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo
     }
   }
   return true;
+}
+
+// The first K blocks of a tile this CTA will load next, into L2: the loads
+// of the current tile then overlap the DRAM latency of the next one (short-K
+// tiles of a new segment otherwise all start with misses).
+template <int KIND, int CG = 1>
+__device__ __forceinline__ void prefetch_tile(const GemmParams& p, const TileInfo& t, int rank = 0) {
+  const int n = min(t.nkb, p.prefetch_kb);
+  for (int kb = 0; kb < n; ++kb) issue_loads<KIND, CG, true>(p, t, kb, nullptr, nullptr, nullptr, rank);
 }
 
 // Lets every copy the producer issued land before the CTA may exit.

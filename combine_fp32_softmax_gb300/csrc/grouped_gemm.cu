@@ -59,10 +59,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       tma_prefetch_desc(&p.tmA0);
       tma_prefetch_desc(&p.tmB0);
       ProducerState ps;
-      for (int tile = first; tile < total && !*abort; tile += step)
+      for (int tile = first; tile < total && !*abort; tile += step) {
+        if (p.prefetch_kb > 0 && tile + step < total)
+          prefetch_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile + step, rank), rank);
         if (!produce_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
                                          where0 | tile, rank))
           break;
+      }
       if (*abort) producer_drain(ss, ps);
     }
   } else if (warp == 1) {
@@ -91,7 +94,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
 }
 
-int g_pair_kinds = (1 << 6) - 1;  // kinds that run on CTA pairs (bit = GemmKind)
+// Kinds that run on CTA pairs (bit = GemmKind): measured at the 8192-token
+// DeepSeek-V2-Lite-like shape, pairs win for GEMM 1, GEMM 2, dH and dX; the
+// ragged-K weight-gradient kinds are faster one CTA per tile.
+int g_pair_kinds = (1 << kG1) | (1 << kG2) | (1 << kDH) | (1 << kDX);
+int g_prefetch_kb[6] = {0, 0, 0, 0, 0, 0};  // per kind: next-tile K blocks prefetched into L2
 
 // Launch configuration of one kind; CG = 2 adds the cluster dimension.
 template <int KIND, int CG>
@@ -134,6 +141,7 @@ template <int KIND, int CG>
 int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
   GemmParams p;
   if (!fill_params<KIND, CG>(a, p)) return MOE_ERR_CUDA;
+  p.prefetch_kb = g_prefetch_kb[KIND];
   constexpr int kSmem = smem_bytes<KIND, CG>();
   static_assert(kSmem <= 232448, "shared memory budget of one CTA");
   auto kern = grouped_gemm_kernel<KIND, CG>;
@@ -187,6 +195,13 @@ int gemm_pair_capacity(GemmKind kind) {
     case kDW2: return pair_capacity<kDW2>();
   }
   return 0;
+}
+
+int set_gemm_prefetch(GemmKind kind, int kblocks) {
+  if (kind < kG1 || kind > kDW2) return -1;
+  const int prev = g_prefetch_kb[kind];
+  g_prefetch_kb[kind] = kblocks < 0 ? 0 : (kblocks > 64 ? 64 : kblocks);
+  return prev;
 }
 
 int set_gemm_pair_kinds(int mask) {

@@ -124,6 +124,14 @@ __device__ __forceinline__ void mbar_arrive_rank(uint64_t* bar, uint32_t rank) {
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Brings one box of a tensor into L2 without touching shared memory (no
+// completion to wait for; boxes outside the tensor are ignored).
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
 // 2D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes.  c0 is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int c0, int c1) {

@@ -28,6 +28,10 @@ class MoeError(RuntimeError):
         self.code = code
 
 
+class moe_tune_result(ctypes.Structure):
+    _fields_ = [("pair", ctypes.c_int * 6), ("prefetch_kb", ctypes.c_int * 6), ("us", ctypes.c_float * 6)]
+
+
 class moe_cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("T", "d_model", "d_ff", "E", "k", "n_shared", "renorm")]
 
@@ -60,6 +64,9 @@ _SIGS = {
     "moe_set_grid_limit": ([_I], _I),
     "moe_set_gemm_pair_kinds": ([_I], _I),
     "moe_gemm_pair_capacity": ([_I], _I),
+    "moe_set_gemm_prefetch": ([_I, _I], _I),
+    "moe_set_bwd_overlap": ([_I], _I),
+    "moe_autotune": ([_CFG] + [_P] * 15 + [_I, _P, ctypes.POINTER(moe_tune_result)], _I),
     "moe_debug_skip_megakernel_task": ([_I], _I),
     "moe_debug_megakernel_trace": ([_P, _I], _I),
     "moe_trace_enable": ([_I], _I),
@@ -208,6 +215,30 @@ ALL_PAIR_KINDS = (1 << len(GEMM_KINDS)) - 1
 def moe_set_gemm_pair_kinds(mask: int) -> int:
     """Bit k: grouped-GEMM kind GEMM_KINDS[k] on CTA pairs. Returns the previous mask."""
     return int(lib().moe_set_gemm_pair_kinds(int(mask)))
+
+
+def moe_set_gemm_prefetch(kind: int, kblocks: int) -> int:
+    """Next-tile K blocks grouped-GEMM kind `kind` prefetches into L2. Returns the previous depth."""
+    r = int(lib().moe_set_gemm_prefetch(int(kind), int(kblocks)))
+    if r < 0:
+        raise MoeError("moe_set_gemm_prefetch", r)
+    return r
+
+
+def moe_autotune(cfg, logits, x, W1, W3, W2, dy, y, topk_idx, topk_w, dx, dlogits, dW1, dW3, dW2, ws,
+                 reps=0, stream=None) -> dict:
+    """Times each grouped-GEMM kind under every candidate on this layer, applies the fastest
+    per kind, and returns {kind name: (pair, prefetch_kb, us)}."""
+    res = moe_tune_result()
+    _call("moe_autotune", _cfg(cfg), _ptr(logits), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), _ptr(y),
+          _ptr(topk_idx), _ptr(topk_w), _ptr(dx), _ptr(dlogits), _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(ws),
+          int(reps), _stream(stream), ctypes.byref(res))
+    return {name: (res.pair[i], res.prefetch_kb[i], res.us[i]) for i, name in enumerate(GEMM_KINDS)}
+
+
+def moe_set_bwd_overlap(on: bool) -> int:
+    """Weight-gradient GEMMs of the backward on a second stream beside the dX tail. Returns the previous setting."""
+    return int(lib().moe_set_bwd_overlap(int(bool(on))))
 
 
 def moe_gemm_pair_capacity(kind: int) -> int:

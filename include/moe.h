@@ -254,15 +254,66 @@ int moe_num_sms(void);
  * it exists to test exactly that.  Process-wide, not thread-safe. */
 int moe_set_grid_limit(int n);
 
+/* B/W overlap of moe_layer_bwd with which == 3 (GraphPP page, section 2:
+ * input gradients B on the critical path, weight gradients W deferrable).
+ * On (the default), the dW GEMMs run on a second stream that the library
+ * owns (one per device, created on first use, kept until exit), forked from
+ * the caller's stream after the dH GEMM and joined back before the call
+ * returns, so the caller's stream still orders everything; they then fill
+ * the SMs that the dX GEMM's tail frees and that the memory-bound dx sum and
+ * router backward leave idle.  Off runs everything on the caller's stream.
+ * The bits are the same either way.  Returns the previous setting.
+ * Process-wide, not thread-safe. */
+int moe_set_bwd_overlap(int on);
+
 /* Selects, per grouped-GEMM kind, the tile shape: bit k of `mask` set runs
  * kind k on CTA pairs (thread-block clusters of two; the pair computes a
  * 256 x 256 tile with tcgen05 MMAs of the CTA group of two, each CTA holding
  * half of A and half of B); clear runs it one CTA per 128 x 256 tile.  Bits:
  * 0 GEMM 1 (gate/up), 1 GEMM 2 (down), 2 dH, 3 dX, 4 dW1/dW3, 5 dW2.  The
- * default is all six.  Results are the same bits either way: every output
- * element is the same fp32 sum over K in the same order.  Returns the
- * previous mask.  Process-wide, not thread-safe. */
+ * default is bits 0-3, what measures fastest on a DeepSeek-V2-Lite-like
+ * layer (T=8192, d=2048, f=1408, E=64, k=6, S=2); moe_autotune picks per
+ * layer.  Results are the same bits either way: every output element is the
+ * same fp32 sum over K in the same order.  Returns the previous mask.
+ * Process-wide, not thread-safe. */
 int moe_set_gemm_pair_kinds(int mask);
+
+/* Prefetch depth of grouped-GEMM kind `kind` (numbered as above): while a
+ * CTA loads a tile, it brings the first `kblocks` K blocks (64 deep) of its
+ * next tile into L2 (0 = none; clamped to [0, 64]).  A performance knob only:
+ * results are unchanged.  Returns the previous depth, or MOE_ERR_ARG for an
+ * unknown kind.  Process-wide, not thread-safe. */
+int moe_set_gemm_prefetch(int kind, int kblocks);
+
+/* ------------------------------------------------------------ autotuner
+ * UniEP page ("Unified Expert-Parallel MoE MegaKernel for LLM Training"),
+ * section 3 names autotuning and an analytical model without giving their
+ * content.  moe_autotune measures instead: for each grouped-GEMM kind it times
+ * the caller's own layer (forward + backward, kernel chain) under each
+ * candidate (one CTA per tile or CTA pairs; next-tile L2 prefetch depth 0, 4
+ * or 8 K blocks), keeps the fastest per kind, applies it process-wide through
+ * moe_set_gemm_pair_kinds / moe_set_gemm_prefetch, and reports it.
+ *
+ * Arguments are those of moe_layer_fwd and moe_layer_bwd (all device memory
+ * owned by the caller, layouts as there); every output and `ws` are
+ * overwritten as by a normal forward + backward.  `reps` timed steps per
+ * candidate (0 = 2), after one warm-up step each, with the backward's B/W
+ * overlap off (restored afterwards) so each kernel is timed alone.
+ * Synchronizes `stream` (host-blocking) and resets the kernel-timing totals
+ * (moe_trace_*).
+ * Choices never change results: the outputs after tuning are the same bits.
+ * On error the previous settings are restored and the error is returned. */
+typedef struct {
+  int pair[6];         /* per kind (numbered as above): 1 = CTA pairs */
+  int prefetch_kb[6];  /* per kind: next-tile K blocks prefetched into L2 */
+  float us[6];         /* per kind: measured microseconds per launch of the choice */
+} moe_tune_result;
+
+int moe_autotune(const moe_cfg* cfg, const float* logits, const uint16_t* x,
+                 const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                 const uint16_t* dy, float* y, int32_t* topk_idx, float* topk_w,
+                 float* dx, float* dlogits, float* dW1, float* dW3, float* dW2,
+                 void* ws, int reps, void* stream, moe_tune_result* out);
 
 /* Number of CTA pairs of grouped-GEMM kind `kind` (numbered as above) that
  * the current device holds at once; the pair-mode launches use that many

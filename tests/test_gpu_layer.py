@@ -10,8 +10,8 @@ from combine_fp32_softmax_gb300 import moe
 from combine_fp32_softmax_gb300.configs import DSV2_LITE, LONG128K, MIXTRAL, SKEWED, TINY, MoEConfig
 from combine_fp32_softmax_gb300.inputs import make_layer_inputs
 from oracle import moe_oracle as O
-from tests.gpu_util import (DEV, assert_grad_close, assert_layer_close, device_error, np64, run_layer,
-                            to_dev)
+from tests.gpu_util import (DEV, assert_grad_close, assert_layer_close, device_error, empty_outputs, np64,
+                            run_layer, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -90,6 +90,86 @@ def test_cta_pair_tiles_equal_single_cta_tiles_bitwise(cfg):
         assert torch.equal(a[k], b[k]), k
     for name in ("H", "AB", "Op", "dAB", "Hw"):
         assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
+
+
+def _gemm_settings():
+    mask = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
+    moe.moe_set_gemm_pair_kinds(mask)
+    depths = []
+    for k in range(len(moe.GEMM_KINDS)):
+        depths.append(moe.moe_set_gemm_prefetch(k, 0))
+        moe.moe_set_gemm_prefetch(k, depths[-1])
+    return mask, depths
+
+
+def _restore_gemm_settings(saved):
+    mask, depths = saved
+    moe.moe_set_gemm_pair_kinds(mask)
+    for k, d in enumerate(depths):
+        moe.moe_set_gemm_prefetch(k, d)
+
+
+@pytest.mark.parametrize("depth", [4, 16])
+def test_next_tile_l2_prefetch_keeps_bits(depth):
+    """Prefetching the next tile's K blocks into L2 only moves data earlier."""
+    cfg = WIDE
+    g = to_dev(make_layer_inputs(cfg, seed=20))
+    saved = _gemm_settings()
+    try:
+        a, _ = run_layer(cfg, g)
+        for k in range(len(moe.GEMM_KINDS)):
+            moe.moe_set_gemm_prefetch(k, depth)
+        b, wsb = run_layer(cfg, g, fill=float("nan"))
+    finally:
+        _restore_gemm_settings(saved)
+    assert device_error(wsb) == (0, 0)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_autotune_chooses_per_kind_and_keeps_bits():
+    """The measured autotuner returns a valid choice for every grouped-GEMM
+    kind, applies it, and the layer's outputs afterwards are the same bits."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=19))
+    saved = _gemm_settings()
+    try:
+        ref, ws = run_layer(cfg, g)
+        ref = {k: v.clone() for k, v in ref.items()}
+        o = empty_outputs(cfg)
+        res = moe.moe_autotune(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], g["dy"], o["y"], o["topk_idx"],
+                               o["topk_w"], o["dx"], o["dlogits"], o["dW1"], o["dW3"], o["dW2"], ws)
+        assert set(res) == set(moe.GEMM_KINDS)
+        for name, (pair, depth, us) in res.items():
+            assert pair in (0, 1) and depth in (0, 4, 8) and us > 0, (name, pair, depth, us)
+        mask, depths = _gemm_settings()
+        assert mask == sum(res[n][0] << i for i, n in enumerate(moe.GEMM_KINDS))
+        assert depths == [res[n][1] for n in moe.GEMM_KINDS]
+        tuned, ws2 = run_layer(cfg, g, fill=float("nan"))
+    finally:
+        _restore_gemm_settings(saved)
+    assert device_error(ws2) == (0, 0)
+    for k in ref:
+        assert torch.equal(ref[k], tuned[k]), k
+
+
+@pytest.mark.parametrize("cfg", [MID, SKEW], ids=lambda c: c.name)
+def test_bw_overlap_on_a_second_stream_keeps_bits(cfg):
+    """The weight-gradient GEMMs on the library's second stream (forked after
+    dH, joined before return) give the same bits as the single-stream order,
+    and the caller's stream alone orders the results."""
+    g = to_dev(make_layer_inputs(cfg, seed=21))
+    prev = moe.moe_set_bwd_overlap(False)
+    try:
+        a, _ = run_layer(cfg, g)
+        moe.moe_set_bwd_overlap(True)
+        b, wsb = run_layer(cfg, g, fill=float("nan"))
+        c = {k: v.clone() for k, v in b.items()}  # read right after the call, ordered by the stream only
+    finally:
+        moe.moe_set_bwd_overlap(prev)
+    assert device_error(wsb) == (0, 0)
+    for k in a:
+        assert torch.equal(a[k], c[k]), k
 
 
 def test_b_and_w_parts_split():
