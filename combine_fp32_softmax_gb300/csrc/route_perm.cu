@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -23,7 +25,10 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kRouteWarps = 8;
+// One warp per token: a token's softmax and top-k are a serial chain of
+// shuffles, so the parallelism is in the tokens (a block is the 32 tokens of
+// one histogram block).
+constexpr int kRouteWarps = kRouteTokensPerBlock;
 constexpr int kMaxRowsPerToken = 12;  // k <= 8 routed + S <= 4 shared
 
 // Softmax statistics of one logit row held lane-strided by a warp
@@ -36,13 +41,24 @@ struct RowSoftmax {
   float m, s;     // max, sum of ex
 };
 
+// One logit row, lane-strided (-inf beyond E).
 template <int EPL>
-__device__ __forceinline__ bool row_softmax(const float* __restrict__ row, int E, int lane, RowSoftmax<EPL>& r) {
+__device__ __forceinline__ void row_load(const float* __restrict__ row, int E, int lane, float (&v)[EPL]) {
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? row[e] : -INFINITY;
+  }
+}
+
+// Softmax statistics of the row already in r.v; false if it holds a
+// non-finite logit.
+template <int EPL>
+__device__ __forceinline__ bool row_stats(int E, int lane, RowSoftmax<EPL>& r) {
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    r.v[i] = (e < E) ? row[e] : -INFINITY;
     if (e < E && !isfinite(r.v[i])) bad = true;
   }
   bad = __any_sync(kFull, bad);
@@ -68,6 +84,12 @@ __device__ __forceinline__ bool row_softmax(const float* __restrict__ row, int E
 }
 
 template <int EPL>
+__device__ __forceinline__ bool row_softmax(const float* __restrict__ row, int E, int lane, RowSoftmax<EPL>& r) {
+  row_load<EPL>(row, E, lane, r.v);
+  return row_stats<EPL>(E, lane, r);
+}
+
+template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
     route_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm, int32_t* __restrict__ topk_idx,
                  float* __restrict__ topk_w, int32_t* __restrict__ hist, int nb, int* err) {
@@ -76,13 +98,25 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
   const int tok0 = blockIdx.x * kRouteTokensPerBlock;
-  for (int tt = warp; tt < kRouteTokensPerBlock; tt += kRouteWarps) {
-    const int t = tok0 + tt;
+  // Every row of this warp's tokens is loaded before the first is routed
+  // (one memory latency, not one per token, should a warp hold several).
+  constexpr int kTPW = kRouteTokensPerBlock / kRouteWarps;
+  float rows[kTPW][EPL];
+#pragma unroll
+  for (int q = 0; q < kTPW; ++q) {
+    const int t = tok0 + warp + q * kRouteWarps;
+    if (t < T) row_load<EPL>(logits + static_cast<size_t>(t) * E, E, lane, rows[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < kTPW; ++q) {
+    const int t = tok0 + warp + q * kRouteWarps;
     if (t >= T) break;
     RowSoftmax<EPL> r;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) r.v[i] = rows[q][i];
     int my_idx = lane;  // placeholder routing for a rejected row: slot j -> expert j
     float my_w = 0.f;
-    if (!row_softmax<EPL>(logits + static_cast<size_t>(t) * E, E, lane, r)) {
+    if (!row_stats<EPL>(E, lane, r)) {
       if (lane == 0) record_error(err, MOE_ERR_NONFINITE_CODE, t);
     } else {
       uint32_t taken = 0;
@@ -165,41 +199,77 @@ __global__ void __launch_bounds__(256)
 // One flat exclusive scan of the expert-major [E][nb] histogram: at (e, b)
 // it equals offsets[e] + (slots of expert e in blocks < b), i.e. the base
 // address of block b's first slot for expert e.
-__global__ void __launch_bounds__(1024)
+// The flat array hist[E][nb] is scanned by one 1024-thread block in tiles
+// of kScanTile entries: each tile is loaded coalesced into shared memory
+// (entry i at i + i/32, so a warp reading 8 consecutive entries per thread
+// hits every bank once), each thread sums its 8 entries, a two-level warp
+// shuffle scan gives every thread its exclusive prefix, and the prefixes go
+// back out coalesced; a carry runs across tiles.
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 8;
+constexpr int kScanTile = kScanThreads * kScanPer;
+
+__global__ void __launch_bounds__(kScanThreads)
     scan_kernel(const int32_t* __restrict__ hist, int E, int nb, int R, int32_t* __restrict__ base,
                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int tile[kScanTile + kScanTile / 32];
   __shared__ int warp_tot[32];
+  __shared__ int tile_total;
   const int n = E * nb;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (n + 1023) / 1024;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int local = 0;
-  for (int i = lo; i < hi; ++i) local += hist[i];
-  int incl = local;
+  int carry = 0;
+  for (int t0 = 0; t0 < n; t0 += kScanTile) {
+    const int m = min(kScanTile, n - t0);
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, off);
-    if (lane >= off) incl += y;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    const int v = warp_tot[lane];
-    int inc = v;
+    for (int j = 0; j < kScanPer; ++j) {
+      const int i = tid + j * kScanThreads;
+      tile[i + (i >> 5)] = i < m ? hist[t0 + i] : 0;
+    }
+    __syncthreads();
+    int v[kScanPer];
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      const int i = tid * kScanPer + j;
+      v[j] = tile[i + (i >> 5)];
+      local += v[j];
+    }
+    int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(kFull, inc, off);
-      if (lane >= off) inc += y;
+      const int y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
     }
-    warp_tot[lane] = inc - v;
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      const int x = warp_tot[lane];
+      int inc = x;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, inc, off);
+        if (lane >= off) inc += y;
+      }
+      warp_tot[lane] = inc - x;
+      if (lane == 31) tile_total = inc;
+    }
+    __syncthreads();
+    int run = carry + warp_tot[w] + incl - local;
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      const int i = tid * kScanPer + j;
+      tile[i + (i >> 5)] = run;
+      run += v[j];
+    }
+    carry += tile_total;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) {
+      const int i = tid + j * kScanThreads;
+      if (i < m) base[t0 + i] = tile[i + (i >> 5)];
+    }
+    __syncthreads();  // tile[], warp_tot and tile_total are rewritten by the next tile
   }
-  __syncthreads();
-  int run = warp_tot[w] + incl - local;
-  for (int i = lo; i < hi; ++i) {
-    base[i] = run;
-    run += hist[i];
-  }
-  __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
     const int b0 = base[static_cast<size_t>(e) * nb];
     const int b1 = (e + 1 < E) ? base[static_cast<size_t>(e + 1) * nb] : R;
@@ -307,6 +377,11 @@ __global__ void __launch_bounds__(256)
 // token is a template parameter so the loads of every row (two float4 per
 // lane per step) are in registers with no spare slots, which keeps enough
 // warps resident to stream at HBM rate.
+// A warp's unit of work is one token's span of kSumSpan float4 columns, so
+// the work divides into many more units than there are resident warps and
+// the last wave is short; the grid is the resident capacity.
+constexpr int kSumSpan = 128;
+
 template <int NR>
 __global__ void __launch_bounds__(256)
     sum_rows_f32_kernel(const float4* __restrict__ rows, const int32_t* __restrict__ sel, int T, int k, int S,
@@ -315,7 +390,12 @@ __global__ void __launch_bounds__(256)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const long long R = static_cast<long long>(T) * k;
   const long long nrows = R + static_cast<long long>(S) * T;
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+  const int spans = (nvec + kSumSpan - 1) / kSumSpan;
+  const int units = T * spans;  // < 2^31: checked by the launcher
+  for (int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += nwarps) {
+    const int t = u / spans;
+    const int v0 = (u - t * spans) * kSumSpan;
+    const int v1 = min(nvec, v0 + kSumSpan);
     long long myrow = 0;
     if (lane < k) {
       myrow = sel[static_cast<size_t>(t) * k + lane];
@@ -327,8 +407,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < NR; ++j) base[j] = rows + static_cast<size_t>(__shfl_sync(kFull, myrow, j)) * nvec;
     float4* o = out + static_cast<size_t>(t) * nvec;
-    for (int v = lane; v < nvec; v += 64) {
-      const bool two = v + 32 < nvec;
+    for (int v = v0 + lane; v < v1; v += 64) {
+      const bool two = v + 32 < v1;
       float4 val[NR], val2[NR];
 #pragma unroll
       for (int j = 0; j < NR; ++j) {
@@ -488,12 +568,27 @@ cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int
 cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
                                 int trace_kind, cudaStream_t s) {
   TraceScope trace_scope(trace_kind, s);
-  const int blocks = min(ceil_div(T, 8), num_sms() * 8);
+  const long long units = static_cast<long long>(T) * ceil_div(d / 4, kSumSpan);
+  if (units >= (1ll << 31)) return cudaErrorInvalidValue;
   const float4* r4 = reinterpret_cast<const float4*>(rows);
   float4* o4 = reinterpret_cast<float4*>(out);
+  // Grid: the blocks that are resident at once (cached per row count), or
+  // fewer when there is less work.
+  auto grid_for = [&](auto kern, int nr) {
+    static int resident[kMaxRowsPerToken + 1] = {0};
+    if (resident[nr] == 0) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+      resident[nr] = per_sm * num_sms();
+    }
+    return static_cast<int>(std::min<long long>(ceil_div(units, 8), resident[nr]));
+  };
   switch (k + S) {
 #define MOE_SUM_ROWS_CASE(N) \
-  case N: sum_rows_f32_kernel<N><<<blocks, 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4); break;
+  case N:                                                                                           \
+    sum_rows_f32_kernel<N><<<grid_for(sum_rows_f32_kernel<N>, N), 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4); \
+    break;
     MOE_SUM_ROWS_CASE(1)
     MOE_SUM_ROWS_CASE(2)
     MOE_SUM_ROWS_CASE(3)
