@@ -41,6 +41,8 @@ def parse_args():
     ap.add_argument("--workload", default="dsv2lite_T8192_d2048_f1408_E64_k6_S2")
     ap.add_argument("--megakernel", type=int, default=-1, help="1: forward MegaKernel, 0: kernel chain, "
                     "-1: MegaKernel when the library provides it")
+    ap.add_argument("--bwd-megakernel", type=int, default=-1, help="1: backward input part as one MegaKernel, "
+                    "0: kernel chain, -1: the faster of the two (same bits)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
@@ -283,11 +285,34 @@ def run_ours(args):
     if mk < 0:  # the faster forward of the two (same bits either way)
         mk = 1 if fwd_times["megakernel"] < fwd_times["chain"] else 0
 
+    def bwd_ms(use_mk, iters=5):
+        """Device time of the backward alone (kernel chain or MegaKernel input part)."""
+        which = 3 | (moe.MOE_BWD_MEGAKERNEL if use_mk else 0)
+
+        def one():
+            moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["idx"], out["w"],
+                              ws, out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], which=which)
+        for _ in range(2):
+            one()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            one()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / iters
+
+    bwd_times = {"chain": bwd_ms(0), "megakernel": bwd_ms(1)}
+    bmk = args.bwd_megakernel
+    if bmk < 0:
+        bmk = 1 if bwd_times["megakernel"] < bwd_times["chain"] else 0
+    bwd_which = 3 | (moe.MOE_BWD_MEGAKERNEL if bmk else 0)
+
     def step(src=g):
         moe.moe_layer_fwd(cfg, src["logits"], src["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
                           ws, use_megakernel=mk)
         moe.moe_layer_bwd(cfg, src["dy"], src["logits"], src["x"], g["W1"], g["W3"], g["W2"], out["idx"], out["w"],
-                          ws, out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], which=3)
+                          ws, out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], which=bwd_which)
 
     def barrier():
         if world > 1:
@@ -369,7 +394,7 @@ def run_ours(args):
                                   out["idx"], out["w"], ws, use_megakernel=mk)
                 moe.moe_layer_bwd(cfg, srcs[b]["dy"], srcs[b]["logits"], srcs[b]["x"], g["W1"], g["W3"], g["W2"],
                                   out["idx"], out["w"], ws, o["dx"], o["dz"], out["dW1"], out["dW3"], out["dW2"],
-                                  which=3)
+                                  which=bwd_which)
                 done[b].record(stream)
                 if i + 1 < nsteps:
                     with torch.cuda.stream(up):
@@ -435,7 +460,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(cfg, mk),
             "e2e": e2e, "gpu_launches": int(sum(v[1] for v in trace.values())),
             "roofline": roof, "clocks": clocks,
-            "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "kernels": kernels,
+            "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "bwd_ms": bwd_times,
+            "bwd_megakernel": bmk, "kernels": kernels,
             "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap},
             "kernel_timing": "per-launch CUDA events on the launching stream over --steps further steps run with "
                              "the backward's B/W overlap off (the timed steps run with it on)"}

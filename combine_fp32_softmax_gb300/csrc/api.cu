@@ -14,6 +14,8 @@ namespace moe {
 int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint16_t* x, const uint16_t* W1,
                    const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* y, int grid_limit,
                    cudaStream_t s);
+int megakernel_bwd_input(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs& a, const uint16_t* dy,
+                         float* dx, int grid, cudaStream_t s);
 }
 
 using namespace moe;
@@ -341,6 +343,8 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
                   const uint16_t* W3, const uint16_t* W2, const int32_t* topk_idx, const float* topk_w, void* ws,
                   float* dx, float* dlogits, float* dW1, float* dW3, float* dW2, int which, void* stream) {
   MOE_TRY(check_cfg(cfg));
+  const bool mega = (which & MOE_BWD_MEGAKERNEL) != 0;
+  which &= ~MOE_BWD_MEGAKERNEL;
   if (which < 1 || which > 3) return MOE_ERR_ARG;
   MOE_TRY(check_ptrs({dy, logits, x, W1, W3, W2, topk_idx, topk_w}, {dx, dlogits, dW1, dW3, dW2}, ws));
   if ((which & 1) && !(dx && dlogits)) return MOE_ERR_ARG;
@@ -388,7 +392,22 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
   // join before return; no arithmetic moves, so the bits are unchanged.
   const SideStream* side = (which == 3 && g_bwd_overlap) ? side_stream() : nullptr;
   if (which == 3 && g_bwd_overlap && !side) return MOE_ERR_CUDA;
-  if (which & 1) {  // B part: input gradients (critical path)
+  if ((which & 1) && mega) {  // B part as one MegaKernel, then the two small router-gradient launches
+    MOE_TRY(megakernel_bwd_input(c, L, static_cast<uint8_t*>(ws), a, dy, dx, persistent_grid(), s));
+    if (side) {  // the W GEMMs beside the dw reduce and router backward
+      MOE_TRY_CUDA(cudaEventRecord(side->fork, s));
+      MOE_TRY_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+      MOE_TRY(launch_gemm(kDW13, a, side->s, persistent_grid()));
+      MOE_TRY(launch_gemm(kDW2, a, side->s, persistent_grid()));
+      MOE_TRY_CUDA(cudaEventRecord(side->join, side->s));
+    }
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
+    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+    if (side) {
+      MOE_TRY_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+      return MOE_OK;
+    }
+  } else if (which & 1) {  // B part: input gradients (critical path)
     MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, R, c.d_model, G, MOE_K_COMBINE_BWD, s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
     if (side) {

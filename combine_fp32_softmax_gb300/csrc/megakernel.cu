@@ -1,5 +1,11 @@
-// Forward MegaKernel: dispatch gather -> GEMM 1 (+SiLU*mul) -> GEMM 2
-// (+routing weight) -> combine, as one persistent launch.
+// MegaKernels: one persistent launch for
+//   forward:  dispatch gather -> GEMM 1 (+SiLU*mul) -> GEMM 2 (+routing
+//             weight) -> combine;
+//   backward input part:  combine-bwd gather (G = dy rows) -> dH GEMM
+//             (+SwiGLU backward, dw partials) -> dX GEMM -> slot-order dx sum.
+// Both have the same shape (a row gather, a first grouped GEMM over those
+// rows, a second grouped GEMM over the first one's row blocks, a per-token
+// fp32 sum of the second one's rows), so one kernel template serves both.
 //
 // UniEP page ("Unified Expert-Parallel MoE MegaKernel for LLM Training"),
 // section 2.2: exactly one persistent worker per SM, roles chosen at run time
@@ -8,40 +14,44 @@
 // global-memory scoreboard that marks when every token of a GroupGEMM tile
 // has arrived, which compute workers poll before starting the tile.  On one
 // GPU the communication task is the local dispatch gather; the scoreboard is
-// a set of readiness counters:
+// a set of readiness counters (A, B: the first and second GEMM):
 //   ctr[0]                   ticket cursor
-//   ctr[1]                   GEMM-2 warp-tiles finished (combine waits on all)
-//   ctr[2]                   combine cursor: after the last ticket every warp of
+//   ctr[1]                   B warp-tiles finished (the token sums wait on all)
+//   ctr[2]                   sum cursor: after the last ticket every warp of
 //                            every CTA claims tokens one at a time from it
-//   ctr[kCtrXp + g]          Xp row block g (128 rows) gathered
-//   ctr[kCtrXp + NG + mt]    GEMM-1 warp-tiles finished of m-tile mt
-//                            (GEMM-2 tiles of mt wait for all of them)
+//   ctr[kCtrXp + g]          gathered row block g (128 rows) written
+//   ctr[kCtrXp + NG + mt]    A warp-tiles finished of m-tile mt
+//                            (B tiles of mt wait for all of them)
+// The UniEP page (section 2.2) has its MegaKernels serve the backward steps
+// too; the backward one here is its input-gradient (B) part.
 // A task only ever waits on tasks with lower tickets, and each CTA runs its
 // tasks in ticket order, so the lowest unfinished task can always proceed:
 // no deadlock, with or without co-residency of all CTAs.  Every wait is
 // bounded (1 s) and reports MOE_ERR_TIMEOUT instead of hanging.
 //
 // GEMM tiles run exactly the MMA sequence and epilogue of the stand-alone
-// grouped GEMM kernels and the combine sums in the same order as the
-// combine kernel, so the outputs are bitwise equal to the unfused chain.
+// grouped GEMM kernels and the token sums add in the same order as the
+// stand-alone sum kernel, so the outputs are bitwise equal to the unfused
+// chain.
 #include "gemm_tiles.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kTq = 4;              // depth of the producer -> consumer task FIFO
-constexpr int kGatherRows = 128;    // Xp rows per gather task
+constexpr int kGatherRows = 128;    // gathered rows per gather task
 constexpr int kCtrXp = 8;
 constexpr int kMaxTokRows = 12;     // k <= 8 routed + S <= 4 shared rows per token
+constexpr int kMaxMegaStages = 4;
 
 struct MegaParams {
-  GemmParams g1, g2;
-  const uint16_t* x;
+  GemmParams g1, g2;           // first (A) and second (B) grouped GEMM
+  const uint16_t* x;           // gather source rows (x forward, dy backward)
   const int32_t* row_token;
   const int32_t* dest;
-  uint16_t* Xp;
-  const float* Op;
-  float* y;
+  uint16_t* Xp;                // gathered rows (Xp forward, G backward)
+  const float* Op;             // rows summed per token (O' forward, dXp backward)
+  float* y;                    // token sums (y forward, dx backward)
   int* ctr;
   int NG;
   int skip;  // testing aid: ticket treated as never done (-1: none)
@@ -69,21 +79,29 @@ __device__ __forceinline__ void trace_record(const MegaParams& mp, int role, int
   ++n;
 }
 
-constexpr int kMegaStages = 4;
-// epilogue staging per warp: the larger of GEMM 1's and GEMM 2's
-constexpr int kMegaEpiBytes =
-    Traits<kG1>::EPI_BYTES > Traits<kG2>::EPI_BYTES ? Traits<kG1>::EPI_BYTES : Traits<kG2>::EPI_BYTES;
+// Shapes of one MegaKernel: its two GEMM kinds and its pipeline depth
+// (forward 4 stages; backward 3, as dH's epilogue staging is 18 KB a warp).
+template <int KA, int KB, int NST>
+struct Mega {
+  static constexpr int STAGES = NST;
+  // epilogue staging per warp: the larger of the two kinds'
+  static constexpr int EPI_BYTES =
+      Traits<KA>::EPI_BYTES > Traits<KB>::EPI_BYTES ? Traits<KA>::EPI_BYTES : Traits<KB>::EPI_BYTES;
+};
 
 struct MegaShared {
   SharedState g;
-  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kMegaStages];
+  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kMaxMegaStages];
   int tq[kTq];
   int ntn1, ntn2, nt1, nt2, total;
 };
 
-constexpr int kMegaSmemBytes =
-    kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes + static_cast<int>(sizeof(MegaShared));
-static_assert(kMegaSmemBytes <= 232448, "shared memory budget of one CTA");
+template <int KA, int KB, int NST>
+constexpr int mega_smem_bytes() {
+  return NST * kStageBytes + kEpiWarps * Mega<KA, KB, NST>::EPI_BYTES + static_cast<int>(sizeof(MegaShared));
+}
+static_assert(mega_smem_bytes<kG1, kG2, 4>() <= 232448, "shared memory budget of one CTA");
+static_assert(mega_smem_bytes<kDH, kDX, 3>() <= 232448, "shared memory budget of one CTA");
 
 // Bounded acquire-spin until *c >= target.
 __device__ bool wait_counter(const int* c, int target, volatile int* abort, int* err, int where) {
@@ -112,14 +130,15 @@ __device__ __forceinline__ void warp_signal(int* counter) {
   if ((threadIdx.x & 31) == 0) red_release_gpu_add(counter, 1);
 }
 
-// Gather task g (producer lane): Xp rows [128g, 128g+128) <- x[row_token],
-// row by row with bulk copies through the stage buffers (up to 3 chunks in
-// flight), then publish the block.
+// Gather task g (producer lane): gathered rows [128g, 128g+128) <-
+// source[row_token], row by row with bulk copies through the stage buffers
+// (up to NST-1 chunks in flight), then publish the block.
 struct GatherState {
   uint32_t par = 0;      // next wait parity of gbar[b] (bit b)
   uint32_t pending = 0;  // buffers with loads issued but not yet waited on
 };
 
+template <int NST>
 __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem, int g, GatherState& gs,
                             volatile int* abort, int where) {
   const int d = mp.g1.d;
@@ -130,8 +149,8 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
   const int nchunk = (nrows + rps - 1) / rps;
   for (int c = 0; c <= nchunk; ++c) {
     if (c < nchunk) {
-      const int b = c % kMegaStages;
-      if (c >= kMegaStages) bulk_wait_read<kMegaStages - 2>();  // chunk c-4 finished reading buffer b
+      const int b = c % NST;
+      if (c >= NST) bulk_wait_read<NST - 2>();  // chunk c-NST finished reading buffer b
       const int n = min(rps, nrows - c * rps);
       uint8_t* buf = smem + b * kStageBytes;
       mbar_arrive_expect_tx(&ms.gbar[b], n * rb);
@@ -142,7 +161,7 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
       gs.pending |= 1u << b;
     }
     if (c > 0) {
-      const int pc = c - 1, b = pc % kMegaStages;
+      const int pc = c - 1, b = pc % NST;
       if (!mbar_wait(&ms.gbar[b], (gs.par >> b) & 1, abort, mp.g1.err, where)) return false;
       gs.par ^= 1u << b;
       gs.pending &= ~(1u << b);
@@ -160,21 +179,23 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
 
 __device__ void gather_drain(MegaShared& ms, const GatherState& gs) {
   bulk_wait_all();
-  for (int b = 0; b < kMegaStages; ++b)
+  for (int b = 0; b < kMaxMegaStages; ++b)
     if (gs.pending & (1u << b)) mbar_wait_drain(&ms.gbar[b], (gs.par >> b) & 1);
 }
 
-// GEMM-2 tile t2 described with GEMM-1's segment table (same m-tiles).
+// Tile t2 of the second GEMM described with the first one's segment table
+// (both run over the same rows, so they share m-tiles).
+template <int KA, int KB>
 __device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaShared& ms, int t2) {
   const int mt = t2 / ms.ntn2, nb = t2 - mt * ms.ntn2;
-  TileInfo t = decode_tile<kG1>(mp.g1, ms.g, mt * ms.ntn1);
-  t.n0 = nb * kBN;
+  TileInfo t = decode_tile<KA>(mp.g1, ms.g, mt * ms.ntn1);
+  t.n0 = nb * Traits<KB>::BNE;
   t.nkb = mp.g2.K / kBK;
   return t;
 }
 
-// Combine of one token by one warp: the same fp32 sum, in the same order, as
-// the stand-alone combine kernel.
+// Sum of one token's rows by one warp: the same fp32 sum, in the same order,
+// as the stand-alone sum kernel.
 __device__ void combine_token(const MegaParams& mp, int t) {
   const int lane = threadIdx.x & 31;
   const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R;
@@ -241,14 +262,16 @@ __device__ void combine_phase(const MegaParams& mp, int nt2, volatile int* abort
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_constant__ MegaParams mp) {
+template <int KA, int KB, int NST>
+__global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant__ MegaParams mp) {
+  constexpr int EPI = Mega<KA, KB, NST>::EPI_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // see grouped_gemm_kernel: checked, not padded
     if (threadIdx.x == 0) record_error(mp.g1.err, MOE_ERR_CUDA, 0x5A11);
     return;
   }
   uint8_t* smem = smem_raw;
-  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + kMegaStages * kStageBytes + kEpiWarps * kMegaEpiBytes);
+  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + NST * kStageBytes + kEpiWarps * EPI);
   SharedState& ss = ms.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = mp.g1.err;
@@ -259,17 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       mbar_init(&ms.tq_full[q], 1);
       mbar_init(&ms.tq_empty[q], 1 + kEpiWarps);  // MMA warp + epilogue warps
     }
-    for (int b = 0; b < kMegaStages; ++b) mbar_init(&ms.gbar[b], 1);
+    for (int b = 0; b < NST; ++b) mbar_init(&ms.gbar[b], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(&ss.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  build_segments<kG1>(mp.g1, ss);
+  build_segments<KA>(mp.g1, ss);
   if (threadIdx.x == 0) {
-    ms.ntn1 = (mp.g1.N + 127) / 128;
-    ms.ntn2 = (mp.g2.N + kBN - 1) / kBN;
+    ms.ntn1 = (mp.g1.N + Traits<KA>::BNE - 1) / Traits<KA>::BNE;
+    ms.ntn2 = (mp.g2.N + Traits<KB>::BNE - 1) / Traits<KB>::BNE;
     ms.nt1 = ss.total_tiles;
     ms.nt2 = (ms.nt1 / ms.ntn1) * ms.ntn2;
     ms.total = mp.NG + ms.nt1 + ms.nt2;  // combine is claimed per token afterwards
@@ -307,23 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
         if (id == mp.skip) continue;
         const int where = kW | (1 << 20) | (id & 0xFFFFF);
         if (id < NG) {
-          if (!gather_task(mp, ms, smem, id, gs, abort, where)) break;
+          if (!gather_task<NST>(mp, ms, smem, id, gs, abort, where)) break;
         } else if (id < e1) {
-          const TileInfo t = decode_tile<kG1>(mp.g1, ss, id - NG);
-          if (!t.shared) {  // routed rows come from Xp: wait for their gather blocks
+          const TileInfo t = decode_tile<KA>(mp.g1, ss, id - NG);
+          if (!t.shared) {  // routed rows come from the gathered rows: wait for their blocks
             const int g0 = t.grow0 / kGatherRows, g1 = (t.grow0 + t.rows - 1) / kGatherRows;
             bool ok = true;
             for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], 1, abort, err, where);
             if (!ok) break;
             fence_proxy_async_global();
           }
-          if (!produce_tile<kG1, kMegaStages>(mp.g1, t, ss, smem, ps, abort, where)) break;
+          if (!produce_tile<KA, NST>(mp.g1, t, ss, smem, ps, abort, where)) break;
         } else if (id < e2) {
           const int t2 = id - e1;
           const int mt = t2 / ms.ntn2;
           if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kEpiWarps * ms.ntn1, abort, err, where)) break;
           fence_proxy_async_global();
-          if (!produce_tile<kG2, kMegaStages>(mp.g2, decode_g2(mp, ms, t2), ss, smem, ps, abort, where)) break;
+          if (!produce_tile<KB, NST>(mp.g2, decode_g2<KA, KB>(mp, ms, t2), ss, smem, ps, abort, where)) break;
         }
         trace_record(mp, 0, tn, id, t_claim);
       }
@@ -352,16 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       const int where = kW | (2 << 20) | (id & 0xFFFFF);
       bool ok = true;
       if (id >= NG && id < e1)
-        ok = mma_tile<kG1, kMegaStages>(mp.g1, decode_tile<kG1>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<KA, NST>(mp.g1, decode_tile<KA>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
       else if (id >= e1 && id < e2)
-        ok = mma_tile<kG2, kMegaStages>(mp.g2, decode_g2(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<KB, NST>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
       if (!ok) break;
     }
     if (*abort) mma_drain(ss, mst);
     if (!*abort) combine_phase(mp, nt2, abort, err);
   } else {
     EpiState es;
-    uint8_t* stg = smem + kMegaStages * kStageBytes + (warp & 3) * kMegaEpiBytes;
+    uint8_t* stg = smem + NST * kStageBytes + (warp & 3) * EPI;
     int slot = 0, tn = 0;
     uint32_t tph = 0;
     while (true) {
@@ -379,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
       const int where = kW | (3 << 20) | (id & 0xFFFFF);
       if (id >= NG && id < e1) {
         const int t1 = id - NG;
-        if (!epilogue_step<kG1>(mp.g1, decode_tile<kG1>(mp.g1, ss, t1), ss, tmem, stg, es, abort, where)) break;
+        if (!epilogue_step<KA>(mp.g1, decode_tile<KA>(mp.g1, ss, t1), ss, tmem, stg, es, abort, where)) break;
         warp_signal(&mp.ctr[kCtrXp + NG + t1 / ms.ntn1]);
       } else if (id >= e1 && id < e2) {
-        if (!epilogue_step<kG2>(mp.g2, decode_g2(mp, ms, id - e1), ss, tmem, stg, es, abort, where)) break;
+        if (!epilogue_step<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, tmem, stg, es, abort, where)) break;
         warp_signal(&mp.ctr[1]);
       }
       if (warp == 2 && lane == 0) trace_record(mp, 1, tn, id, t_pop);
@@ -395,6 +418,40 @@ __global__ void __launch_bounds__(kThreads, 1) mega_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Launches MegaKernel <KA, KB, NST> with the two GEMMs' arguments `a`
+// (filled for both kinds), the gather (src rows by row_token into dst) and
+// the token sums (rows of ssrc by dest, into sdst).
+template <int KA, int KB, int NST>
+int mega_launch(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs& a, const uint16_t* gsrc,
+                uint16_t* gdst, const float* ssrc, float* sdst, int grid, int trace_kind, cudaStream_t s) {
+  MegaParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  if (!fill_params<KA>(a, mp.g1) || !fill_params<KB>(a, mp.g2)) return MOE_ERR_CUDA;
+  const long long R = static_cast<long long>(c.T) * c.k;
+  mp.x = gsrc;
+  mp.row_token = reinterpret_cast<const int32_t*>(ws + L.row_token);
+  mp.dest = reinterpret_cast<const int32_t*>(ws + L.dest);
+  mp.Xp = gdst;
+  mp.Op = ssrc;
+  mp.y = sdst;
+  mp.ctr = reinterpret_cast<int*>(ws + L.mk);
+  mp.NG = ceil_div(R, kGatherRows);
+  mp.skip = g_skip_ticket;
+  mp.trace = g_trace_buf;
+  mp.trace_per_cta = g_trace_per_cta;
+  // counters: kCtrXp + NG gather flags + (at most R/128 + E + S*ceil(T/128)) m-tiles
+  const long long need = kCtrXp + mp.NG + R / kBM + c.E + static_cast<long long>(c.n_shared) * ceil_div(c.T, kBM) + 2;
+  if (need > L.mk_ints) return MOE_ERR_SHAPE;
+  if (cudaMemsetAsync(mp.ctr, 0, sizeof(int) * L.mk_ints, s) != cudaSuccess) return MOE_ERR_CUDA;
+  constexpr int kSmem = mega_smem_bytes<KA, KB, NST>();
+  if (cudaFuncSetAttribute(mega_kernel<KA, KB, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  TraceScope trace_scope(trace_kind, s);
+  mega_kernel<KA, KB, NST><<<grid > 0 ? grid : num_sms(), kThreads, kSmem, s>>>(mp);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -421,31 +478,14 @@ int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint1
   a.AB_out = reinterpret_cast<uint16_t*>(ws + L.AB);
   a.Op_out = reinterpret_cast<float*>(ws + L.Op);
   a.err = reinterpret_cast<int*>(ws + L.err);
-  MegaParams mp;
-  std::memset(&mp, 0, sizeof(mp));
-  if (!fill_params<kG1>(a, mp.g1) || !fill_params<kG2>(a, mp.g2)) return MOE_ERR_CUDA;
-  const long long R = static_cast<long long>(c.T) * c.k;
-  mp.x = x;
-  mp.row_token = reinterpret_cast<const int32_t*>(ws + L.row_token);
-  mp.dest = reinterpret_cast<const int32_t*>(ws + L.dest);
-  mp.Xp = reinterpret_cast<uint16_t*>(ws + L.Xp);
-  mp.Op = reinterpret_cast<const float*>(ws + L.Op);
-  mp.y = y;
-  mp.ctr = reinterpret_cast<int*>(ws + L.mk);
-  mp.NG = ceil_div(R, kGatherRows);
-  mp.skip = g_skip_ticket;
-  mp.trace = g_trace_buf;
-  mp.trace_per_cta = g_trace_per_cta;
-  // counters: kCtrXp + NG gather flags + (at most R/128 + E + S*ceil(T/128)) m-tiles
-  const long long need = kCtrXp + mp.NG + R / kBM + c.E + static_cast<long long>(c.n_shared) * ceil_div(c.T, kBM) + 2;
-  if (need > L.mk_ints) return MOE_ERR_SHAPE;
-  if (cudaMemsetAsync(mp.ctr, 0, sizeof(int) * L.mk_ints, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(mega_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaSmemBytes) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  TraceScope trace_scope(MOE_K_MEGAKERNEL, s);
-  mega_fwd_kernel<<<grid > 0 ? grid : num_sms(), kThreads, kMegaSmemBytes, s>>>(mp);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return mega_launch<kG1, kG2, 4>(c, L, ws, a, x, reinterpret_cast<uint16_t*>(ws + L.Xp),
+                                  reinterpret_cast<const float*>(ws + L.Op), y, grid, MOE_K_MEGAKERNEL, s);
+}
+
+int megakernel_bwd_input(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs& a, const uint16_t* dy,
+                         float* dx, int grid, cudaStream_t s) {
+  return mega_launch<kDH, kDX, 3>(c, L, ws, a, dy, reinterpret_cast<uint16_t*>(ws + L.G),
+                                  reinterpret_cast<const float*>(ws + L.dXp), dx, grid, MOE_K_MEGAKERNEL_BWD, s);
 }
 
 }  // namespace moe

@@ -78,7 +78,7 @@ _SIGS = {
 # kernel kinds of the timing trace (MOE_K_* in include/moe.h)
 TRACE_KINDS = ["route", "hist", "scan", "scatter", "gather", "gemm1_swiglu", "gemm2_scale", "combine",
                "combine_bwd", "gemm_dh", "dw_reduce", "route_bwd", "gemm_dx", "dispatch_bwd", "gemm_dw13",
-               "gemm_dw2", "megakernel"]
+               "gemm_dw2", "megakernel", "megakernel_bwd"]
 
 _lib = None
 
@@ -185,6 +185,9 @@ def moe_dispatch_bwd(cfg, dXp, dest, dx, ws, stream=None):
 def moe_route_bwd(cfg, logits, topk_idx, topk_w, dw, dlogits, ws, stream=None):
     _call("moe_route_bwd", _cfg(cfg), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(dw), _ptr(dlogits),
           _ptr(ws), _stream(stream))
+
+
+MOE_BWD_MEGAKERNEL = 4  # add to `which`: the B part as one MegaKernel launch
 
 
 def moe_layer_bwd(cfg, dy, logits, x, W1, W3, W2, topk_idx, topk_w, ws, dx, dlogits, dW1, dW3, dW2,

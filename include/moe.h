@@ -231,7 +231,13 @@ int moe_route_bwd(const moe_cfg* cfg, const float* logits, const int32_t* topk_i
 /* Whole backward from the state moe_layer_fwd left in `ws`.
  * which: 1 = dx and dlogits only (B part), 2 = dW1, dW3, dW2 only (W part;
  * needs a previous which=1 or 3 call on the same ws), 3 = everything.
+ * Plus MOE_BWD_MEGAKERNEL: the B part's combine-bwd gather, dH GEMM, dX GEMM
+ * and slot-order dx sum run as one persistent MegaKernel launch (UniEP page,
+ * section 2.2: its MegaKernels serve the backward steps too), with the same
+ * ticket cursor and readiness counters as the forward one; the dw reduce and
+ * router backward follow as two small launches.  Same bits as without.
  * Outputs not requested may be NULL. */
+#define MOE_BWD_MEGAKERNEL 4
 int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits,
                   const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
                   const uint16_t* W2, const int32_t* topk_idx, const float* topk_w,
@@ -346,7 +352,8 @@ enum {
   MOE_K_GEMM_DW13 = 14,   /* ragged-K grouped GEMM dW1, dW3 */
   MOE_K_GEMM_DW2 = 15,    /* ragged-K grouped GEMM dW2 */
   MOE_K_MEGAKERNEL = 16,  /* forward MegaKernel */
-  MOE_K_COUNT = 17
+  MOE_K_MEGAKERNEL_BWD = 17, /* backward (input-gradient) MegaKernel */
+  MOE_K_COUNT = 18
 };
 /* Testing aid for failure detection (no device fault involved): the forward
  * MegaKernel claims task `ticket` but never runs or signals it, so the

@@ -235,6 +235,60 @@ def test_megakernel_wait_timeout_is_reported_and_context_survives():
         assert torch.equal(ref[k], again[k]), k
 
 
+BWD_MK = 3 | moe.MOE_BWD_MEGAKERNEL
+
+
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_bwd_megakernel_bitwise_equals_kernel_chain(cfg):
+    """The backward input part as one MegaKernel launch (gather, dH, dX, dx
+    sum) equals the kernel chain bit for bit: every output and every
+    activation it leaves in the workspace."""
+    g = to_dev(make_layer_inputs(cfg, seed=22))
+    a, wsa = run_layer(cfg, g, which=3)
+    b, wsb = run_layer(cfg, g, which=BWD_MK, fill=float("nan"))
+    assert device_error(wsb) == (0, 0)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    for name in ("G", "dAB", "Hw", "dXp", "dw"):
+        assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
+
+
+def test_bwd_megakernel_does_not_depend_on_grid_size():
+    cfg = WIDE
+    g = to_dev(make_layer_inputs(cfg, seed=23))
+    ref = _digest(run_layer(cfg, g, which=3)[0])
+    try:
+        for n in (1, 7, 0):
+            moe.moe_set_grid_limit(n)
+            assert _digest(run_layer(cfg, g, which=BWD_MK)[0]) == ref, n
+    finally:
+        moe.moe_set_grid_limit(0)
+
+
+def test_bwd_megakernel_wait_timeout_is_reported_and_context_survives():
+    """A dH task that never completes (set on the host): the dX tasks of its
+    row block and the dx sums wait, run out of time, and the kernel returns
+    MOE_ERR_TIMEOUT; the next launches on the same context work."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=24))
+    first_dh_ticket = -(-cfg.R // 128)  # gather tasks come first, 128 rows each
+    out, ws = run_layer(cfg, g)
+    try:
+        moe.moe_debug_skip_megakernel_task(first_dh_ticket)
+        moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["topk_idx"],
+                          out["topk_w"], ws, out["dx"], out["dlogits"], out["dW1"], out["dW3"], out["dW2"],
+                          which=BWD_MK)
+        code, info = device_error(ws)
+    finally:
+        moe.moe_debug_skip_megakernel_task(-1)
+    assert code == moe.MOE_ERR_TIMEOUT, (code, info)
+    ref, _ = run_layer(cfg, g, which=3)
+    again, ws2 = run_layer(cfg, g, which=BWD_MK)
+    assert device_error(ws2) == (0, 0)
+    for k in ref:
+        assert torch.equal(ref[k], again[k]), k
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("cfg", [DSV2_LITE, MIXTRAL, SKEWED, LONG128K], ids=lambda c: c.name)
 def test_full_size_sampled_parity(cfg):
