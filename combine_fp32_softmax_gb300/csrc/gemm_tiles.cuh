@@ -288,7 +288,17 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     else
       moe::tma_load_2d(dst, map, b, c0, c1);
   };
-  constexpr int NB = Pipe<KIND, CG>::B_BOXES;
+  // MN-major operand: rows [row, row + 64) and columns [col, col + 64 n) in one
+  // instruction (a 3D box of n 64-column chunks, see map3d_mn); the single
+  // producer lane issues every load, so fewer instructions keep it ahead.
+  auto tma_load_mn = [&](void* dst, const CUtensorMap* map, uint64_t* b, int col, int row) {
+    if constexpr (PREFETCH)
+      tma_prefetch_3d(map, 0, row, col / 64);
+    else if (CG == 2 && to_even)
+      tma_load_3d_to_even(dst, map, b, 0, row, col / 64);
+    else
+      moe::tma_load_3d(dst, map, b, 0, row, col / 64);
+  };
   const int kk = kb * kBK;
   const int bn0 = t.n0 + 128 * rank;  // first B column this CTA stages
   if constexpr (KIND == kG1) {
@@ -301,29 +311,18 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.d + bn0);
   } else if constexpr (KIND == kDH) {
     tma_load_2d(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, kk, t.shared ? t.m0 : t.grow0);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, bn0 + 64 * i, t.seg * p.d + kk);
+    tma_load_mn(sB, &p.tmB0, bar, bn0, t.seg * p.d + kk);
   } else if constexpr (KIND == kDX) {
     tma_load_2d(sA, &p.tmA0, bar, kk, t.grow0);
     const bool second = kk >= p.f;
     const int krow = t.seg * p.f + (second ? kk - p.f : kk);
-#pragma unroll
-    for (int i = 0; i < NB; ++i)
-      tma_load_2d(sB + i * kBoxBytes, second ? &p.tmB1 : &p.tmB0, bar, bn0 + 64 * i, krow);
+    tma_load_mn(sB, second ? &p.tmB1 : &p.tmB0, bar, bn0, krow);
   } else if constexpr (KIND == kDW13) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) tma_load_2d(sA + i * kBoxBytes, &p.tmA0, bar, t.m0 + 64 * i, t.grow0 + kk);
-    const int brow = t.shared ? kk : t.grow0 + kk;
-#pragma unroll
-    for (int i = 0; i < NB; ++i)
-      tma_load_2d(sB + i * kBoxBytes, t.shared ? &p.tmB1 : &p.tmB0, bar, bn0 + 64 * i, brow);
+    tma_load_mn(sA, &p.tmA0, bar, t.m0, t.grow0 + kk);
+    tma_load_mn(sB, t.shared ? &p.tmB1 : &p.tmB0, bar, bn0, t.shared ? kk : t.grow0 + kk);
   } else {  // kDW2
-    const int arow = t.shared ? kk : t.grow0 + kk;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      tma_load_2d(sA + i * kBoxBytes, t.shared ? &p.tmA1 : &p.tmA0, bar, t.m0 + 64 * i, arow);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) tma_load_2d(sB + i * kBoxBytes, &p.tmB0, bar, bn0 + 64 * i, t.grow0 + kk);
+    tma_load_mn(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, t.m0, t.shared ? kk : t.grow0 + kk);
+    tma_load_mn(sB, &p.tmB0, bar, bn0, t.grow0 + kk);
   }
 }
 
@@ -946,6 +945,23 @@ bool map2d_any(CUtensorMap* m, const void* base, int esize, uint64_t inner, uint
 bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
   return map2d_any(m, base, 2, inner, outer, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
+// MN-major operand tiles: a row-major bf16 matrix [rows, cols] (cols a
+// multiple of 64) seen as 3D {64 columns of a chunk, row, chunk} (strides
+// cols*2 and 128 bytes).  A box {64, 64 rows, chunks} lands in shared memory
+// as `chunks` consecutive 64 x 64 blocks of 8 KB with 128-byte swizzled rows:
+// the layout the MN-major UMMA descriptor reads (8 KB between 64-element
+// groups), fetched by one instruction instead of one per block.
+bool map3d_mn(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base || cols == 0 || rows == 0 || cols % 64) return false;
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, 64, chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 // Epilogue chunks: 32 rows x 64 bytes (32 bf16 or 16 fp32), 64-byte swizzle.
 bool map_chunk_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
   return map2d_any(m, base, 2, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -995,7 +1011,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
   } else if constexpr (KIND == kDH) {
     ok &= map2d(&p.tmA0, a.G, d, R, 64, 128);
     ok &= map2d(&p.tmA1, a.dy, d, T, 64, 128);
-    ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 64);
+    ok &= map3d_mn(&p.tmB0, a.W2, f, nexp * d, 4 / CG);
     ok &= map_chunk_bf16(&p.tmO0, a.dAB_out, 2 * f, Rs);
     ok &= map_chunk_bf16(&p.tmO1, a.Hw_out, f, Rs);
     ok &= map_chunk_bf16(&p.tmX0, a.AB, 2 * f, Rs);
@@ -1007,16 +1023,16 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     p.out_partial = a.partial_out;
   } else if constexpr (KIND == kDX) {
     ok &= map2d(&p.tmA0, a.dAB, 2 * f, Rs, 64, 128);
-    ok &= map2d(&p.tmB0, a.W1, d, nexp * f, 64, 64);
-    ok &= map2d(&p.tmB1, a.W3, d, nexp * f, 64, 64);
+    ok &= map3d_mn(&p.tmB0, a.W1, d, nexp * f, 4 / CG);
+    ok &= map3d_mn(&p.tmB1, a.W3, d, nexp * f, 4 / CG);
     ok &= map_chunk_f32(&p.tmO0, a.dXp_out, d, Rs);
     p.N = a.d;
     p.K = 2 * a.f;
     p.out0 = a.dXp_out;
   } else if constexpr (KIND == kDW13) {
-    ok &= map2d(&p.tmA0, a.dAB, 2 * f, Rs, 64, 64);
-    ok &= map2d(&p.tmB0, a.Xp, d, R, 64, 64);
-    ok &= map2d(&p.tmB1, alt(a.x, a.Xp), d, a.x ? T : R, 64, 64);
+    ok &= map3d_mn(&p.tmA0, a.dAB, 2 * f, Rs, 2);
+    ok &= map3d_mn(&p.tmB0, a.Xp, d, R, 4 / CG);
+    ok &= map3d_mn(&p.tmB1, alt(a.x, a.Xp), d, a.x ? T : R, 4 / CG);
     ok &= map_chunk_f32(&p.tmO0, a.dW1_out, d, nexp * f);
     ok &= map_chunk_f32(&p.tmO1, a.dW3_out, d, nexp * f);
     p.Mw = 2 * a.f;
@@ -1024,9 +1040,9 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     p.out0 = a.dW1_out;
     p.out1 = a.dW3_out;
   } else {
-    ok &= map2d(&p.tmA0, a.G, d, R, 64, 64);
-    ok &= map2d(&p.tmA1, a.dy, d, T, 64, 64);
-    ok &= map2d(&p.tmB0, a.Hw, f, Rs, 64, 64);
+    ok &= map3d_mn(&p.tmA0, a.G, d, R, 2);
+    ok &= map3d_mn(&p.tmA1, a.dy, d, T, 2);
+    ok &= map3d_mn(&p.tmB0, a.Hw, f, Rs, 4 / CG);
     ok &= map_chunk_f32(&p.tmO0, a.dW2_out, f, nexp * d);
     p.Mw = a.d;
     p.N = a.f;

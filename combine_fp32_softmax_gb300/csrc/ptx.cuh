@@ -153,6 +153,32 @@ __device__ __forceinline__ void tma_load_2d_to_even(void* dst, const void* map, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// 3D tiled load (one box of {64, rows, chunks}: the MN-major operand tiles,
+// see map3d_mn) into this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// The same with completion counted on the pair's even CTA's barrier.
+__device__ __forceinline__ void tma_load_3d_to_even(void* dst, const void* map, uint64_t* bar, int c0, int c1,
+                                                    int c2) {
+  asm volatile(
+      "{\n\t.reg .b32 rb;\n\t"
+      "mapa.shared::cluster.u32 rb, %2, 0;\n\t"
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%3, %4, %5}], [rb];\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 // 2D tiled store of one box from shared memory (bulk-group completion).
 // Parts of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* map, const void* src_smem, int c0, int c1) {
