@@ -60,17 +60,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
   return ok != 0;
 }
 
-// Waits for the phase of `bar` with parity `parity` to complete.  Gives up
-// after kWaitLimitNs, or as soon as *abort is set by another role of the
-// CTA; on giving up it records MOE_ERR_TIMEOUT (info = `where`) in the
-// device error word, sets *abort and returns false.  CLUSTER selects the
-// cluster-scope acquire.
-template <bool CLUSTER = false>
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
-                                              int where) {
+// Bounded part of mbar_wait (out of line: it is the rare path).
+template <bool CLUSTER>
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                   int where) {
   const uint32_t a = smem_u32(bar);
   auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
-  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -83,6 +78,19 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, vo
       return false;
     }
   }
+}
+
+// Waits for the phase of `bar` with parity `parity` to complete.  Gives up
+// after kWaitLimitNs, or as soon as *abort is set by another role of the
+// CTA; on giving up it records MOE_ERR_TIMEOUT (info = `where`) in the
+// device error word, sets *abort and returns false.  CLUSTER selects the
+// cluster-scope acquire.  The first poll is inline: the producer and MMA
+// lanes wait once per K block and are on the critical path.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int where) {
+  const uint32_t a = smem_u32(bar);
+  if (CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  return mbar_wait_slow<CLUSTER>(bar, parity, abort, err, where);
 }
 
 // ------------------------------------------------------- thread-block clusters
