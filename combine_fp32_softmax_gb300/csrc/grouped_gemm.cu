@@ -95,9 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 }
 
 // Kinds that run on CTA pairs (bit = GemmKind): measured at the 8192-token
-// DeepSeek-V2-Lite-like shape, pairs win for GEMM 1, GEMM 2, dH and dX; the
-// ragged-K weight-gradient kinds are faster one CTA per tile.
-int g_pair_kinds = (1 << kG1) | (1 << kG2) | (1 << kDH) | (1 << kDX);
+// DeepSeek-V2-Lite-like shape, pairs win for all six (moe_autotune re-decides
+// per layer).
+int g_pair_kinds = (1 << 6) - 1;
 int g_prefetch_kb[6] = {0, 0, 0, 0, 0, 0};  // per kind: next-tile K blocks prefetched into L2
 
 // Launch configuration of one kind; CG = 2 adds the cluster dimension.

@@ -277,7 +277,7 @@ int moe_set_bwd_overlap(int on);
  * 256 x 256 tile with tcgen05 MMAs of the CTA group of two, each CTA holding
  * half of A and half of B); clear runs it one CTA per 128 x 256 tile.  Bits:
  * 0 GEMM 1 (gate/up), 1 GEMM 2 (down), 2 dH, 3 dX, 4 dW1/dW3, 5 dW2.  The
- * default is bits 0-3, what measures fastest on a DeepSeek-V2-Lite-like
+ * default is all six, what measures fastest on a DeepSeek-V2-Lite-like
  * layer (T=8192, d=2048, f=1408, E=64, k=6, S=2); moe_autotune picks per
  * layer.  Results are the same bits either way: every output element is the
  * same fp32 sum over K in the same order.  Returns the previous mask.
