@@ -348,27 +348,35 @@ __global__ void rebase_kernel(int32_t* __restrict__ base, const int32_t* __restr
   base[i] += rank_base[e] - offsets[e];
 }
 
-// dst[r] = src[idx[r]]: one warp per row, 16-byte vectors, 4 in flight per
-// lane.  An index outside [0, nsrc) writes a zero row.
+// dst[r] = src[idx[r]]: one warp per row, 16-byte vectors, kGatherVec in
+// flight per lane (a whole 4 KB row of d = 2048 bf16); the next row's index
+// is loaded before the current row is copied.  An index outside [0, nsrc)
+// writes a zero row.
+constexpr int kGatherVec = 8;
+
 __global__ void __launch_bounds__(256)
     gather_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ idx, int nsrc, int nrows,
                             int nvec, uint4* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows; r += nwarps) {
-    const int sr = idx[r];
+  int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int sr = r < nrows ? idx[r] : 0;
+  for (; r < nrows; r += nwarps) {
+    const int rn = r + nwarps;
+    const int sr_next = rn < nrows ? idx[rn] : 0;
     const bool ok = static_cast<unsigned>(sr) < static_cast<unsigned>(nsrc);
     const uint4* s = src + static_cast<size_t>(ok ? sr : 0) * nvec;
     uint4* o = dst + static_cast<size_t>(r) * nvec;
-    for (int v = lane; v < nvec; v += 32 * 4) {
-      uint4 t[4];
+    for (int v = lane; v < nvec; v += 32 * kGatherVec) {
+      uint4 t[kGatherVec];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kGatherVec; ++u)
         if (v + 32 * u < nvec) t[u] = ok ? __ldg(s + v + 32 * u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kGatherVec; ++u)
         if (v + 32 * u < nvec) o[v + 32 * u] = t[u];
     }
+    sr = sr_next;
   }
 }
 
@@ -559,7 +567,15 @@ cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int
                                     uint16_t* dst, int trace_kind, cudaStream_t s) {
   if (nrows <= 0) return cudaSuccess;
   TraceScope trace_scope(trace_kind, s);
-  const int blocks = min(ceil_div(nrows, 8), num_sms() * 8);
+  static int resident = 0;  // blocks resident at once
+  if (resident == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_rows_bf16_kernel, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    resident = per_sm * num_sms();
+  }
+  const int blocks = min(ceil_div(nrows, 8), resident);
   gather_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), idx, nsrc, nrows, d / 8,
                                                  reinterpret_cast<uint4*>(dst));
   return cudaGetLastError();
