@@ -199,7 +199,7 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_TRY_CUDA(launch_hist(topk_idx, c.T, c.E, c.k, at<int32_t>(ws, L.hist), L.nb_route, at<int>(ws, L.err), s));
   MOE_TRY(build_tables(c, L, ws, topk_idx, counts, offsets, dest, row_token, row_slot, s));
-  if (x && Xp) MOE_TRY_CUDA(launch_gather_rows_bf16(x, row_token, c.T, c.T * c.k, c.d_model, Xp, MOE_K_GATHER, s));
+  if (x && Xp) MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, s));
   return MOE_OK;
 }
 
@@ -257,7 +257,7 @@ int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x, co
     return megakernel_fwd(c, L, static_cast<uint8_t*>(ws), x, W1, W3, W2, topk_w, y, persistent_grid(), s);
   uint16_t* Xp = at<uint16_t>(ws, L.Xp);
   float* Op = at<float>(ws, L.Op);
-  MOE_TRY_CUDA(launch_gather_rows_bf16(x, row_token, c.T, R, c.d_model, Xp, MOE_K_GATHER, s));
+  MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, s));
   MOE_TRY(fwd_gemms(c, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, at<uint16_t>(ws, L.H),
                     at<uint16_t>(ws, L.AB), Op, s));
   MOE_TRY_CUDA(launch_sum_rows_f32(Op, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, s));
@@ -408,7 +408,7 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
       return MOE_OK;
     }
   } else if (which & 1) {  // B part: input gradients (critical path)
-    MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, R, c.d_model, G, MOE_K_COMBINE_BWD, s));
+    MOE_TRY_CUDA(launch_scatter_rows_bf16(dy, dest, c.T, c.k, c.d_model, G, MOE_K_COMBINE_BWD, s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
     if (side) {
       MOE_TRY_CUDA(cudaEventRecord(side->fork, s));

@@ -24,6 +24,10 @@ cudaError_t launch_rebase(int32_t* base, const int32_t* offsets, const int32_t* 
 // index is outside [0, nsrc)).
 cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
                                     uint16_t* dst, int trace_kind, cudaStream_t s);
+// dst[dest[t*k+j]] = src[t] for t < T, j < k (rows of `d` bf16): the rows a
+// gather by row_token writes, each source row read once.
+cudaError_t launch_scatter_rows_bf16(const uint16_t* src, const int32_t* dest, int T, int k, int d, uint16_t* dst,
+                                     int trace_kind, cudaStream_t s);
 // out[t] = sum_j rows[sel[t*k+j]] (slot order) + sum_s rows[R + s*T + t], fp32.
 cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
                                 int trace_kind, cudaStream_t s);

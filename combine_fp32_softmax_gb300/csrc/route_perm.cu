@@ -380,6 +380,40 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// dst[dest[t*k + j]] = src[t] for every token t and slot j < k: the same
+// rows a gather by row_token writes, but each source row is read once and
+// written k times, so a source larger than L2 is streamed from HBM once
+// instead of k times.  A warp's unit is one token's span of 32*kGatherVec
+// vectors (kGatherVec in flight per lane); the grid is the resident
+// capacity.  A destination outside [0, ndst) is skipped.
+__global__ void __launch_bounds__(256)
+    scatter_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ dest, int T, int k,
+                             int ndst, int nvec, uint4* __restrict__ dst) {
+  constexpr int kSpan = 32 * kGatherVec;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int spans = (nvec + kSpan - 1) / kSpan;
+  const int units = T * spans;  // < 2^31: checked by the launcher
+  for (int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += nwarps) {
+    const int t = u / spans;
+    const int v0 = (u - t * spans) * kSpan + lane;
+    const int mydest = lane < k ? dest[static_cast<size_t>(t) * k + lane] : -1;
+    const uint4* s = src + static_cast<size_t>(t) * nvec;
+    uint4 val[kGatherVec];
+#pragma unroll
+    for (int i = 0; i < kGatherVec; ++i)
+      if (v0 + 32 * i < nvec) val[i] = __ldg(s + v0 + 32 * i);
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(kFull, mydest, j);
+      if (static_cast<unsigned>(r) >= static_cast<unsigned>(ndst)) continue;
+      uint4* o = dst + static_cast<size_t>(r) * nvec;
+#pragma unroll
+      for (int i = 0; i < kGatherVec; ++i)
+        if (v0 + 32 * i < nvec) o[v0 + 32 * i] = val[i];
+    }
+  }
+}
+
 // out[t] = ((rows[sel[t*k]] + rows[sel[t*k+1]]) + ...) + rows[R + t] + ...
 // in exactly that order, fp32, one warp per token.  NR = k + S rows per
 // token is a template parameter so the loads of every row (two float4 per
@@ -578,6 +612,26 @@ cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int
   const int blocks = min(ceil_div(nrows, 8), resident);
   gather_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), idx, nsrc, nrows, d / 8,
                                                  reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_rows_bf16(const uint16_t* src, const int32_t* dest, int T, int k, int d, uint16_t* dst,
+                                     int trace_kind, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const long long units = static_cast<long long>(T) * ceil_div(d / 8, 32 * kGatherVec);
+  if (units >= (1ll << 31) || static_cast<long long>(T) * k >= (1ll << 31)) return cudaErrorInvalidValue;
+  TraceScope trace_scope(trace_kind, s);
+  static int resident = 0;  // blocks resident at once
+  if (resident == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scatter_rows_bf16_kernel, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    resident = per_sm * num_sms();
+  }
+  const int blocks = static_cast<int>(std::min<long long>(ceil_div(units, 8), resident));
+  scatter_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dest, T, k, T * k, d / 8,
+                                                  reinterpret_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 
