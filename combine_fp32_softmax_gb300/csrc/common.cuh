@@ -32,6 +32,10 @@ constexpr int kRouteTokensPerBlock = 32;
 // Grouped GEMM tile: 128 rows x 256 accumulator columns, K staged 64 at a
 // time (one 128-byte swizzle atom of bf16).
 constexpr int kBM = 128;
+// Smallest rows per MegaKernel gather task (the counter region is sized for
+// it): small tasks spread the gather (a bulk load per row from one lane)
+// over many CTAs when there are few rows.
+constexpr int kMegaGatherRows = 32;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 
@@ -55,10 +59,10 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.nb_route = ceil_div(c.T, kRouteTokensPerBlock);
   L.nt_dh = ceil_div(c.d_ff, kBN);
   // MegaKernel counters: cursor + 3 phase counters, one readiness counter
-  // per 128-row block of Xp, one per GEMM-1 m-tile (bounded by the m-tiles
-  // of every segment), padding.
+  // per gathered row block (kMegaGatherRows rows), one per first-GEMM m-tile
+  // (bounded by the m-tiles of every segment), padding.
   const size_t mtiles_max = R / kBM + E + S * static_cast<size_t>(ceil_div(c.T, kBM)) + 2;
-  L.mk_ints = static_cast<int>(16 + ceil_div(static_cast<long long>(R), kBM) + mtiles_max + 16);
+  L.mk_ints = static_cast<int>(16 + ceil_div(static_cast<long long>(R), kMegaGatherRows) + mtiles_max + 16);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;

@@ -19,7 +19,7 @@
 //   ctr[1]                   B warp-tiles finished (the token sums wait on all)
 //   ctr[2]                   sum cursor: after the last ticket every warp of
 //                            every CTA claims tokens one at a time from it
-//   ctr[kCtrXp + g]          gathered row block g (128 rows) written
+//   ctr[kCtrXp + g]          gathered row block g (mp.grows rows) written
 //   ctr[kCtrXp + NG + mt]    A warp-tiles finished of m-tile mt
 //                            (B tiles of mt wait for all of them)
 // The UniEP page (section 2.2) has its MegaKernels serve the backward steps
@@ -39,7 +39,7 @@ namespace moe {
 namespace {
 
 constexpr int kTq = 4;              // depth of the producer -> consumer task FIFO
-constexpr int kGatherRows = 128;    // gathered rows per gather task
+
 constexpr int kCtrXp = 8;
 constexpr int kMaxTokRows = 12;     // k <= 8 routed + S <= 4 shared rows per token
 constexpr int kMaxMegaStages = 4;
@@ -54,6 +54,7 @@ struct MegaParams {
   float* y;                    // token sums (y forward, dx backward)
   int* ctr;
   int NG;
+  int grows;  // gathered rows per gather task (kMegaGatherRows or 128)
   int skip;  // testing aid: ticket treated as never done (-1: none)
   // optional per-task timeline: records_per_cta records of 3 x u64
   // (ticket | role << 32 | cta << 40, start ns, end ns) per CTA, the first
@@ -130,9 +131,10 @@ __device__ __forceinline__ void warp_signal(int* counter) {
   if ((threadIdx.x & 31) == 0) red_release_gpu_add(counter, 1);
 }
 
-// Gather task g (producer lane): gathered rows [128g, 128g+128) <-
-// source[row_token], row by row with bulk copies through the stage buffers
-// (up to NST-1 chunks in flight), then publish the block.
+// Gather task g (producer lane): gathered rows [grows*g, grows*(g+1)) <-
+// source[row_token], a bulk load per row into the stage buffers (up to
+// NST-1 chunks in flight) and one bulk store per chunk (its destination rows
+// are consecutive), then publish the block.
 struct GatherState {
   uint32_t par = 0;      // next wait parity of gbar[b] (bit b)
   uint32_t pending = 0;  // buffers with loads issued but not yet waited on
@@ -143,9 +145,9 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
                             volatile int* abort, int where) {
   const int d = mp.g1.d;
   const uint32_t rb = 2u * d;
-  const int rps = min(kGatherRows, kStageBytes / static_cast<int>(rb));
-  const int r0 = g * kGatherRows;
-  const int nrows = min(kGatherRows, mp.g1.R - r0);
+  const int rps = min(mp.grows, kStageBytes / static_cast<int>(rb));
+  const int r0 = g * mp.grows;
+  const int nrows = min(mp.grows, mp.g1.R - r0);
   const int nchunk = (nrows + rps - 1) / rps;
   for (int c = 0; c <= nchunk; ++c) {
     if (c < nchunk) {
@@ -167,7 +169,8 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
       gs.pending &= ~(1u << b);
       const int n = min(rps, nrows - pc * rps);
       uint8_t* buf = smem + b * kStageBytes;
-      for (int i = 0; i < n; ++i) bulk_store(mp.Xp + static_cast<size_t>(r0 + pc * rps + i) * d, buf + i * rb, rb);
+      // the chunk's destination rows are consecutive: one bulk store
+      bulk_store(mp.Xp + static_cast<size_t>(r0 + pc * rps) * d, buf, n * rb);
       bulk_commit();
     }
   }
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
         } else if (id < e1) {
           const TileInfo t = decode_tile<KA>(mp.g1, ss, id - NG);
           if (!t.shared) {  // routed rows come from the gathered rows: wait for their blocks
-            const int g0 = t.grow0 / kGatherRows, g1 = (t.grow0 + t.rows - 1) / kGatherRows;
+            const int g0 = t.grow0 / mp.grows, g1 = (t.grow0 + t.rows - 1) / mp.grows;
             bool ok = true;
             for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], 1, abort, err, where);
             if (!ok) break;
@@ -437,7 +440,10 @@ int mega_launch(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs
   mp.Op = ssrc;
   mp.y = sdst;
   mp.ctr = reinterpret_cast<int*>(ws + L.mk);
-  mp.NG = ceil_div(R, kGatherRows);
+  // 128-row gather tasks when every SM gets a few; 32-row ones for small
+  // layers, whose gather would otherwise sit on a handful of CTAs.
+  mp.grows = R >= 256ll * num_sms() ? 128 : kMegaGatherRows;
+  mp.NG = ceil_div(R, mp.grows);
   mp.skip = g_skip_ticket;
   mp.trace = g_trace_buf;
   mp.trace_per_cta = g_trace_per_cta;

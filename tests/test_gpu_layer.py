@@ -217,7 +217,7 @@ def test_megakernel_wait_timeout_is_reported_and_context_survives():
     device error word, and the next launches on the same context work."""
     cfg = MID
     g = to_dev(make_layer_inputs(cfg, seed=17))
-    first_gemm1_ticket = -(-cfg.R // 128)  # gather tasks come first, 128 rows each
+    first_gemm1_ticket = -(-cfg.R // 32)  # gather tasks come first, 32 rows each
     ws = moe.alloc_workspace(cfg, DEV)
     out = {k: v for k, v in run_layer(cfg, g, ws=ws, use_megakernel=0)[0].items()}
     try:
@@ -271,7 +271,7 @@ def test_bwd_megakernel_wait_timeout_is_reported_and_context_survives():
     MOE_ERR_TIMEOUT; the next launches on the same context work."""
     cfg = MID
     g = to_dev(make_layer_inputs(cfg, seed=24))
-    first_dh_ticket = -(-cfg.R // 128)  # gather tasks come first, 128 rows each
+    first_dh_ticket = -(-cfg.R // 32)  # gather tasks come first, 32 rows each
     out, ws = run_layer(cfg, g)
     try:
         moe.moe_debug_skip_megakernel_task(first_dh_ticket)
