@@ -14,13 +14,17 @@
 // worker model of section 2.2 and the streaming-GEMM argument of the
 // AutoOverlap page, section 2.1 (no per-expert launches, no partial waves).
 //
-// Design (one CTA per SM, 192 threads):
+// Design (one CTA per SM, 192 threads; CG = 1 or 2 CTAs per tile):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
-//               (256 x 64) into a 3- or 4-stage shared-memory ring
-//               (48 KB/stage).
-//   warp 1      allocates 512 TMEM columns, issues tcgen05.mma
-//               (M=128, N=256, K=16, bf16 -> fp32) from one lane, commits
-//               to mbarriers; a ragged-K tail is zeroed in shared memory.
+//               (256 x 64, or this CTA's 128 x 64 half on a CTA pair) into
+//               a shared-memory ring: 3-4 stages of 48 KB (one CTA per
+//               tile), 4-6 of 32 KB (pairs).  MN-major operands come as one
+//               3D box per operand (map3d_mn).
+//   warp 1      allocates 512 TMEM columns, issues tcgen05.mma from one lane
+//               (M=128, or M=256 on a pair from the even CTA; N=256, K=16,
+//               bf16 -> fp32), commits to mbarriers (multicast to both
+//               CTAs of a pair); a ragged-K tail's last partial 16-row step
+//               is zeroed in shared memory.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
 //               thread = one output row), fused elementwise work, results
 //               staged through swizzled shared memory and written with TMA
