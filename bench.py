@@ -51,6 +51,8 @@ def parse_args():
                     help="bit mask of grouped-GEMM kinds run on CTA pairs (-1: the library default)")
     ap.add_argument("--no-bwd-overlap", action="store_true",
                     help="run the backward's weight-gradient GEMMs on the caller's stream (no B/W overlap)")
+    ap.add_argument("--no-route-fusion", action="store_true",
+                    help="run the router, scan and scatter as three kernels instead of one cooperative launch")
     ap.add_argument("--no-autotune", action="store_true",
                     help="skip the library's measured GEMM autotuner (run during set-up, untimed)")
     return ap.parse_args()
@@ -246,6 +248,8 @@ def run_ours(args):
         moe.moe_set_gemm_pair_kinds(args.gemm_pair_kinds)
     if args.no_bwd_overlap:
         moe.moe_set_bwd_overlap(False)
+    if args.no_route_fusion:
+        moe.moe_set_route_fusion(False)
     f32 = torch.float32
     nexp = cfg.E + cfg.S
     out = dict(y=torch.empty(cfg.T, cfg.d, dtype=f32, device=dev),
@@ -462,7 +466,8 @@ def run_ours(args):
             "roofline": roof, "clocks": clocks,
             "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "bwd_ms": bwd_times,
             "bwd_megakernel": bmk, "kernels": kernels,
-            "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap},
+            "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap,
+                       "route_fusion": not args.no_route_fusion},
             "kernel_timing": "per-launch CUDA events on the launching stream over --steps further steps run with "
                              "the backward's B/W overlap off (the timed steps run with it on)"}
     if world == 1 and not args.no_cpu_baseline:

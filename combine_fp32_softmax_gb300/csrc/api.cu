@@ -23,6 +23,7 @@ using namespace moe;
 namespace {
 
 int g_grid_limit = 0;
+int g_route_fusion = 1;
 int g_bwd_overlap = 1;
 
 // Per device: a second stream and two events for the backward's fork/join
@@ -117,6 +118,30 @@ int build_tables(const moe_cfg& c, const WsLayout& L, void* ws, const int32_t* t
   return MOE_OK;
 }
 
+// Router and permutation tables of the layer forward: one cooperative
+// launch, else (fusion off or refused) the router and build_tables.
+int route_tables(const moe_cfg& c, const WsLayout& L, void* ws, const float* logits, int32_t* topk_idx,
+                 float* topk_w, cudaStream_t s) {
+  int32_t* hist = at<int32_t>(ws, L.hist);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* dest = at<int32_t>(ws, L.dest);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  int32_t* row_slot = at<int32_t>(ws, L.row_slot);
+  int* err = at<int>(ws, L.err);
+  if (g_route_fusion) {
+    const cudaError_t e =
+        launch_route_tables(logits, c.T, c.E, c.k, c.renorm, L.nb_route, topk_idx, topk_w, hist,
+                            at<int32_t>(ws, L.base), counts, offsets, dest, row_token, row_slot, err,
+                            g_grid_limit, s);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorCooperativeLaunchTooLarge && e != cudaErrorNotSupported) return MOE_ERR_CUDA;
+    (void)cudaGetLastError();  // not a sticky error: take the three-kernel path
+  }
+  MOE_TRY_CUDA(launch_route(logits, c.T, c.E, c.k, c.renorm, topk_idx, topk_w, hist, L.nb_route, err, s));
+  return build_tables(c, L, ws, topk_idx, counts, offsets, dest, row_token, row_slot, s);
+}
+
 int fwd_gemms(const moe_cfg& c, const WsLayout& L, void* ws, const uint16_t* Xp, const uint16_t* x,
               const int32_t* offsets, const int32_t* row_slot, const float* topk_w, const uint16_t* W1,
               const uint16_t* W3, const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Op, cudaStream_t s) {
@@ -163,6 +188,12 @@ int moe_set_grid_limit(int n) {
 }
 
 int moe_set_gemm_pair_kinds(int mask) { return set_gemm_pair_kinds(mask); }
+
+int moe_set_route_fusion(int on) {
+  const int prev = g_route_fusion;
+  g_route_fusion = on != 0;
+  return prev;
+}
 
 int moe_set_bwd_overlap(int on) {
   const int prev = g_bwd_overlap;
@@ -250,9 +281,7 @@ int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x, co
   int32_t* row_token = at<int32_t>(ws, L.row_token);
   int32_t* row_slot = at<int32_t>(ws, L.row_slot);
   int32_t* dest = at<int32_t>(ws, L.dest);
-  MOE_TRY_CUDA(launch_route(logits, c.T, c.E, c.k, c.renorm, topk_idx, topk_w, at<int32_t>(ws, L.hist), L.nb_route,
-                            at<int>(ws, L.err), s));
-  MOE_TRY(build_tables(c, L, ws, topk_idx, at<int32_t>(ws, L.counts), offsets, dest, row_token, row_slot, s));
+  MOE_TRY(route_tables(c, L, ws, logits, topk_idx, topk_w, s));
   if (use_megakernel)
     return megakernel_fwd(c, L, static_cast<uint8_t*>(ws), x, W1, W3, W2, topk_w, y, persistent_grid(), s);
   uint16_t* Xp = at<uint16_t>(ws, L.Xp);

@@ -24,6 +24,12 @@ __device__ __forceinline__ void record_error(int* err, int code, int info) {
 }
 #endif
 
+// Words of the 64-byte error region (int index) that hold the grid barrier
+// of the fused routing + permutation kernel: the arrival count (back to 0
+// after every completed barrier) and the generation.  moe_ws_init zeroes
+// them with the error word.
+constexpr int kErrBarrierWord = 8;
+
 // Router / permutation: tokens per block (8 warps x 4 tokens).  Small blocks
 // give the latency-bound router enough warps; the per-block histogram the
 // scan walks has E * ceil(T / 32) entries.

@@ -11,6 +11,13 @@ namespace moe {
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* topk_idx,
                          float* topk_w, int32_t* hist, int nb, int* err, cudaStream_t s);
+// Router + histogram + scan + stable scatter in one cooperative launch of
+// at most max_grid blocks (0: as many as fit).  Returns the launch's error
+// without recording it if the device cannot run the grid cooperatively.
+cudaError_t launch_route_tables(const float* logits, int T, int E, int k, int renorm, int nb, int32_t* topk_idx,
+                                float* topk_w, int32_t* hist, int32_t* base, int32_t* counts, int32_t* offsets,
+                                int32_t* dest, int32_t* row_token, int32_t* row_slot, int* err, int max_grid,
+                                cudaStream_t s);
 cudaError_t launch_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* hist, int nb, int* err,
                         cudaStream_t s);
 cudaError_t launch_scan(const int32_t* hist, int E, int nb, int R, int32_t* base, int32_t* counts,

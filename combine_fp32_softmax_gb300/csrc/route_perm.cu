@@ -51,22 +51,36 @@ __device__ __forceinline__ void row_load(const float* __restrict__ row, int E, i
   }
 }
 
+// Order-preserving key of a finite float: a larger value has a larger
+// unsigned key, -0.0 and +0.0 share one, and every finite value's key is
+// above 0 (the key of "no entry").  Warp max/min over keys are single
+// redux.sync instructions, where a float max needs a shuffle butterfly.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // Softmax statistics of the row already in r.v; false if it holds a
-// non-finite logit.
+// non-finite logit (the statistics are then unspecified).  key[i] is the
+// order key of entry i (0 beyond E).
 template <int EPL>
-__device__ __forceinline__ bool row_stats(int E, int lane, RowSoftmax<EPL>& r) {
+__device__ __forceinline__ bool row_stats(int E, int lane, RowSoftmax<EPL>& r, unsigned (&key)[EPL]) {
   bool bad = false;
+  unsigned kmax = 0;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E && !isfinite(r.v[i])) bad = true;
+    key[i] = e < E ? order_key(r.v[i]) : 0u;
+    kmax = max(kmax, key[i]);
   }
   bad = __any_sync(kFull, bad);
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) m = fmaxf(m, r.v[i]);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  // The maximum is exact whichever way it is found; -0.0 and +0.0 give the
+  // same exp(v - m) bits.
+  const float m = key_value(__reduce_max_sync(kFull, kmax));
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -86,7 +100,79 @@ __device__ __forceinline__ bool row_stats(int E, int lane, RowSoftmax<EPL>& r) {
 template <int EPL>
 __device__ __forceinline__ bool row_softmax(const float* __restrict__ row, int E, int lane, RowSoftmax<EPL>& r) {
   row_load<EPL>(row, E, lane, r.v);
-  return row_stats<EPL>(E, lane, r);
+  unsigned key[EPL];
+  return row_stats<EPL>(E, lane, r, key);
+}
+
+// Routes token t on one warp (its logit row already in r.v): softmax
+// statistics, then k rounds of warp argmax.  Lane j < k ends with slot j's
+// expert and weight.  A row with a non-finite logit is reported and gets the
+// placeholder routing slot j -> expert j with weight 0.
+template <int EPL>
+__device__ __forceinline__ void route_token(RowSoftmax<EPL>& r, int t, int E, int k, int renorm, int lane, int* err,
+                                            int& my_idx, float& my_w) {
+  my_idx = lane;
+  my_w = 0.f;
+  unsigned key[EPL];
+  if (!row_stats<EPL>(E, lane, r, key)) {
+    if (lane == 0) record_error(err, MOE_ERR_NONFINITE_CODE, t);
+    return;
+  }
+  float psum = 0.f, my_p = 0.f;
+  for (int j = 0; j < k; ++j) {
+    // Best remaining entry of this lane: strictly greater keeps the lower
+    // index on ties (entries are visited in increasing expert index).
+    unsigned bk = 0;
+    unsigned be = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (key[i] > bk) {
+        bk = key[i];
+        be = static_cast<unsigned>(lane + 32 * i);
+      }
+    // Winner under (value desc, index asc), a strict total order: the
+    // largest key, then the lowest expert index holding it.  Every lane
+    // gets the same winner.
+    const unsigned kbest = __reduce_max_sync(kFull, bk);
+    const int bi = static_cast<int>(__reduce_min_sync(kFull, bk == kbest ? be : 0xffffffffu));
+    const int owner = bi & 31, which = bi >> 5;
+    float p_local = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane == owner && i == which) {
+        key[i] = 0u;  // taken
+        p_local = r.ex[i] / r.s;
+      }
+    const float p = __shfl_sync(kFull, p_local, owner);
+    if (lane == j) {
+      my_idx = bi;
+      my_p = p;
+    }
+    psum += p;
+  }
+  my_w = renorm ? my_p / psum : my_p;
+}
+
+// Routes the 32 tokens of histogram block hb (warp w: token 32*hb + w) and
+// counts their slots per expert in s_hist (zeroed by the caller).
+template <int EPL>
+__device__ __forceinline__ void route_block(const float* __restrict__ logits, int hb, int T, int E, int k, int renorm,
+                                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* s_hist,
+                                            int* err) {
+  static_assert(kRouteWarps == kRouteTokensPerBlock, "one warp per token");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = hb * kRouteTokensPerBlock + warp;
+  if (t >= T) return;
+  RowSoftmax<EPL> r;
+  row_load<EPL>(logits + static_cast<size_t>(t) * E, E, lane, r.v);
+  int my_idx;
+  float my_w;
+  route_token<EPL>(r, t, E, k, renorm, lane, err, my_idx, my_w);
+  if (lane < k) {
+    topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+    topk_w[static_cast<size_t>(t) * k + lane] = my_w;
+    atomicAdd(&s_hist[my_idx], 1);  // integer count: order-independent
+  }
 }
 
 template <int EPL>
@@ -94,80 +180,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     route_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm, int32_t* __restrict__ topk_idx,
                  float* __restrict__ topk_w, int32_t* __restrict__ hist, int nb, int* err) {
   __shared__ int s_hist[256];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
-  const int tok0 = blockIdx.x * kRouteTokensPerBlock;
-  // Every row of this warp's tokens is loaded before the first is routed
-  // (one memory latency, not one per token, should a warp hold several).
-  constexpr int kTPW = kRouteTokensPerBlock / kRouteWarps;
-  float rows[kTPW][EPL];
-#pragma unroll
-  for (int q = 0; q < kTPW; ++q) {
-    const int t = tok0 + warp + q * kRouteWarps;
-    if (t < T) row_load<EPL>(logits + static_cast<size_t>(t) * E, E, lane, rows[q]);
-  }
-#pragma unroll
-  for (int q = 0; q < kTPW; ++q) {
-    const int t = tok0 + warp + q * kRouteWarps;
-    if (t >= T) break;
-    RowSoftmax<EPL> r;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) r.v[i] = rows[q][i];
-    int my_idx = lane;  // placeholder routing for a rejected row: slot j -> expert j
-    float my_w = 0.f;
-    if (!row_stats<EPL>(E, lane, r)) {
-      if (lane == 0) record_error(err, MOE_ERR_NONFINITE_CODE, t);
-    } else {
-      uint32_t taken = 0;
-      float psum = 0.f, my_p = 0.f;
-      for (int j = 0; j < k; ++j) {
-        // Best untaken entry of this lane: strictly greater keeps the lower
-        // index on ties (entries are visited in increasing expert index).
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !(taken & (1u << i)) && (bi == 0x7fffffff || r.v[i] > bv)) {
-            bv = r.v[i];
-            bi = e;
-          }
-        }
-        // Warp argmax under (value desc, index asc): a strict total order,
-        // so every lane agrees on the winner.  -0.0 == +0.0 compares equal.
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-          const float ov = __shfl_xor_sync(kFull, bv, off);
-          const int oi = __shfl_xor_sync(kFull, bi, off);
-          if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        const int owner = bi & 31, which = bi >> 5;
-        float p_local = 0.f;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-          if (lane == owner && i == which) {
-            taken |= 1u << i;
-            p_local = r.ex[i] / r.s;
-          }
-        const float p = __shfl_sync(kFull, p_local, owner);
-        if (lane == j) {
-          my_idx = bi;
-          my_p = p;
-        }
-        psum += p;
-      }
-      my_w = renorm ? my_p / psum : my_p;
-    }
-    if (lane < k) {
-      topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
-      topk_w[static_cast<size_t>(t) * k + lane] = my_w;
-      atomicAdd(&s_hist[my_idx], 1);  // integer count: order-independent
-    }
-  }
+  route_block<EPL>(logits, blockIdx.x, T, E, k, renorm, topk_idx, topk_w, s_hist, err);
   __syncthreads();
   if (hist)
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(e) * nb + blockIdx.x] = s_hist[e];
@@ -196,26 +211,25 @@ __global__ void __launch_bounds__(256)
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(e) * nb + blockIdx.x] = s_hist[e];
 }
 
-// One flat exclusive scan of the expert-major [E][nb] histogram: at (e, b)
-// it equals offsets[e] + (slots of expert e in blocks < b), i.e. the base
-// address of block b's first slot for expert e.
-// The flat array hist[E][nb] is scanned by one 1024-thread block in tiles
-// of kScanTile entries: each tile is loaded coalesced into shared memory
-// (entry i at i + i/32, so a warp reading 8 consecutive entries per thread
-// hits every bank once), each thread sums its 8 entries, a two-level warp
-// shuffle scan gives every thread its exclusive prefix, and the prefixes go
-// back out coalesced; a carry runs across tiles.
+// Exclusive scan of in[0, n) into out by one kScanThreads-thread block;
+// returns the total to every thread.  The array is scanned in tiles of
+// kScanTile entries: each tile is loaded coalesced into shared memory (entry
+// i at i + i/32, so a warp reading 8 consecutive entries per thread hits
+// every bank once), each thread sums its 8 entries, a two-level warp shuffle
+// scan gives every thread its exclusive prefix, and the prefixes go back out
+// coalesced; a carry runs across tiles.  in is read through L2 only (it may
+// have been written by other blocks of the same launch).
 constexpr int kScanThreads = 1024;
 constexpr int kScanPer = 8;
 constexpr int kScanTile = kScanThreads * kScanPer;
 
-__global__ void __launch_bounds__(kScanThreads)
-    scan_kernel(const int32_t* __restrict__ hist, int E, int nb, int R, int32_t* __restrict__ base,
-                int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int tile[kScanTile + kScanTile / 32];
-  __shared__ int warp_tot[32];
-  __shared__ int tile_total;
-  const int n = E * nb;
+struct ScanSmem {
+  int tile[kScanTile + kScanTile / 32];
+  int warp_tot[32];
+  int tile_total;
+};
+
+__device__ __forceinline__ int block_exclusive_scan(const int32_t* in, int n, int32_t* out, ScanSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   int carry = 0;
   for (int t0 = 0; t0 < n; t0 += kScanTile) {
@@ -223,7 +237,7 @@ __global__ void __launch_bounds__(kScanThreads)
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const int i = tid + j * kScanThreads;
-      tile[i + (i >> 5)] = i < m ? hist[t0 + i] : 0;
+      sm.tile[i + (i >> 5)] = i < m ? __ldcg(in + t0 + i) : 0;
     }
     __syncthreads();
     int v[kScanPer];
@@ -231,7 +245,7 @@ __global__ void __launch_bounds__(kScanThreads)
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const int i = tid * kScanPer + j;
-      v[j] = tile[i + (i >> 5)];
+      v[j] = sm.tile[i + (i >> 5)];
       local += v[j];
     }
     int incl = local;
@@ -240,77 +254,91 @@ __global__ void __launch_bounds__(kScanThreads)
       const int y = __shfl_up_sync(kFull, incl, off);
       if (lane >= off) incl += y;
     }
-    if (lane == 31) warp_tot[w] = incl;
+    if (lane == 31) sm.warp_tot[w] = incl;
     __syncthreads();
     if (w == 0) {
-      const int x = warp_tot[lane];
+      const int x = sm.warp_tot[lane];
       int inc = x;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(kFull, inc, off);
         if (lane >= off) inc += y;
       }
-      warp_tot[lane] = inc - x;
-      if (lane == 31) tile_total = inc;
+      sm.warp_tot[lane] = inc - x;
+      if (lane == 31) sm.tile_total = inc;
     }
     __syncthreads();
-    int run = carry + warp_tot[w] + incl - local;
+    int run = carry + sm.warp_tot[w] + incl - local;
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const int i = tid * kScanPer + j;
-      tile[i + (i >> 5)] = run;
+      sm.tile[i + (i >> 5)] = run;
       run += v[j];
     }
-    carry += tile_total;
+    carry += sm.tile_total;
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const int i = tid + j * kScanThreads;
-      if (i < m) base[t0 + i] = tile[i + (i >> 5)];
+      if (i < m) out[t0 + i] = sm.tile[i + (i >> 5)];
     }
-    __syncthreads();  // tile[], warp_tot and tile_total are rewritten by the next tile
+    __syncthreads();  // tile, warp_tot and tile_total are rewritten by the next tile
   }
-  for (int e = tid; e < E; e += blockDim.x) {
+  return carry;
+}
+
+// One flat exclusive scan of the expert-major [E][nb] histogram: at (e, b)
+// it equals offsets[e] + (slots of expert e in blocks < b), i.e. the base
+// address of block b's first slot for expert e.
+__global__ void __launch_bounds__(kScanThreads)
+    scan_kernel(const int32_t* __restrict__ hist, int E, int nb, int R, int32_t* __restrict__ base,
+                int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ ScanSmem sm;
+  block_exclusive_scan(hist, E * nb, base, sm);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int b0 = base[static_cast<size_t>(e) * nb];
     const int b1 = (e + 1 < E) ? base[static_cast<size_t>(e + 1) * nb] : R;
     offsets[e] = b0;
     counts[e] = b1 - b0;
   }
-  if (tid == 0) offsets[E] = R;
+  if (threadIdx.x == 0) offsets[E] = R;
 }
 
-// Stable in-block ranks.  Warp w owns tokens [TPW*w, TPW*w+TPW) of the block,
-// i.e. a contiguous run of TPW*k flat slots, visited in rounds of 32.  Pass 1
-// counts per (warp, expert); a prefix over warps (starting at the block's
-// global base) gives each warp's first address per expert; pass 2 ranks each
-// slot among equal-expert lanes of its round (match mask) and advances.
-constexpr int kScatterTPW = kRouteTokensPerBlock / 8;  // tokens per warp
-
-__global__ void __launch_bounds__(256)
-    scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, int T, int E, int k,
-                   int nb, int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
-                   int32_t* __restrict__ row_slot) {
-  __shared__ int wrun[8][256];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, b = blockIdx.x;
-  for (int i = tid; i < 8 * 256; i += 256) (&wrun[0][0])[i] = 0;
+// Stable in-block ranks of histogram block hb on NW warps.  Warp w owns
+// tokens [TPW*w, TPW*w+TPW) of the block, i.e. a contiguous run of TPW*k flat
+// slots, visited in rounds of 32.  Pass 1 counts per (warp, expert); a prefix
+// over warps (starting at the block's global base for the expert, plus
+// off[e] where the base holds only the within-expert prefix) gives each
+// warp's first address per expert; pass 2 ranks each slot among
+// equal-expert lanes of its round (match mask) and advances.  The result
+// does not depend on NW: a slot's address is its expert's base plus the
+// number of earlier slots of the block with the same expert.
+template <int NW>
+__device__ __forceinline__ void scatter_block(const int32_t* __restrict__ topk_idx, const int32_t* base,
+                                              const int* off, int hb, int T, int E, int k, int nb,
+                                              int (*wrun)[256], int32_t* __restrict__ dest,
+                                              int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot) {
+  constexpr int TPW = kRouteTokensPerBlock / NW;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < NW * 256; i += NW * 32) (&wrun[0][0])[i] = 0;
   __syncthreads();
-  const size_t slot0 = static_cast<size_t>(b) * kRouteTokensPerBlock * k;
-  const int nslot = (min(T, (b + 1) * kRouteTokensPerBlock) - b * kRouteTokensPerBlock) * k;
-  const int wslots = kScatterTPW * k;
+  const size_t slot0 = static_cast<size_t>(hb) * kRouteTokensPerBlock * k;
+  const int nslot = (min(T, (hb + 1) * kRouteTokensPerBlock) - hb * kRouteTokensPerBlock) * k;
+  const int wslots = TPW * k;
   const int wslot0 = w * wslots;
   const int rounds = (wslots + 31) / 32;
   for (int rnd = 0; rnd < rounds; ++rnd) {
     const int il = wslot0 + rnd * 32 + lane;
     const bool valid = rnd * 32 + lane < wslots && il < nslot;
-    const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
+    const int e = valid ? min(max(__ldcg(topk_idx + slot0 + il), 0), E - 1) : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     if (valid && lane == __ffs(peers) - 1) wrun[w][e] += __popc(peers);
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = base[static_cast<size_t>(e) * nb + b];
+  for (int e = tid; e < E; e += NW * 32) {
+    int run = __ldcg(base + static_cast<size_t>(e) * nb + hb) + (off ? off[e] : 0);
 #pragma unroll
-    for (int ww = 0; ww < 8; ++ww) {
+    for (int ww = 0; ww < NW; ++ww) {
       const int c = wrun[ww][e];
       wrun[ww][e] = run;
       run += c;
@@ -321,7 +349,7 @@ __global__ void __launch_bounds__(256)
   for (int rnd = 0; rnd < rounds; ++rnd) {
     const int il = wslot0 + rnd * 32 + lane;
     const bool valid = rnd * 32 + lane < wslots && il < nslot;
-    const int e = valid ? min(max(topk_idx[slot0 + il], 0), E - 1) : -1;
+    const int e = valid ? min(max(__ldcg(topk_idx + slot0 + il), 0), E - 1) : -1;
     const unsigned peers = __match_any_sync(kFull, e);
     const int r = valid ? wrun[w][e] + __popc(peers & lt) : 0;
     __syncwarp();
@@ -335,6 +363,162 @@ __global__ void __launch_bounds__(256)
         row_slot[r] = static_cast<int>(i);
       }
     }
+  }
+}
+
+constexpr int kScatterWarps = 8;
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, int T, int E, int k,
+                   int nb, int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
+                   int32_t* __restrict__ row_slot) {
+  __shared__ int wrun[kScatterWarps][256];
+  scatter_block<kScatterWarps>(topk_idx, base, nullptr, blockIdx.x, T, E, k, nb, wrun, dest, row_token, row_slot);
+}
+
+// Grid barrier of a cooperative launch (every block resident at once).
+// Thread 0 of each block reads the generation, publishes the block's writes
+// and arrives; the last arrival resets the count and advances the
+// generation; the others spin on the generation for at most kWaitLimitNs.
+// On a timeout (recorded in err) it returns false in every thread of the
+// block; the count is then left inconsistent until moe_ws_init.
+__device__ bool grid_barrier(int* bar, int* err, int where) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const int gen = ld_acquire_gpu(bar + 1);
+    __threadfence();
+    if (atomicAdd(bar, 1) == static_cast<int>(gridDim.x) - 1) {
+      __threadfence();
+      atomicExch(bar, 0);
+      red_release_gpu_add(bar + 1, 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(bar + 1) == gen) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          record_error(err, MOE_ERR_TIMEOUT_CODE, where);
+          ok = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// After a timed-out grid barrier: placeholder tables that keep the later
+// kernels of the call in bounds (every slot to its own row, all rows in the
+// last expert); the error word already marks the results void.  Blocks that
+// passed the barrier write the real tables, which are in range as well.
+__device__ void placeholder_tables(int T, int E, int k, int nb, int32_t* counts, int32_t* offsets, int32_t* dest,
+                                   int32_t* row_token, int32_t* row_slot) {
+  const int R = T * k;
+  for (int hb = blockIdx.x; hb < nb; hb += gridDim.x) {
+    const int i0 = hb * kRouteTokensPerBlock * k, i1 = min(R, i0 + kRouteTokensPerBlock * k);
+    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += blockDim.x) {
+      dest[i] = i;
+      row_token[i] = i / k;
+      row_slot[i] = i;
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      offsets[e] = 0;
+      counts[e] = e == E - 1 ? R : 0;
+    }
+    if (threadIdx.x == 0) offsets[E] = R;
+  }
+}
+
+// Scratch of the fused kernel, one phase at a time.
+union RouteTablesSmem {
+  int hist[256];
+  ScanSmem scan;
+  struct {
+    int wrun[kRouteWarps][256];
+    int off[256];
+  } scatter;
+};
+
+// Router and permutation builder in one cooperative launch: the same three
+// steps as route_kernel, scan_kernel and scatter_kernel, with grid barriers
+// in place of kernel boundaries, so the tables are bit-identical to theirs.
+//   1. Each block routes histogram blocks hb = blockIdx.x, + gridDim.x, ...
+//      and writes their expert counts hist[e][hb].
+//   2. Each block scans whole expert rows: base[e][b] = slots of expert e
+//      in blocks < b, counts[e] = the row's total.
+//   3. Every block turns counts into offsets (block 0 stores them) and
+//      ranks its histogram blocks' slots (address = offsets[e] + base[e][b]
+//      + earlier slots of block b with expert e).
+// Two CTAs per SM (32 registers a thread) where the router's rows fit.
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 2 : 1)
+    route_tables_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm, int nb, int R,
+                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist,
+                        int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
+                        int32_t* __restrict__ row_slot, int* err) {
+  __shared__ RouteTablesSmem sm;
+  int* bar = err + kErrBarrierWord;
+  for (int hb = blockIdx.x; hb < nb; hb += gridDim.x) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sm.hist[e] = 0;
+    __syncthreads();
+    route_block<EPL>(logits, hb, T, E, k, renorm, topk_idx, topk_w, sm.hist, err);
+    __syncthreads();
+    // Thread e reads sm.hist[e] here and zeroes it next iteration itself.
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(e) * nb + hb] = sm.hist[e];
+  }
+  if (!grid_barrier(bar, err, 1)) {
+    placeholder_tables(T, E, k, nb, counts, offsets, dest, row_token, row_slot);
+    return;
+  }
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const size_t row = static_cast<size_t>(e) * nb;
+    const int total = block_exclusive_scan(hist + row, nb, base + row, sm.scan);
+    if (threadIdx.x == 0) counts[e] = total;
+  }
+  if (!grid_barrier(bar, err, 2)) {
+    placeholder_tables(T, E, k, nb, counts, offsets, dest, row_token, row_slot);
+    return;
+  }
+  if (threadIdx.x < 32) {  // E <= 256: eight experts per lane
+    const int lane = threadIdx.x;
+    int v[8];
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      v[j] = e < E ? __ldcg(counts + e) : 0;
+      local += v[j];
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      if (e < E) {
+        sm.scatter.off[e] = run;
+        if (blockIdx.x == 0) offsets[e] = run;
+      }
+      run += v[j];
+    }
+    if (blockIdx.x == 0 && lane == 0) offsets[E] = R;
+  }
+  __syncthreads();
+  for (int hb = blockIdx.x; hb < nb; hb += gridDim.x) {
+    scatter_block<kRouteWarps>(topk_idx, base, sm.scatter.off, hb, T, E, k, nb, sm.scatter.wrun, dest, row_token,
+                               row_slot);
+    __syncthreads();  // the next block zeroes wrun
   }
 }
 
@@ -505,32 +689,41 @@ __global__ void __launch_bounds__(256)
       my_w = topk_w[static_cast<size_t>(t) * k + lane];
       my_dw = dw[static_cast<size_t>(t) * k + lane];
     }
-    float inner = 0.f;  // sum_j dw_j w_j in slot order
-    for (int j = 0; j < k; ++j)
-      inner += __shfl_sync(kFull, my_dw, j) * __shfl_sync(kFull, my_w, j);
+    // One pass over the k slots: inner = sum_j dw_j w_j in slot order, and
+    // each entry this lane holds learns whether (and in which slot) it was
+    // picked.
+    float inner = 0.f;
+    float pick_dw[EPL], pick_w[EPL];
+    bool picked[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      pick_dw[i] = pick_w[i] = 0.f;
+      picked[i] = false;
+    }
+    for (int j = 0; j < k; ++j) {
+      const int sj = __shfl_sync(kFull, my_idx, j);
+      const float dj = __shfl_sync(kFull, my_dw, j);
+      const float wj = __shfl_sync(kFull, my_w, j);
+      inner += dj * wj;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (sj == lane + 32 * i) {
+          picked[i] = true;
+          pick_dw[i] = dj;
+          pick_w[i] = wj;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      float pick_dw = 0.f, pick_w = 0.f;
-      bool picked = false;
-      for (int j = 0; j < k; ++j) {
-        const int sj = __shfl_sync(kFull, my_idx, j);
-        const float dj = __shfl_sync(kFull, my_dw, j);
-        const float wj = __shfl_sync(kFull, my_w, j);
-        if (sj == e) {
-          picked = true;
-          pick_dw = dj;
-          pick_w = wj;
-        }
-      }
       if (e < E) {
         float dz;
         if (!ok)
           dz = 0.f;
         else if (renorm == 0)
-          dz = (r.ex[i] / r.s) * ((picked ? pick_dw : 0.f) - inner);
+          dz = (r.ex[i] / r.s) * ((picked[i] ? pick_dw[i] : 0.f) - inner);
         else
-          dz = picked ? pick_w * (pick_dw - inner) : 0.f;
+          dz = picked[i] ? pick_w[i] * (pick_dw[i] - inner) : 0.f;
         dlogits[static_cast<size_t>(t) * E + e] = dz;
       }
     }
@@ -567,6 +760,46 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
   else
     route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, renorm, topk_idx, topk_w, hist, nb, err);
   return cudaGetLastError();
+}
+
+namespace {
+template <int EPL>
+cudaError_t launch_route_tables_epl(const float* logits, int T, int E, int k, int renorm, int nb, int32_t* topk_idx,
+                                    float* topk_w, int32_t* hist, int32_t* base, int32_t* counts, int32_t* offsets,
+                                    int32_t* dest, int32_t* row_token, int32_t* row_slot, int* err, int max_grid,
+                                    cudaStream_t s) {
+  static int per_sm = 0;  // blocks of this kernel resident per SM
+  if (per_sm == 0) {
+    int n = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_tables_kernel<EPL>, kRouteWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorCooperativeLaunchTooLarge;
+    per_sm = n;
+  }
+  int grid = std::min(nb, per_sm * num_sms());
+  if (max_grid > 0) grid = std::min(grid, max_grid);
+  int R = T * k;
+  void* args[] = {&logits, &T,    &E,      &k,    &renorm,    &nb,       &R,   &topk_idx, &topk_w,
+                  &hist,   &base, &counts, &offsets, &dest, &row_token, &row_slot, &err};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(route_tables_kernel<EPL>), dim3(grid),
+                                     dim3(kRouteWarps * 32), args, 0, s);
+}
+}  // namespace
+
+cudaError_t launch_route_tables(const float* logits, int T, int E, int k, int renorm, int nb, int32_t* topk_idx,
+                                float* topk_w, int32_t* hist, int32_t* base, int32_t* counts, int32_t* offsets,
+                                int32_t* dest, int32_t* row_token, int32_t* row_slot, int* err, int max_grid,
+                                cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_ROUTE_TABLES, s);
+#define MOE_ROUTE_TABLES(EPL)                                                                                    \
+  launch_route_tables_epl<EPL>(logits, T, E, k, renorm, nb, topk_idx, topk_w, hist, base, counts, offsets, dest, \
+                               row_token, row_slot, err, max_grid, s)
+  if (E <= 32) return MOE_ROUTE_TABLES(1);
+  if (E <= 64) return MOE_ROUTE_TABLES(2);
+  if (E <= 128) return MOE_ROUTE_TABLES(4);
+  return MOE_ROUTE_TABLES(8);
+#undef MOE_ROUTE_TABLES
 }
 
 cudaError_t launch_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* hist, int nb, int* err,

@@ -66,6 +66,7 @@ _SIGS = {
     "moe_gemm_pair_capacity": ([_I], _I),
     "moe_set_gemm_prefetch": ([_I, _I], _I),
     "moe_set_bwd_overlap": ([_I], _I),
+    "moe_set_route_fusion": ([_I], _I),
     "moe_autotune": ([_CFG] + [_P] * 15 + [_I, _P, ctypes.POINTER(moe_tune_result)], _I),
     "moe_debug_skip_megakernel_task": ([_I], _I),
     "moe_debug_megakernel_trace": ([_P, _I], _I),
@@ -78,7 +79,8 @@ _SIGS = {
 # kernel kinds of the timing trace (MOE_K_* in include/moe.h)
 TRACE_KINDS = ["route", "hist", "scan", "scatter", "gather", "gemm1_swiglu", "gemm2_scale", "combine",
                "combine_bwd", "gemm_dh", "dw_reduce", "route_bwd", "gemm_dx", "dispatch_bwd", "gemm_dw13",
-               "gemm_dw2", "megakernel", "megakernel_bwd"]
+               "gemm_dw2", "megakernel", "megakernel_bwd",
+               "route_tables"]
 
 _lib = None
 
@@ -244,6 +246,11 @@ def moe_set_bwd_overlap(on: bool) -> int:
     return int(lib().moe_set_bwd_overlap(int(bool(on))))
 
 
+def moe_set_route_fusion(on: bool) -> int:
+    """Router and permutation tables of moe_layer_fwd as one cooperative launch. Returns the previous setting."""
+    return int(lib().moe_set_route_fusion(int(bool(on))))
+
+
 def moe_gemm_pair_capacity(kind: int) -> int:
     """CTA pairs of grouped-GEMM kind `kind` resident at once on the current device."""
     return int(lib().moe_gemm_pair_capacity(int(kind)))
@@ -319,7 +326,7 @@ def ws_view(ws: torch.Tensor, cfg: MoEConfig, name: str) -> torch.Tensor:
     """A typed view of one workspace region."""
     T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
     R, Rs = T * k, T * k + S * T
-    shapes = {"counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
+    shapes = {"err": ((16,), torch.int32), "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
               "row_token": ((R,), torch.int32), "row_slot": ((R,), torch.int32),
               "Xp": ((R, d), torch.bfloat16), "AB": ((Rs, 2 * f), torch.bfloat16), "H": ((Rs, f), torch.bfloat16),
               "Op": ((Rs, d), torch.float32), "G": ((R, d), torch.bfloat16), "dAB": ((Rs, 2 * f), torch.bfloat16),

@@ -168,7 +168,9 @@ int moe_combine(const moe_cfg* cfg, const float* Oprime, const int32_t* dest,
  * runs dispatch..combine as one persistent launch that claims tasks from an
  * atomic ticket counter and orders them with device-side readiness counters
  * (UniEP page, section 2.2: persistent workers, scoreboard, dynamic SM
- * scheduling); its outputs are bitwise equal to use_megakernel = 0. */
+ * scheduling); its outputs are bitwise equal to use_megakernel = 0.
+ * Route and the permutation tables run as one cooperative launch with grid
+ * barriers between histogram, scan and scatter (see moe_set_route_fusion). */
 int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x,
                   const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
                   float* y, int32_t* topk_idx, float* topk_w, void* ws,
@@ -254,11 +256,22 @@ int moe_get_device_error(const void* ws, void* stream, int* code, int* info);
  * its persistent kernels). */
 int moe_num_sms(void);
 
-/* Caps the number of CTAs of the persistent kernels (grouped GEMMs and the
- * MegaKernel) at n; n <= 0 restores one CTA per SM.  Results never depend
+/* Caps the number of CTAs of the persistent kernels (grouped GEMMs, the
+ * MegaKernel and the fused routing launch) at n; n <= 0 restores one CTA per SM.  Results never depend
  * on it (each output element has one fixed producer and reduction order);
  * it exists to test exactly that.  Process-wide, not thread-safe. */
 int moe_set_grid_limit(int n);
+
+/* Fused routing of moe_layer_fwd.  On (the default), the router, the
+ * per-block expert histogram, the scan and the stable scatter run as one
+ * cooperative launch (every CTA resident; two grid barriers, each a bounded
+ * wait that sets MOE_ERR_TIMEOUT rather than hang; the barrier state lives in
+ * the error region, so after a timeout call moe_ws_init).  Off, or where the
+ * device refuses the cooperative launch, they run as three kernels.  The
+ * tables are bitwise the same either way, and the CTA cap of
+ * moe_set_grid_limit applies to this launch too.  Returns the previous
+ * setting.  Process-wide, not thread-safe. */
+int moe_set_route_fusion(int on);
 
 /* B/W overlap of moe_layer_bwd with which == 3 (GraphPP page, section 2:
  * input gradients B on the critical path, weight gradients W deferrable).
@@ -353,7 +366,8 @@ enum {
   MOE_K_GEMM_DW2 = 15,    /* ragged-K grouped GEMM dW2 */
   MOE_K_MEGAKERNEL = 16,  /* forward MegaKernel */
   MOE_K_MEGAKERNEL_BWD = 17, /* backward (input-gradient) MegaKernel */
-  MOE_K_COUNT = 18
+  MOE_K_ROUTE_TABLES = 18, /* router + histogram + scan + scatter, one launch */
+  MOE_K_COUNT = 19
 };
 /* Testing aid for failure detection (no device fault involved): the forward
  * MegaKernel claims task `ticket` but never runs or signals it, so the

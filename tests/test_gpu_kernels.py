@@ -76,6 +76,43 @@ def test_route_ties_and_signed_zero():
     np.testing.assert_allclose(np64(w), ref.w, rtol=4e-6)
 
 
+@pytest.mark.parametrize("E,k", [(20, 3), (48, 6), (200, 8)])
+def test_route_extreme_and_tied_values(E, k):
+    """Logits drawn from a small set of extreme and tied values (+-FLT_MAX,
+    the smallest denormals, the smallest normal, signed zeros, +-1): the
+    picks follow (value desc, index asc) exactly, with -0.0 == +0.0 and
+    denormals ordered by value, through the router and through the fused
+    routing of the layer forward."""
+    cfg = MoEConfig(f"extreme_E{E}_k{k}", 1500, 64, 64, E, k)
+    tiny = np.finfo(np.float32).tiny
+    fmax = np.finfo(np.float32).max
+    dmin = np.float32(1e-45)
+    vals = np.array([fmax, -fmax, dmin, -dmin, 2 * dmin, tiny, -tiny, 0.0, -0.0, 1.0, -1.0, 1.0, 0.0],
+                    dtype=np.float32)
+    rng = np.random.default_rng(E)
+    z = torch.from_numpy(vals[rng.integers(0, len(vals), size=(cfg.T, E))].copy())
+    z[: cfg.T // 2][z[: cfg.T // 2] == fmax] = 1.0  # half the rows without the saturating value
+    idx, w, ws = _route(cfg, z.to(DEV))
+    ref = O.route(z, cfg.k)
+    assert np.array_equal(idx.cpu().numpy(), ref.sel)
+    np.testing.assert_allclose(np64(w), ref.w, rtol=4e-6, atol=0)
+    assert device_error(ws) == (0, 0)
+    g = {"logits": z.to(DEV), "x": torch.zeros(cfg.T, cfg.d, dtype=torch.bfloat16, device=DEV),
+         "W1": torch.zeros(E, cfg.f, cfg.d, dtype=torch.bfloat16, device=DEV),
+         "W3": torch.zeros(E, cfg.f, cfg.d, dtype=torch.bfloat16, device=DEV),
+         "W2": torch.zeros(E, cfg.d, cfg.f, dtype=torch.bfloat16, device=DEV)}
+    ws2 = moe.alloc_workspace(cfg, DEV)
+    y = torch.empty(cfg.T, cfg.d, dtype=torch.float32, device=DEV)
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], y, idx2, w2, ws2)
+    assert device_error(ws2) == (0, 0)
+    assert torch.equal(idx2, idx) and torch.equal(w2, w)
+    perm = O.permute(ref.sel, E)
+    for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
+        assert np.array_equal(moe.ws_view(ws2, cfg, name).cpu().numpy(), getattr(perm, name)), name
+
+
 def test_hand_case_through_the_library():
     cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "route_hand_T8E4k2.json")))["cases"]
     for case in cases:

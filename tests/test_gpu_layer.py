@@ -235,6 +235,75 @@ def test_megakernel_wait_timeout_is_reported_and_context_survives():
         assert torch.equal(ref[k], again[k]), k
 
 
+TABLES = ("counts", "offsets", "dest", "row_token", "row_slot")
+# ragged T, one expert row per lane (E = 32), the wider rows (E = 100, 256),
+# and a single histogram block (T = 8)
+ROUTE_CFGS = [TINY, MID, SKEW, EK, MoEConfig("e100_T1234_d64_f64_E100_k5", 1234, 64, 64, 100, 5),
+              MoEConfig("e256_T333_d64_f64_E256_k8_renorm", 333, 64, 64, 256, 8, renorm=1),
+              MoEConfig("t8_d64_f64_E4_k2", 8, 64, 64, 4, 2)]
+
+
+def _fwd_tables(cfg, g, fused, grid):
+    prev = moe.moe_set_route_fusion(fused)
+    moe.moe_set_grid_limit(grid)
+    try:
+        ws = moe.alloc_workspace(cfg, DEV)
+        out = empty_outputs(cfg)
+        moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["topk_idx"],
+                          out["topk_w"], ws)
+        assert device_error(ws) == (0, 0)
+        res = {name: moe.ws_view(ws, cfg, name).clone() for name in TABLES}
+        res.update(topk_idx=out["topk_idx"], topk_w=out["topk_w"], y=out["y"])
+        return res
+    finally:
+        moe.moe_set_route_fusion(prev)
+        moe.moe_set_grid_limit(0)
+
+
+@pytest.mark.parametrize("cfg", ROUTE_CFGS, ids=lambda c: c.name)
+def test_fused_routing_tables_equal_three_kernels_and_oracle(cfg):
+    """The cooperative route + histogram + scan + scatter launch gives the
+    tables of the three separate kernels bit for bit, on any grid (one CTA
+    walks every histogram block and every expert row), and they are the
+    oracle's permutation."""
+    inp = make_layer_inputs(cfg, seed=21)
+    g = to_dev(inp)
+    ref = _fwd_tables(cfg, g, fused=0, grid=0)
+    for grid in (0, 1, 3):
+        got = _fwd_tables(cfg, g, fused=1, grid=grid)
+        for name in ref:
+            assert torch.equal(got[name], ref[name]), (grid, name)
+    routing = O.route(inp.logits, cfg.k, cfg.renorm)
+    perm = O.permute(routing.sel, cfg.E)
+    assert np.array_equal(ref["topk_idx"].cpu().numpy(), routing.sel)
+    for name in TABLES:
+        assert np.array_equal(ref[name].cpu().numpy(), getattr(perm, name)), name
+
+
+def test_fused_routing_barrier_timeout_is_reported_and_context_survives():
+    """A grid barrier whose arrival count is poisoned on the host (no CTA is
+    ever the last to arrive) runs out its bounded wait: the launch returns
+    with MOE_ERR_TIMEOUT in the device error word instead of hanging, and
+    after moe_ws_init the same workspace routes correctly again."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=22))
+    ref = _fwd_tables(cfg, g, fused=0, grid=0)
+    ws = moe.alloc_workspace(cfg, DEV)
+    out = empty_outputs(cfg)
+    moe.ws_view(ws, cfg, "err")[8] = -5
+    moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["topk_idx"],
+                      out["topk_w"], ws)
+    code, info = device_error(ws)
+    assert code == moe.MOE_ERR_TIMEOUT and info == 1, (code, info)
+    moe.moe_ws_init(cfg, ws)
+    moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["topk_idx"],
+                      out["topk_w"], ws)
+    assert device_error(ws) == (0, 0)
+    for name in TABLES:
+        assert torch.equal(moe.ws_view(ws, cfg, name), ref[name]), name
+    assert torch.equal(out["y"], ref["y"])
+
+
 BWD_MK = 3 | moe.MOE_BWD_MEGAKERNEL
 
 
