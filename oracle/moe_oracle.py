@@ -358,17 +358,16 @@ def dW_entries(x, logits, W1, W3, W2, dy, k: int, S: int, renorm: int,
         tok = np.arange(T); wgt = np.ones(T)
     rows = np.asarray(rows); cols = np.asarray(cols)
     xr = take_rows(x, tok); g = take_rows(dy, tok)
-    out = np.zeros(len(rows))
-    for i, (m, c) in enumerate(zip(rows, cols)):
-        if which in ("W1", "W3"):
-            n = m
-            a = xr @ W1e[n]; b = xr @ W3e[n]
-            dh = wgt * (g @ W2e[:, n])
-            grad_pre = dh * b * dsilu(a) if which == "W1" else dh * silu(a)
-            out[i] = grad_pre @ xr[:, c]
-        else:  # W2[c_out=m, n=c]
-            n = c
-            a = xr @ W1e[n]; b = xr @ W3e[n]
-            h = silu(a) * b
-            out[i] = (wgt * g[:, m]) @ h
-    return out
+    # The hidden unit n of each entry: the row of dW1/dW3, the column of dW2.
+    # The segment-long columns a[:, n], b[:, n] (and dh[:, n]) are formed once
+    # per distinct n, all of them in one product with the segment.
+    ns, j = np.unique(rows if which in ("W1", "W3") else cols, return_inverse=True)
+    a = xr @ W1e[ns].T; b = xr @ W3e[ns].T  # [segment rows, distinct n]
+    if which in ("W1", "W3"):
+        dh = wgt[:, None] * (g @ W2e[:, ns])
+        grad_pre = dh * b * dsilu(a) if which == "W1" else dh * silu(a)
+        # dW1/dW3[n, c] = sum over the segment of grad_pre[:, n] * x[:, c]
+        return np.einsum("ri,ri->i", grad_pre[:, j], xr[:, cols])
+    h = silu(a) * b
+    # dW2[m, n] = sum over the segment of (w * g)[:, m] * h[:, n]
+    return np.einsum("ri,ri->i", wgt[:, None] * g[:, rows], h[:, j])

@@ -362,10 +362,11 @@ def test_bwd_megakernel_wait_timeout_is_reported_and_context_survives():
 @pytest.mark.parametrize("cfg", [DSV2_LITE, MIXTRAL, SKEWED, LONG128K], ids=lambda c: c.name)
 def test_full_size_sampled_parity(cfg):
     """Every workload at full size, in the benchmark's launch configuration:
-    routing and the permutation in full, y / dx / dlogits on 256 seeded
-    tokens (128 for the widest layers), and weight-gradient entries of
-    several experts (largest, smallest, a middle one, the shared ones)
-    summed over their whole segments; empty experts' gradients exactly 0."""
+    routing and the permutation in full, y / dx / dlogits on 2048 seeded
+    tokens, and 352 weight-gradient entries of each of dW1, dW3 and dW2 for
+    several experts (largest, smallest, a middle one, one more, the shared
+    ones; 4224 entries or more), each summed over the expert's whole segment;
+    empty experts' gradients exactly 0."""
     inp = make_layer_inputs(cfg, seed=0)
     out, ws = run_layer(cfg, to_dev(inp))
     assert device_error(ws) == (0, 0)
@@ -375,7 +376,7 @@ def test_full_size_sampled_parity(cfg):
     for name in ("counts", "offsets", "dest", "row_token", "row_slot"):
         assert np.array_equal(moe.ws_view(ws, cfg, name).cpu().numpy(), getattr(perm, name)), name
     rng = np.random.default_rng(0)
-    ntok = 128 if cfg.f * cfg.d > 8e6 else 256
+    ntok = 2048
     toks = np.sort(rng.choice(cfg.T, ntok, replace=False))
     _, y, dx, dz, _ = O.tokens_fwd_bwd(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
                                        cfg.renorm, toks)
@@ -385,6 +386,8 @@ def test_full_size_sampled_parity(cfg):
     counts = perm.counts
     nonempty = np.nonzero(counts)[0]
     experts = [int(np.argmax(counts)), int(nonempty[np.argmin(counts[nonempty])]), int(nonempty[len(nonempty) // 2])]
+    others = [int(e) for e in nonempty if int(e) not in experts]
+    experts += [others[int(rng.integers(0, len(others)))]] if others else []
     experts += [cfg.E + s for s in range(cfg.S)]
     for e in np.nonzero(counts == 0)[0][:4]:  # empty experts: exact zeros
         for gpu in (out["dW1"], out["dW3"], out["dW2"]):
@@ -392,7 +395,14 @@ def test_full_size_sampled_parity(cfg):
     for which, gpu in (("W1", out["dW1"]), ("W3", out["dW3"]), ("W2", out["dW2"])):
         for e in experts:
             nr, nc = gpu.shape[1], gpu.shape[2]
-            rows, cols = rng.integers(0, nr, 64), rng.integers(0, nc, 64)
+            # 22 hidden units x 16 entries each (the oracle forms one
+            # segment-long column per hidden unit)
+            nf = nr if which in ("W1", "W3") else nc
+            units = np.repeat(rng.choice(nf, 22, replace=False), 16)
+            if which in ("W1", "W3"):
+                rows, cols = units, rng.integers(0, nc, units.size)
+            else:
+                rows, cols = rng.integers(0, nr, units.size), units
             ref = O.dW_entries(inp.x, inp.logits.numpy(), inp.W1, inp.W3, inp.W2, inp.dy, cfg.k, cfg.S,
                                cfg.renorm, which, e, rows, cols, routing=routing, perm=perm)
             got = np64(gpu[e])[rows, cols]

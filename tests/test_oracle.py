@@ -244,7 +244,8 @@ def test_sampled_evaluators_agree_with_full_layer():
     rng = np.random.default_rng(1)
     for which, full in [("W1", bw.dW1), ("W3", bw.dW3), ("W2", bw.dW2)]:
         for e in range(E + S):
-            rows = rng.integers(0, full.shape[1], 5)
-            cols = rng.integers(0, full.shape[2], 5)
+            # repeated rows and columns: entries that share a hidden unit
+            rows = np.concatenate([rng.integers(0, full.shape[1], 5), [1, 1, 1]])
+            cols = np.concatenate([rng.integers(0, full.shape[2], 5), [2, 0, 2]])
             got = O.dW_entries(x, z.numpy(), W1, W3, W2, dy, k, S, 0, which, e, rows, cols)
             np.testing.assert_allclose(got, full[e][rows, cols], rtol=1e-12, atol=1e-13)
