@@ -176,7 +176,7 @@ int moe_ws_init(const moe_cfg* cfg, void* ws, void* stream) {
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({}, {}, ws));
   const WsLayout L = ws_layout(*cfg);
-  MOE_TRY_CUDA(cudaMemsetAsync(at<uint8_t>(ws, L.err), 0, 64, static_cast<cudaStream_t>(stream)));
+  MOE_TRY_CUDA(cudaMemsetAsync(at<uint8_t>(ws, L.err), 0, kErrRegionBytes, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

@@ -29,6 +29,11 @@ __device__ __forceinline__ void record_error(int* err, int code, int info) {
 // after every completed barrier) and the generation.  moe_ws_init zeroes
 // them with the error word.
 constexpr int kErrBarrierWord = 8;
+// Words of the error region (which spans 256 bytes) that hold each grouped
+// GEMM kind's tile-ticket counter and finished-CTA count, two per kind from
+// this word on; both are back at 0 after every complete launch.
+constexpr int kErrSchedWord = 16;
+constexpr int kErrRegionBytes = 256;
 
 // Router / permutation: tokens per block (8 warps x 4 tokens).  Small blocks
 // give the latency-bound router enough warps; the per-block histogram the
@@ -75,7 +80,7 @@ inline WsLayout ws_layout(const moe_cfg& c) {
     o = align_up(o + bytes, 256);
     return at;
   };
-  L.err = take(64);
+  L.err = take(kErrRegionBytes);
   L.hist = take(sizeof(int) * E * L.nb_route);
   L.base = take(sizeof(int) * E * L.nb_route);
   L.counts = take(sizeof(int) * E);

@@ -52,6 +52,9 @@ namespace moe {
 namespace {
 
 constexpr int kMaxStages = 6;
+// Tile numbers in flight from the ticket-taking producer to the other roles
+// (dynamic tile scheduling of the grouped GEMM kernels).
+constexpr int kTileRing = 8;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB (one CTA per tile)
@@ -116,6 +119,8 @@ struct SharedState {
   uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain;
   uint64_t ready[kMaxStages];  // CG = 2, even CTA: the odd CTA's stage has landed
   uint64_t aux[kEpiWarps][2];  // dH epilogue input buffers of each warp
+  uint64_t tile_full[kTileRing], tile_empty[kTileRing];  // tile-number ring
+  int tile_ring[kTileRing];
   uint32_t tmem_base;
   int abort;
   int nseg;
@@ -651,8 +656,15 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
 
 // CG = 2: the even CTA's tempty barriers count the epilogue warps of both
 // CTAs; ready[s] takes the odd CTA's word that its part of stage s landed.
+// tile_empty (used in the even CTA, or the only one) counts every role that
+// reads a tile number from the ring: the MMA warp and the epilogue warps of
+// both CTAs, and the odd CTA's producer.
 template <int CG = 1>
 __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
+  for (int i = 0; i < kTileRing; ++i) {
+    mbar_init(&ss.tile_full[i], 1);
+    mbar_init(&ss.tile_empty[i], CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 1 + kEpiWarps);
+  }
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&ss.full[s], 1);
     mbar_init(&ss.empty[s], 1);

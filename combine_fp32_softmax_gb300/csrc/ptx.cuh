@@ -128,6 +128,17 @@ __device__ __forceinline__ void mbar_arrive_rank(uint64_t* bar, uint32_t rank) {
       : "memory");
 }
 
+// Stores v at the same shared-memory offset as `p` in the cluster's CTA
+// `rank`.
+__device__ __forceinline__ void st_shared_rank(int* p, uint32_t rank, int v) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "st.shared::cluster.u32 [ra], %2;\n\t}" ::"r"(smem_u32(p)),
+      "r"(rank), "r"(v)
+      : "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

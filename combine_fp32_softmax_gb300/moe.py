@@ -312,7 +312,7 @@ def ws_offsets(cfg: MoEConfig) -> dict:
         out[name] = o
         o = (o + nbytes + 255) // 256 * 256
 
-    for name, nbytes in [("err", 64), ("hist", 4 * E * nb), ("base", 4 * E * nb), ("counts", 4 * E),
+    for name, nbytes in [("err", 256), ("hist", 4 * E * nb), ("base", 4 * E * nb), ("counts", 4 * E),
                          ("offsets", 4 * (E + 1)), ("dest", 4 * R), ("row_token", 4 * R),
                          ("row_slot", 4 * R), ("Xp", 2 * R * d), ("AB", 4 * Rs * f), ("H", 2 * Rs * f),
                          ("Op", 4 * Rs * d), ("G", 2 * R * d), ("dAB", 4 * Rs * f), ("Hw", 2 * Rs * f),
@@ -326,7 +326,7 @@ def ws_view(ws: torch.Tensor, cfg: MoEConfig, name: str) -> torch.Tensor:
     """A typed view of one workspace region."""
     T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
     R, Rs = T * k, T * k + S * T
-    shapes = {"err": ((16,), torch.int32), "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
+    shapes = {"err": ((64,), torch.int32), "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
               "row_token": ((R,), torch.int32), "row_slot": ((R,), torch.int32),
               "Xp": ((R, d), torch.bfloat16), "AB": ((Rs, 2 * f), torch.bfloat16), "H": ((Rs, f), torch.bfloat16),
               "Op": ((Rs, d), torch.float32), "G": ((R, d), torch.bfloat16), "dAB": ((Rs, 2 * f), torch.bfloat16),
