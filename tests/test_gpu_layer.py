@@ -57,17 +57,56 @@ def test_bitwise_identical_across_10_runs():
     assert len(digests) == 1
 
 
+def _sched_words_clear(ws, cfg):
+    """The routing grid barrier's arrival count and every grouped-GEMM kind's
+    tile-ticket counter and finished-CTA count are back at 0."""
+    err = moe.ws_view(ws, cfg, "err").cpu().numpy()
+    return err[8] == 0 and not err[16:16 + 2 * len(moe.GEMM_KINDS)].any()
+
+
 def test_results_do_not_depend_on_grid_size():
+    """Any CTA cap (one CTA, an odd count, all SMs) gives the same bits: every
+    output element has one producer and one reduction order, whether its tile
+    came from the static round-robin or the ticket counter.  The scheduling
+    counters are back at 0 after every call."""
     cfg = SKEW
     g = to_dev(make_layer_inputs(cfg, seed=13))
     digests = set()
     try:
         for n in (1, 7, 0):
             moe.moe_set_grid_limit(n)
-            digests.add(_digest(run_layer(cfg, g)[0]))
+            out, ws = run_layer(cfg, g)
+            digests.add(_digest(out))
+            assert device_error(ws) == (0, 0)
+            assert _sched_words_clear(ws, cfg)
     finally:
         moe.moe_set_grid_limit(0)
     assert len(digests) == 1
+
+
+def test_weight_gradient_tickets_reset_between_launches():
+    """Many back-to-back weight-gradient launches (the W part alone, on the B
+    part's dA|dB and Hw kept in the workspace; both tile shapes) keep giving
+    the same bits: each launch starts from a ticket counter that the previous
+    one's last CTA set back to 0."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=23))
+    ref, ws = run_layer(cfg, g)
+    prev = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
+    try:
+        for mask in (moe.ALL_PAIR_KINDS, 0, moe.ALL_PAIR_KINDS):
+            moe.moe_set_gemm_pair_kinds(mask)
+            for _ in range(4):
+                out = empty_outputs(cfg)
+                moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"], ref["topk_idx"],
+                                  ref["topk_w"], ws, out["dx"], out["dlogits"], out["dW1"], out["dW3"], out["dW2"],
+                                  which=2)
+                assert device_error(ws) == (0, 0)
+                assert _sched_words_clear(ws, cfg)
+                for k in ("dW1", "dW3", "dW2"):
+                    assert torch.equal(out[k], ref[k]), (mask, k)
+    finally:
+        moe.moe_set_gemm_pair_kinds(prev)
 
 
 @pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
