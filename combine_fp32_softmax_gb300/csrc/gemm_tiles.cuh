@@ -94,11 +94,11 @@ struct Traits {
   static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
   // fp32 kinds: 16-column chunks, two staging buffers in flight.
   static constexpr int F32_ROUNDS = 2;
-  // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two input buffers
-  // ([a, b, H] chunks) plus one output chunk of dA, dB, Hw; fp32 kinds
-  // F32_ROUNDS output chunks.
+  // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two buffers of three
+  // chunks, each taking a chunk's [a, b, H] inputs and then, in place, its
+  // dA, dB, Hw outputs; fp32 kinds F32_ROUNDS output chunks.
   static constexpr int EPI_BYTES = (KIND == kG1)   ? 3 * kChunkBytes
-                                   : (KIND == kDH) ? 9 * kChunkBytes
+                                   : (KIND == kDH) ? 6 * kChunkBytes
                                                    : F32_ROUNDS * kChunkBytes;
 };
 
@@ -112,7 +112,7 @@ struct Pipe {
   static constexpr int B_BYTES = kBBytes / CG;
   static constexpr int B_BOXES = 4 / CG;  // MN-major B: 64-column boxes per CTA
   static constexpr int STAGE_BYTES = kABytes + B_BYTES;
-  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 4 : 6);
+  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 5 : 6);
 };
 
 struct SharedState {
@@ -542,8 +542,10 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
 }
 
 // dH: inputs a, b, H of the tile's 32-column chunks are TMA-loaded per warp
-// into two buffers (3 chunks of 2 KB each); outputs dA, dB, Hw are staged
-// in a third.
+// into two buffers (3 chunks of 2 KB each); a chunk's outputs dA, dB, Hw are
+// staged in the buffer its inputs came in, which is refilled (two chunks
+// ahead) once the output stores have read it.  Sharing the buffers this way
+// left room for a fifth pipeline stage on CTA pairs.
 __device__ __forceinline__ int dh_chunks(const GemmParams& p, const TileInfo& t) {
   return min(8, (p.f - t.n0 + 31) / 32);
 }
@@ -582,7 +584,6 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
   if (rowok && !t.shared) w = p.topk_w[p.row_slot[grow]];
   uint16_t* dAB = static_cast<uint16_t*>(p.out0);
   uint16_t* Hw = static_cast<uint16_t*>(p.out1);
-  uint8_t* out = stg + 6 * kChunkBytes;
   const int nch = dh_chunks(p, t);
   const uint32_t first = es.auxn - (nch > 1 ? 2 : 1);  // input chunk index of chunk 0
   float dot = 0.f;
@@ -602,10 +603,8 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
     load_row64(in, lane, aw);
     load_row64(in + kChunkBytes, lane, bw);
     load_row64(in + 2 * kChunkBytes, lane, hw);
-    // the buffer is free again: every lane has its row in registers
-    fence_proxy_async_smem();
+    // every lane has its rows in registers: the buffer now takes the outputs
     __syncwarp();
-    if (c + 2 < nch) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
     uint32_t ra[16], rb[16], rh[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -627,8 +626,9 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
       rb[u] = pack_bf16(dB2[0], dB2[1]);
       rh[u] = pack_bf16(hw2[0], hw2[1]);
     }
+    uint8_t* out = stg + buf * 3 * kChunkBytes;
     if (full) {
-      staging_reuse_wait<0>(es.chunks);
+      // Each lane overwrites only the row it read.
       stage_row64(out, lane, ra);
       stage_row64(out + kChunkBytes, lane, rb);
       stage_row64(out + 2 * kChunkBytes, lane, rh);
@@ -638,13 +638,20 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
         tma_store_2d(&p.tmO0, out + kChunkBytes, p.f + n, orow0);
         tma_store_2d(&p.tmO1, out + 2 * kChunkBytes, n, orow0);
         bulk_commit();
+        if (c + 2 < nch) bulk_wait_read<0>();  // the stores have read the buffer before it is refilled
       }
+      __syncwarp();
       ++es.chunks;
-    } else if (rowok) {
-      store_words16(dAB + grow * 2 * p.f + n, ra);
-      store_words16(dAB + grow * 2 * p.f + p.f + n, rb);
-      store_words16(Hw + grow * p.f + n, rh);
+    } else {
+      if (rowok) {
+        store_words16(dAB + grow * 2 * p.f + n, ra);
+        store_words16(dAB + grow * 2 * p.f + p.f + n, rb);
+        store_words16(Hw + grow * p.f + n, rh);
+      }
+      fence_proxy_async_smem();  // the inputs' generic reads before the refill's TMA writes
+      __syncwarp();
     }
+    if (c + 2 < nch) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
   }
   if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + t.n0 / kBN] = dot;
   return true;
