@@ -35,9 +35,10 @@ constexpr int kErrBarrierWord = 8;
 constexpr int kErrSchedWord = 16;
 constexpr int kErrRegionBytes = 256;
 
-// Router / permutation: tokens per block (8 warps x 4 tokens).  Small blocks
-// give the latency-bound router enough warps; the per-block histogram the
-// scan walks has E * ceil(T / 32) entries.
+// Router / permutation: tokens per histogram block (the router and the fused
+// routing kernel run one warp per token, the stand-alone scatter 8 warps of 4
+// tokens).  Small blocks give the latency-bound router enough warps; the
+// per-block histogram the scan walks has E * ceil(T / 32) entries.
 constexpr int kRouteTokensPerBlock = 32;
 
 // Grouped GEMM tile: 128 rows x 256 accumulator columns, K staged 64 at a

@@ -18,7 +18,7 @@
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //               (256 x 64, or this CTA's 128 x 64 half on a CTA pair) into
 //               a shared-memory ring: 3-4 stages of 48 KB (one CTA per
-//               tile), 4-6 of 32 KB (pairs).  MN-major operands come as one
+//               tile), 5-6 of 32 KB (pairs).  MN-major operands come as one
 //               3D box per operand (map3d_mn).
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma from one lane
 //               (M=128, or M=256 on a pair from the even CTA; N=256, K=16,
@@ -31,11 +31,14 @@
 //               tensor stores (coalesced, asynchronous).  Warps whose 32
 //               rows are not all valid (a segment's last m-tile) store
 //               their valid rows directly.  The dH epilogue TMA-loads its
-//               elementwise inputs ([a|b], H) per warp, double-buffered.
+//               elementwise inputs ([a|b], H) per warp, double-buffered,
+//               and stages its outputs in the buffer the inputs came in.
 //   The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 //   epilogue of tile i overlaps the main loop of tile i+1.
-// Tiles are taken in a static round-robin over CTAs; every output element is
-// produced by exactly one tile with a fixed K order.
+// Tiles of equal length are taken in a static round-robin over CTAs, those of
+// the weight-gradient kinds from a ticket counter (grouped_gemm.cu); either
+// way every output element is produced by exactly one tile with a fixed K
+// order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -81,7 +81,8 @@ __device__ __forceinline__ void trace_record(const MegaParams& mp, int role, int
 }
 
 // Shapes of one MegaKernel: its two GEMM kinds and its pipeline depth
-// (forward 4 stages; backward 3, as dH's epilogue staging is 18 KB a warp).
+// (forward 4 stages of 48 KB; backward 3, as a fourth does not fit beside
+// dH's 12 KB a warp of epilogue staging).
 template <int KA, int KB, int NST>
 struct Mega {
   static constexpr int STAGES = NST;
