@@ -16,6 +16,7 @@ is the max over ranks and `value` counts the tokens of all ranks.
 `--impl reference` times the CPU fp64 oracle on the host cores instead.
 """
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -35,7 +36,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv2lite_T8192_d2048_f1408_E64_k6_S2")
@@ -101,23 +102,49 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms; only the
+    samples taken inside the timed window count."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu_index = gpu_index
         self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
         self.proc = None
+        self.window = None
 
     def start(self):
+        """Starts sampling and returns once the first sample is written (at
+        most 3 s), so the timed window that follows is covered."""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.gpu_index)], stdout=self.tmp,
+                                          "-lms", "50", "-i", str(self.gpu_index)], stdout=self.tmp,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t_end = time.time() + 3.0
+        while time.time() < t_end and os.path.getsize(self.tmp.name) == 0:
+            time.sleep(0.01)
+
+    def mark(self, t0, t1):
+        """Host wall-clock bounds of the timed window."""
+        self.window = (t0, t1)
+
+    def _rows(self):
+        rows = []
+        for line in open(self.tmp.name):
+            r = [c.strip() for c in line.strip().split(", ")]
+            if len(r) < 10 or not r[2].replace(".", "").isdigit():
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            rows.append((ts, r))
+        return rows
 
     def stop(self):
         if self.proc is None:
@@ -128,16 +155,25 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.tmp.flush()
-        rows = [l.strip().split(", ") for l in open(self.tmp.name) if l.strip()]
+        rows = self._rows()
         os.unlink(self.tmp.name)
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
-        if not sm:
+        inside = rows
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [x for x in rows if x[0] is not None and t0 <= x[0] <= t1]
+            if not inside:  # a window shorter than the sampling period: the first sample after it began
+                after = [x for x in rows if x[0] is not None and x[0] >= t0]
+                inside = after[:1]
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(sm)}
+        sm = [float(r[2]) for _, r in inside]
+        mx = [float(r[3]) for _, r in inside if r[3].replace(".", "").isdigit()]
+        reasons = sorted({self.REASONS[i] for _, r in inside for i in range(4) if r[6 + i] == "Active"})
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(sm), "period_ms": 50}
+        if self.window is not None:
+            out["window_ms"] = round(1000 * (self.window[1] - self.window[0]), 1)
+        return out
 
 
 def workload_cfg(name, tokens=0):
@@ -333,14 +369,15 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     barrier()
+    sampler.mark(t_host0, time.time())
     clocks = sampler.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     value = job_tokens_per_s(cfg.T, world, ms)

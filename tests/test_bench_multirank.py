@@ -45,3 +45,37 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.job_tokens_per_s(100, 1, 10.0) == pytest.approx(10000.0)
+
+
+def test_clock_samples_outside_the_timed_window_are_ignored():
+    """The clock record keeps only nvidia-smi samples taken inside the timed
+    window (host wall clock), and falls back to the first sample after the
+    window began when the window is shorter than the sampling period."""
+    import datetime
+    import bench
+
+    def line(t, mhz, cap="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {mhz}, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, {cap}\n"
+
+    t0 = 1_800_000_000.0
+    s = bench.ClockSampler(0)
+    with open(s.tmp.name, "w") as f:
+        f.write(line(t0 - 0.2, 345))                    # idle, before the window
+        f.write(line(t0 + 0.05, 1950, cap="Active"))
+        f.write(line(t0 + 0.10, 1965))
+        f.write(line(t0 + 0.40, 400))                    # after the window
+    s.proc = type("P", (), {"terminate": lambda self: None, "wait": lambda self, timeout=None: 0})()
+    s.mark(t0, t0 + 0.2)
+    c = s.stop()
+    assert c["samples"] == 2 and c["sm_mhz"] == 1957.5 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+
+    s = bench.ClockSampler(0)
+    with open(s.tmp.name, "w") as f:
+        f.write(line(t0 - 0.2, 345))
+        f.write(line(t0 + 0.03, 1980))
+    s.proc = type("P", (), {"terminate": lambda self: None, "wait": lambda self, timeout=None: 0})()
+    s.mark(t0, t0 + 0.01)
+    c = s.stop()
+    assert c["samples"] == 1 and c["sm_mhz"] == 1980.0
