@@ -276,10 +276,11 @@ def test_megakernel_wait_timeout_is_reported_and_context_survives():
 
 TABLES = ("counts", "offsets", "dest", "row_token", "row_slot")
 # ragged T, one expert row per lane (E = 32), the wider rows (E = 100, 256),
-# and a single histogram block (T = 8)
+# a single histogram block (T = 8) and a single token (T = 1, one CTA)
 ROUTE_CFGS = [TINY, MID, SKEW, EK, MoEConfig("e100_T1234_d64_f64_E100_k5", 1234, 64, 64, 100, 5),
               MoEConfig("e256_T333_d64_f64_E256_k8_renorm", 333, 64, 64, 256, 8, renorm=1),
-              MoEConfig("t8_d64_f64_E4_k2", 8, 64, 64, 4, 2)]
+              MoEConfig("t8_d64_f64_E4_k2", 8, 64, 64, 4, 2),
+              MoEConfig("t1_d64_f64_E5_k3_S1", 1, 64, 64, 5, 3, S=1)]
 
 
 def _fwd_tables(cfg, g, fused, grid):
