@@ -149,6 +149,10 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
+        if self.window is not None:  # a window shorter than a period: let one sample after its start land
+            t_end = time.time() + 0.5
+            while time.time() < t_end and not any(ts is not None and ts >= self.window[0] for ts, _ in self._rows()):
+                time.sleep(0.02)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -296,19 +300,36 @@ def run_ours(args):
                dW1=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
                dW3=torch.empty(nexp, cfg.f, cfg.d, dtype=f32, device=dev),
                dW2=torch.empty(nexp, cfg.d, cfg.f, dtype=f32, device=dev))
-    def fwd_ms(use_mk, iters=5):
-        """Device time of the forward alone (kernel chain or MegaKernel)."""
+    def device_ms(fn, min_ms=20.0, max_iters=400):
+        """Device time per call of fn: 2 untimed calls, then enough timed calls
+        for at least min_ms of work (a short layer's 5 calls are launch noise)."""
         for _ in range(2):
-            moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
-                              ws, use_megakernel=use_mk)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(iters):
-            moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"], out["idx"], out["w"],
-                              ws, use_megakernel=use_mk)
-        b.record()
-        b.synchronize()
-        return a.elapsed_time(b) / iters
+            fn()
+        iters, ms = 5, 0.0
+        while True:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(iters):
+                fn()
+            b.record()
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            if ms >= min_ms or iters >= max_iters:
+                return ms / iters
+            iters = min(max_iters, max(iters + 1, int(iters * 1.2 * min_ms / max(ms, 1e-3))))
+
+    def fwd_ms(use_mk):
+        """Device time of the forward alone (kernel chain or MegaKernel)."""
+        return device_ms(lambda: moe.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["y"],
+                                                   out["idx"], out["w"], ws, use_megakernel=use_mk))
+
+    def best_of(time_one):
+        """Chain and MegaKernel timed alternately twice; the faster time of each."""
+        t = {"chain": [], "megakernel": []}
+        for _ in range(2):
+            t["chain"].append(time_one(0))
+            t["megakernel"].append(time_one(1))
+        return {k: min(v) for k, v in t.items()}
 
     # Set-up, untimed: the library's measured autotuner picks each grouped
     # GEMM's tile shape and L2 prefetch depth on this very layer.
@@ -320,29 +341,19 @@ def run_ours(args):
     pair_kinds = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
     moe.moe_set_gemm_pair_kinds(pair_kinds)
 
-    fwd_times = {"chain": fwd_ms(0), "megakernel": fwd_ms(1)}
+    fwd_times = best_of(fwd_ms)
     mk = args.megakernel
     if mk < 0:  # the faster forward of the two (same bits either way)
         mk = 1 if fwd_times["megakernel"] < fwd_times["chain"] else 0
 
-    def bwd_ms(use_mk, iters=5):
+    def bwd_ms(use_mk):
         """Device time of the backward alone (kernel chain or MegaKernel input part)."""
         which = 3 | (moe.MOE_BWD_MEGAKERNEL if use_mk else 0)
+        return device_ms(lambda: moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"],
+                                                   out["idx"], out["w"], ws, out["dx"], out["dz"], out["dW1"],
+                                                   out["dW3"], out["dW2"], which=which))
 
-        def one():
-            moe.moe_layer_bwd(cfg, g["dy"], g["logits"], g["x"], g["W1"], g["W3"], g["W2"], out["idx"], out["w"],
-                              ws, out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], which=which)
-        for _ in range(2):
-            one()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(iters):
-            one()
-        b.record()
-        b.synchronize()
-        return a.elapsed_time(b) / iters
-
-    bwd_times = {"chain": bwd_ms(0), "megakernel": bwd_ms(1)}
+    bwd_times = best_of(bwd_ms)
     bmk = args.bwd_megakernel
     if bmk < 0:
         bmk = 1 if bwd_times["megakernel"] < bwd_times["chain"] else 0

@@ -20,6 +20,11 @@ constexpr int kTraceOf[kKinds] = {MOE_K_GEMM1,  MOE_K_GEMM2,     MOE_K_GEMM_DH,
                                   MOE_K_GEMM_DX, MOE_K_GEMM_DW13, MOE_K_GEMM_DW2};
 constexpr int kDepths[] = {0, 4, 8};
 constexpr int kNumDepths = sizeof(kDepths) / sizeof(kDepths[0]);
+// A candidate replaces the one kept so far only if it is faster by more than
+// this fraction (about the run-to-run spread of a kernel's time), so near
+// ties keep the first candidate timed: CTA pairs without prefetch, the
+// default.
+constexpr double kMargin = 0.01;
 
 }  // namespace
 
@@ -59,7 +64,8 @@ extern "C" int moe_autotune(const moe_cfg* cfg, const float* logits, const uint1
 
   double best[kKinds];
   for (int k = 0; k < kKinds; ++k) best[k] = -1.0;
-  for (int pair = 0; pair < 2; ++pair) {
+  for (int pi = 0; pi < 2; ++pi) {
+    const int pair = 1 - pi;  // CTA pairs first
     for (int di = 0; di < kNumDepths; ++di) {
       set_gemm_pair_kinds(pair ? (1 << kKinds) - 1 : 0);
       for (int k = 0; k < kKinds; ++k) set_gemm_prefetch(static_cast<GemmKind>(k), kDepths[di]);
@@ -83,7 +89,7 @@ extern "C" int moe_autotune(const moe_cfg* cfg, const float* logits, const uint1
         moe_trace_read(kTraceOf[k], &ms, &n);
         if (n <= 0) continue;
         const double us = 1000.0 * ms / n;
-        if (best[k] < 0 || us < best[k]) {
+        if (best[k] < 0 || us < best[k] * (1.0 - kMargin)) {
           best[k] = us;
           out->pair[k] = pair;
           out->prefetch_kb[k] = kDepths[di];

@@ -311,7 +311,10 @@ int moe_set_gemm_prefetch(int kind, int kblocks);
  * the caller's own layer (forward + backward, kernel chain) under each
  * candidate (one CTA per tile or CTA pairs; next-tile L2 prefetch depth 0, 4
  * or 8 K blocks), keeps the fastest per kind, applies it process-wide through
- * moe_set_gemm_pair_kinds / moe_set_gemm_prefetch, and reports it.
+ * moe_set_gemm_pair_kinds / moe_set_gemm_prefetch, and reports it.  CTA
+ * pairs without prefetch are timed first, and a later candidate replaces the
+ * one kept only if it is more than 1% faster, so near ties (within run-to-run
+ * spread) do not flip the choice.
  *
  * Arguments are those of moe_layer_fwd and moe_layer_bwd (all device memory
  * owned by the caller, layouts as there); every output and `ws` are
