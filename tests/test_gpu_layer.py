@@ -19,7 +19,11 @@ MID = MoEConfig("mid_T700_d256_f320_E6_k2_S1", 700, 256, 320, 6, 2, S=1)
 SKEW = MoEConfig("skew_T2048_d128_f192_E32_k4_zipf", 2048, 128, 192, 32, 4, zipf=True)
 EK = MoEConfig("ek_T200_d128_f128_E4_k4_renorm", 200, 128, 128, 4, 4, renorm=1)
 WIDE = MoEConfig("wide_T1500_d512_f704_E8_k2_S2", 1500, 512, 704, 8, 2, S=2)
-LAYER_CFGS = [TINY, MID, SKEW, EK, WIDE]
+# the most rows a token sums: k = 8 routed slots and S = 4 shared experts
+MAXROWS = MoEConfig("maxrows_T300_d128_f192_E16_k8_S4", 300, 128, 192, 16, 8, S=4)
+# the most segments a grouped GEMM walks: E = 256 routed experts (many empty) + 4 shared
+MAXSEG = MoEConfig("maxseg_T400_d64_f64_E256_k8_S4", 400, 64, 64, 256, 8, S=4)
+LAYER_CFGS = [TINY, MID, SKEW, EK, WIDE, MAXROWS, MAXSEG]
 
 
 def _check_layer(cfg, out, inp):
