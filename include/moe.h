@@ -69,7 +69,10 @@ enum {
  * the activations the backward needs (Xp, [a|b], H, O'), the backward's
  * intermediates, scratch counters and the device error word.  The caller
  * allocates it once; moe_layer_fwd fills it and moe_layer_bwd reads it, so
- * it must stay alive and unmodified between the two. */
+ * it must stay alive and unmodified between the two.  Calls that share a
+ * workspace must not run concurrently on the GPU (e.g. on two streams with
+ * no ordering between them): they share its scratch, its scheduling
+ * counters and its error word.  Different workspaces are independent. */
 size_t moe_workspace_bytes(const moe_cfg* cfg);
 
 /* Clears the device error word in `ws` (async on `stream`).  Call once after
