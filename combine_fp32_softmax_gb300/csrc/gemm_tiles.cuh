@@ -391,7 +391,15 @@ struct EpiState {
   uint32_t auxn = 0;      // dH input chunks loaded so far (buffer = auxn & 1)
   uint32_t auxpar = 0;    // next wait parity of each dH input buffer
   uint32_t auxpend = 0;   // dH input buffers with a load in flight
+  float w = 1.f;          // GEMM 2, dH: this lane's row's routing weight, read before the accumulator is ready
 };
+
+// The routing weight of the lane's row (1 for shared rows and rows past the
+// segment), read while the tile's main loop still runs.
+__device__ __forceinline__ float row_weight(const GemmParams& p, const TileInfo& t, int q) {
+  const int r = 32 * q + (threadIdx.x & 31);
+  return (r < t.rows && !t.shared) ? p.topk_w[p.row_slot[static_cast<size_t>(t.grow0) + r]] : 1.f;
+}
 
 // Staging helper: lane 0 waits until earlier chunks stopped reading the
 // buffer about to be rewritten.
@@ -426,8 +434,7 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
     const size_t grow = static_cast<size_t>(t.grow0) + r;
     orow0 = t.grow0 + 32 * q;
     optr = static_cast<float*>(p.out0) + grow * N;
-    if constexpr (KIND == kG2)
-      if (rowok && !t.shared) scale = p.topk_w[p.row_slot[grow]];
+    if constexpr (KIND == kG2) scale = es.w;
   } else if constexpr (KIND == kDW13) {
     N = p.d;
     const int mw0 = t.m0 + 32 * q;  // the warp's 32 rows all sit in dW1 or all in dW3 (f % 32 == 0)
@@ -583,8 +590,7 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
   const bool rowok = r < t.rows, full = t.rows >= 32 * q + 32;
   const size_t grow = static_cast<size_t>(t.grow0) + r;
   const int orow0 = t.grow0 + 32 * q;
-  float w = 1.f;
-  if (rowok && !t.shared) w = p.topk_w[p.row_slot[grow]];
+  const float w = es.w;
   uint16_t* dAB = static_cast<uint16_t*>(p.out0);
   uint16_t* Hw = static_cast<uint16_t*>(p.out1);
   const int nch = dh_chunks(p, t);
@@ -898,6 +904,8 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   ++es.it;
   if constexpr (KIND == kDH)
     if (t.active) dh_prefetch(p, t, q, stg, ss, es);
+  if constexpr (KIND == kG2 || KIND == kDH)
+    if (t.active) es.w = row_weight(p, t, q);
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
   tc_fence_after();
   const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
