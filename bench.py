@@ -54,6 +54,8 @@ def parse_args():
                     help="run the backward's weight-gradient GEMMs on the caller's stream (no B/W overlap)")
     ap.add_argument("--no-route-fusion", action="store_true",
                     help="run the router, scan and scatter as three kernels instead of one cooperative launch")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's kernels from the host instead of replaying one captured CUDA graph")
     ap.add_argument("--no-autotune", action="store_true",
                     help="skip the library's measured GEMM autotuner (run during set-up, untimed)")
     return ap.parse_args()
@@ -377,6 +379,20 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device error {code} ({info}) during warm-up")
 
+    # The timed steps replay the step as one CUDA graph (the library's
+    # launches, including the cooperative routing launch, the CTA-pair
+    # launches and the fork/join of the weight-gradient stream, captured once):
+    # the same kernels on the same buffers, without a host launch per kernel.
+    run_step = step
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step()
+        run_step = graph.replay
+        for _ in range(2):
+            run_step()
+        barrier()
+
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
     sampler.start()
@@ -385,7 +401,7 @@ def run_ours(args):
     t_host0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     e1.record(stream)
     barrier()
     sampler.mark(t_host0, time.time())
@@ -515,7 +531,7 @@ def run_ours(args):
             "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "bwd_ms": bwd_times,
             "bwd_megakernel": bmk, "kernels": kernels,
             "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap,
-                       "route_fusion": not args.no_route_fusion},
+                       "route_fusion": not args.no_route_fusion, "cuda_graph": not args.no_graph},
             "kernel_timing": "per-launch CUDA events on the launching stream over --steps further steps run with "
                              "the backward's B/W overlap off (the timed steps run with it on)"}
     if world == 1 and not args.no_cpu_baseline:

@@ -88,6 +88,33 @@ def test_results_do_not_depend_on_grid_size():
     assert len(digests) == 1
 
 
+def test_cuda_graph_replay_gives_the_same_bits():
+    """The layer's forward and backward captured in one CUDA graph (the
+    cooperative routing launch, CTA-pair launches, the fork/join of the
+    weight-gradient stream) and replayed several times give the bits of the
+    plain calls, with the scheduling counters back at 0 after each replay."""
+    cfg = MID
+    g = to_dev(make_layer_inputs(cfg, seed=24))
+    ref, _ = run_layer(cfg, g)
+    ws = moe.alloc_workspace(cfg, DEV)
+    out = empty_outputs(cfg)
+    run_layer(cfg, g, ws=ws, out=out)  # first launches outside the capture (attributes, tensor maps)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        run_layer(cfg, g, ws=ws, out=out)
+    for _ in range(3):
+        for t in out.values():
+            if t.dtype.is_floating_point:
+                t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert device_error(ws) == (0, 0)
+        assert _sched_words_clear(ws, cfg)
+        for k in ref:
+            assert torch.equal(out[k], ref[k]), k
+
+
 def test_weight_gradient_tickets_reset_between_launches():
     """Many back-to-back weight-gradient launches (the W part alone, on the B
     part's dA|dB and Hw kept in the workspace; both tile shapes) keep giving
