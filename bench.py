@@ -384,14 +384,26 @@ def run_ours(args):
     # launches and the fork/join of the weight-gradient stream, captured once):
     # the same kernels on the same buffers, without a host launch per kernel.
     run_step = step
+    graph_state = "off (--no-graph)" if args.no_graph else "replayed"
     if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            step()
-        run_step = graph.replay
-        for _ in range(2):
-            run_step()
-        barrier()
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+                step()
+            run_step = graph.replay
+            for _ in range(2):
+                run_step()
+            barrier()
+        except Exception as exc:  # a capture the driver refuses: measure with host launches instead
+            graph_state = f"capture failed, host launches: {str(exc).splitlines()[0][:120]}"
+            run_step = step
+            torch.cuda.synchronize()
+            for _ in range(2):
+                step()
+            barrier()
+        code, info = moe.moe_get_device_error(ws)
+        if code != 0:
+            raise RuntimeError(f"device error {code} ({info}) after the graph capture")
 
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
@@ -531,7 +543,7 @@ def run_ours(args):
             "gemm_tflops_all": all_gemm_tflops, "fwd_ms": fwd_times, "bwd_ms": bwd_times,
             "bwd_megakernel": bmk, "kernels": kernels,
             "tuning": {"gemm_pair_kinds": pair_kinds, "autotune": tuning, "bwd_overlap": overlap,
-                       "route_fusion": not args.no_route_fusion, "cuda_graph": not args.no_graph},
+                       "route_fusion": not args.no_route_fusion, "cuda_graph": graph_state},
             "kernel_timing": "per-launch CUDA events on the launching stream over --steps further steps run with "
                              "the backward's B/W overlap off (the timed steps run with it on)"}
     if world == 1 and not args.no_cpu_baseline:
