@@ -33,6 +33,14 @@
  *  - Results are bitwise deterministic: no call accumulates floating-point
  *    values with atomics, and every reduction runs in a fixed order.
  *  - Every output is fully overwritten (no accumulate-into mode).
+ *  - The layer calls can be captured in a CUDA graph and replayed (stream
+ *    capture of the caller's stream, relaxed or thread-local mode): every
+ *    launch is capturable, including the cooperative routing launch, the
+ *    CTA-pair cluster launches and the fork/join of the backward's second
+ *    stream, and the scheduling counters in `ws` reset themselves on the
+ *    device.  The first call with a configuration should run uncaptured
+ *    (it sets kernel attributes and caches occupancy); moe_autotune and the
+ *    moe_trace_* timing calls synchronise and must stay outside a capture.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
