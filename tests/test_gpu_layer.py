@@ -23,7 +23,9 @@ WIDE = MoEConfig("wide_T1500_d512_f704_E8_k2_S2", 1500, 512, 704, 8, 2, S=2)
 MAXROWS = MoEConfig("maxrows_T300_d128_f192_E16_k8_S4", 300, 128, 192, 16, 8, S=4)
 # the most segments a grouped GEMM walks: E = 256 routed experts (many empty) + 4 shared
 MAXSEG = MoEConfig("maxseg_T400_d64_f64_E256_k8_S4", 400, 64, 64, 256, 8, S=4)
-LAYER_CFGS = [TINY, MID, SKEW, EK, WIDE, MAXROWS, MAXSEG]
+# the degenerate router: one expert, k = 1 (every token to expert 0, weight 1)
+ONE = MoEConfig("one_T100_d64_f64_E1_k1", 100, 64, 64, 1, 1)
+LAYER_CFGS = [TINY, MID, SKEW, EK, WIDE, MAXROWS, MAXSEG, ONE]
 
 
 def _check_layer(cfg, out, inp):
