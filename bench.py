@@ -198,24 +198,43 @@ def gemm_flops_per_launch(cfg):
             "gemm_dw13": 2 * dfr, "gemm_dw2": dfr}
 
 
+def memory_bytes_per_launch(cfg):
+    """Algorithmic DRAM bytes of one launch of each memory-bound kernel
+    (what the method must read and write once; index reads included)."""
+    T, d, E, k, R, Rs = cfg.T, cfg.d, cfg.E, cfg.k, cfg.R, cfg.Rs
+    nt = -(-cfg.f // 256)
+    rows_copy = T * d * 2 + R * d * 2 + R * 4           # each x (dy) row read once, written to its k rows
+    rows_sum = Rs * d * 4 + T * d * 4 + R * 4           # fp32 rows read once, one fp32 row per token written
+    return {"gather": rows_copy, "combine_bwd": rows_copy, "combine": rows_sum, "dispatch_bwd": rows_sum,
+            "route_tables": T * E * 4 + T * k * 8 + R * 12,  # logits in; top-k out; dest, row_token, row_slot
+            "route_bwd": T * E * 8 + T * k * 12,             # logits in, dlogits out; idx, w, dw in
+            "dw_reduce": R * nt * 4 + R * 4 + T * k * 4}
+
+
 def traffic_from_profiles(kernel, workload, cta_group=None):
-    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, or None.
-    A line `traffic_bytes_per_launch[cta_group=N]: B` is specific to one tile
-    shape of a grouped GEMM (N = 1 or 2 CTAs per tile) and is preferred when
-    that shape ran; `traffic_bytes_per_launch: B` holds for any."""
+    """Per-launch DRAM bytes recorded from an ncu capture in profiles/, as
+    (bytes or None, note).  A line `traffic_bytes_per_launch[cta_group=N]: B`
+    is specific to one tile shape of a grouped GEMM and is preferred when that
+    shape ran; `traffic_bytes_per_launch: B` holds for any.  The capture names
+    the kernel build it measured (`source_sha256:`); bytes of another build
+    are not reported."""
+    from combine_fp32_softmax_gb300.build import source_digest
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
-        return None
-    keys = ([f"traffic_bytes_per_launch[cta_group={cta_group}]:"] if cta_group else []) + ["traffic_bytes_per_launch:"]
+        return None, "no ncu capture of this kernel and workload in profiles/"
     lines = [ln.strip() for ln in open(path)]
+    built = [ln.split(":", 1)[1].strip() for ln in lines if ln.startswith("source_sha256:")]
+    if not built or built[0] != source_digest():
+        return None, f"ncu capture in profiles/ is of another build of the kernels ({built[0] if built else '?'})"
+    keys = ([f"traffic_bytes_per_launch[cta_group={cta_group}]:"] if cta_group else []) + ["traffic_bytes_per_launch:"]
     for key in keys:
         for line in lines:
             if line.startswith(key):
                 try:
-                    return float(line.split(":", 1)[1].strip().split()[0])
+                    return float(line.split(":", 1)[1].strip().split()[0]), f"ncu capture {os.path.relpath(path, ROOT)}"
                 except ValueError:
-                    return None
-    return None
+                    return None, "unreadable traffic line"
+    return None, "no traffic line for this tile shape"
 
 
 # ------------------------------------------------------------ oracle timing
@@ -433,9 +452,11 @@ def run_ours(args):
     overlap = moe.moe_set_bwd_overlap(False)
     moe.moe_trace_reset()
     moe.moe_trace_enable(True)
+    t_trace = time.time()
     for _ in range(args.steps):
         step()
     barrier()
+    trace_wall_s = time.time() - t_trace
     moe.moe_trace_enable(False)
     trace = moe.moe_trace_read()
     moe.moe_set_bwd_overlap(overlap)
@@ -515,29 +536,52 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    # ---- roofline of the dominant kernel (largest share of device time)
+    # ---- roofline of every kernel, and of the dominant one (largest share of
+    # device time).  GEMMs against the measured bf16 peak, memory-bound kernels
+    # against the measured copy rate.  The kernels were timed one launch at a
+    # time over a pass well under a second: the burst figure applies, unless
+    # the pass was long or the clocks inside the timed window showed the power
+    # cap, when the sustained figure does.
     peaks, peak_src = load_peaks()
     flops = gemm_flops_per_launch(cfg)
+    mem = memory_bytes_per_launch(cfg)
+    capped = bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
+    sustained = trace_wall_s >= 1.0 or capped
+    bf16_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops",
+                          FALLBACK_PEAKS["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    peak_kind = (f"bf16 {'sustained' if sustained else 'burst'} ({peak_src}; per-kernel pass "
+                 f"{trace_wall_s:.2f} s, power cap {'seen' if capped else 'not seen'} in the timed window)")
     total_ms = sum(v[0] for v in trace.values())
+    per_kernel = {}
+    for name, (tot, n) in trace.items():
+        ms_launch = tot / n
+        if name in flops:
+            a = flops[name] / (ms_launch / 1000.0) / 1e12
+            per_kernel[name] = {"bound": "tensor", "achieved": a, "peak": bf16_peak, "unit": "TFLOP/s",
+                                "frac": a / bf16_peak, "us": 1000 * ms_launch, "work": flops[name]}
+        elif name in mem:
+            a = mem[name] / (ms_launch / 1000.0) / 1e9
+            per_kernel[name] = {"bound": "hbm", "achieved": a, "peak": hbm_peak, "unit": "GB/s",
+                                "frac": a / hbm_peak, "us": 1000 * ms_launch, "work": mem[name]}
     dom = max(trace, key=lambda k: trace[k][0])
-    dom_ms = trace[dom][0] / trace[dom][1]
-    if dom in flops:
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-        achieved = flops[dom] / (dom_ms / 1000.0) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"bf16 sustained, {peak_src}"}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
-                "frac": None, "peak_source": peak_src}
+    roof = dict(per_kernel.get(dom, {"bound": "hbm", "achieved": None, "peak": hbm_peak, "unit": "GB/s",
+                                     "frac": None}))
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_kind if roof["bound"] == "tensor" else f"HBM copy, {peak_src}"
     gemm_kind = {"gemm1_swiglu": 0, "gemm2_scale": 1, "gemm_dh": 2, "gemm_dx": 3, "gemm_dw13": 4, "gemm_dw2": 5}
     cta_group = 1 + ((pair_kinds >> gemm_kind[dom]) & 1) if dom in gemm_kind else None
-    roof["traffic"] = traffic_from_profiles(dom, cfg.name, cta_group)
+    roof["traffic"], roof["traffic_source"] = traffic_from_profiles(dom, cfg.name, cta_group)
     if cta_group:
         roof["cta_group"] = cta_group
     roof["share"] = trace[dom][0] / total_ms
+    roof["per_kernel"] = {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()
+                              if kk in ("achieved", "frac", "unit", "us")} for k, v in per_kernel.items()}
     kernels = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1], "share": v[0] / total_ms} for k, v in trace.items()}
     gemm_ms = sum(trace[k][0] for k in flops if k in trace) / args.steps
     all_gemm_tflops = sum(flops.values()) / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None
+    roof["all_gemms"] = {"achieved": all_gemm_tflops, "frac": all_gemm_tflops / bf16_peak if all_gemm_tflops else None,
+                         "unit": "TFLOP/s"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_median,

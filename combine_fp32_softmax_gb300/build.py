@@ -30,6 +30,20 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+def source_digest() -> str:
+    """First 16 hex digits of a SHA-256 over the library's CUDA/C++ sources
+    and its public header: names a build of the kernels, so a profile taken
+    of one build is not read as a measurement of another."""
+    import hashlib
+    h = hashlib.sha256()
+    names = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        h.update(f.encode())
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    h.update(open(os.path.join(HERE, "..", "include", "moe.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def build(verbose: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()

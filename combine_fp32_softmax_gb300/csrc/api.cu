@@ -249,6 +249,16 @@ int moe_token_addresses(const moe_cfg* cfg, const int32_t* topk_idx, const int32
   return MOE_OK;
 }
 
+int moe_rank_bases(const int32_t* all_counts, int G, int E, const int32_t* owner, int rank, int32_t* rank_base,
+                   int32_t* recv_rows, void* stream) {
+  if (G < 1 || G > 65536 || E < 1 || E > 256 || rank < 0 || rank >= G) return MOE_ERR_SHAPE;
+  if (!all_counts || !owner || !rank_base) return MOE_ERR_ARG;
+  if (!al16(all_counts) || !al16(owner) || !al16(rank_base) || (recv_rows && !al16(recv_rows))) return MOE_ERR_ALIGN;
+  MOE_TRY_CUDA(launch_rank_bases(all_counts, G, E, owner, rank, rank_base, recv_rows,
+                                 static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x, const int32_t* offsets,
                           const int32_t* row_slot, const float* topk_w, const uint16_t* W1, const uint16_t* W3,
                           const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime, void* ws, void* stream) {

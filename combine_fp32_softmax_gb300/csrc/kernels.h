@@ -27,6 +27,10 @@ cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, 
 // base[e*nb + b] += rank_base[e] - offsets[e] (multi-rank token mapping).
 cudaError_t launch_rebase(int32_t* base, const int32_t* offsets, const int32_t* rank_base, int E, int nb,
                           cudaStream_t s);
+// rank_base[e] (and recv_rows[o], if non-null) of the multi-rank token
+// mapping from the all-gathered counts [G][E] and the expert owners [E].
+cudaError_t launch_rank_bases(const int32_t* counts, int G, int E, const int32_t* owner, int rank,
+                              int32_t* rank_base, int32_t* recv_rows, cudaStream_t s);
 // dst[r] = src[idx[r]] for r < nrows, rows of `d` bf16 (zero row if the
 // index is outside [0, nsrc)).
 cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
@@ -43,5 +47,8 @@ cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, i
 cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const float* topk_w, const float* dw,
                              int T, int E, int k, int renorm, float* dlogits, cudaStream_t s);
 int num_sms();
+// Makes sure the modules of moe_dispatch's kernels (histogram, scan, scatter,
+// row gather) are loaded on the current device.
+cudaError_t preload_dispatch_kernels();
 
 }  // namespace moe

@@ -10,6 +10,9 @@
 // fixed-size array compiled into the library's device image.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,8 +29,31 @@ static __device__ __align__(256) int g_dispatch_scratch[kScratchInts];
 // Device address of g_dispatch_scratch per device, looked up on the first
 // call made with that device current (host code cannot use the symbol's name
 // as a device pointer: on the host it names a stand-in, not device memory).
+// The set-up runs under a lock, once per device; later calls only load the
+// published address.  The address belongs to the CUDA context current at
+// set-up: after a device reset the process must restart before calling this
+// entry point again on that device.
 constexpr int kMaxDevices = 64;
-int* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<int*> g_scratch_addr[kMaxDevices];
+std::mutex g_setup_mu;
+
+// First call on the current device: loads the modules of this file and of
+// the dispatch kernels (under lazy module loading that is when the scratch
+// array is placed in device memory), then looks up the array's address.
+int* scratch_on_current_device(int dev) {
+  int* addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr) return addr;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  addr = g_scratch_addr[dev].load(std::memory_order_relaxed);
+  if (addr) return addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return nullptr;
+  if (moe::preload_dispatch_kernels() != cudaSuccess) return nullptr;
+  (void)moe::num_sms();
+  addr = static_cast<int*>(p);
+  g_scratch_addr[dev].store(addr, std::memory_order_release);
+  return addr;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -52,12 +78,8 @@ extern "C" int moe_dispatch_noalloc(const moe_cfg* cfg, const int32_t* topk_idx,
   if (kErrInts + 2 * table > kScratchInts) return MOE_ERR_SHAPE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_dispatch_scratch) != cudaSuccess) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int*>(addr);
-  }
-  int* err = g_scratch_addr[dev];
+  int* err = scratch_on_current_device(dev);
+  if (!err) return MOE_ERR_CUDA;
   int32_t* hist = err + kErrInts;
   int32_t* base = hist + table;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -522,6 +522,44 @@ __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 2 : 1)
   }
 }
 
+// Cross-rank bases of the multi-rank token mapping (one block of 256
+// threads, thread e = expert e).  counts is the all-gathered [G][E] table of
+// every rank's per-expert slot counts.  Expert e's segment starts, inside
+// its owner's receive buffer, after the segments of the lower experts with
+// the same owner; within it rank r's slots follow those of ranks < r.  All
+// sums run in a fixed (ascending) order.
+__global__ void __launch_bounds__(256)
+    rank_bases_kernel(const int32_t* __restrict__ counts, int G, int E, const int32_t* __restrict__ owner, int rank,
+                      int32_t* __restrict__ rank_base, int32_t* __restrict__ recv_rows) {
+  __shared__ int s_total[256], s_owner[256];
+  const int e = threadIdx.x;
+  int lower = 0;
+  if (e < E) {
+    int total = 0;
+    for (int g = 0; g < G; ++g) {
+      const int c = counts[static_cast<size_t>(g) * E + e];
+      if (g < rank) lower += c;
+      total += c;
+    }
+    s_total[e] = total;
+    s_owner[e] = min(max(owner[e], 0), G - 1);
+  }
+  __syncthreads();
+  if (e < E) {
+    int start = 0;
+    for (int u = 0; u < e; ++u)
+      if (s_owner[u] == s_owner[e]) start += s_total[u];
+    rank_base[e] = start + lower;
+  }
+  if (recv_rows)
+    for (int o = threadIdx.x; o < G; o += blockDim.x) {
+      int rows = 0;
+      for (int u = 0; u < E; ++u)
+        if (s_owner[u] == o) rows += s_total[u];
+      recv_rows[o] = rows;
+    }
+}
+
 // Moves every block base of expert e from the local segment start
 // offsets[e] to the rank's global base rank_base[e] (multi-rank mapping).
 __global__ void rebase_kernel(int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
@@ -830,6 +868,13 @@ cudaError_t launch_rebase(int32_t* base, const int32_t* offsets, const int32_t* 
   return cudaGetLastError();
 }
 
+cudaError_t launch_rank_bases(const int32_t* counts, int G, int E, const int32_t* owner, int rank,
+                              int32_t* rank_base, int32_t* recv_rows, cudaStream_t s) {
+  TraceScope trace_scope(MOE_K_SCAN, s);
+  rank_bases_kernel<<<1, 256, 0, s>>>(counts, G, E, owner, rank, rank_base, recv_rows);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
                                     uint16_t* dst, int trace_kind, cudaStream_t s) {
   if (nrows <= 0) return cudaSuccess;
@@ -930,6 +975,19 @@ cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const
   else
     route_bwd_kernel<8><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
   return cudaGetLastError();
+}
+
+// Loads the modules of the kernels moe_dispatch runs (histogram, scan,
+// scatter, row gather) if the runtime has not loaded them yet: under lazy
+// module loading a kernel's module is loaded, and its device memory set up,
+// on first use, and asking for a kernel's attributes is such a use.
+cudaError_t preload_dispatch_kernels() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, hist_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, scan_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, scatter_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gather_rows_bf16_kernel);
+  return e;
 }
 
 }  // namespace moe

@@ -26,28 +26,22 @@ def owner_of(E: int, G: int):
     return [min(e // per, G - 1) for e in range(E)]
 
 
-def rank_bases(all_counts: torch.Tensor, rank: int, owners) -> torch.Tensor:
-    """all_counts [G, E] int64 -> [E] base address (inside the owner's
-    receive buffer) of rank `rank`'s first slot for every expert."""
+def rank_bases(all_counts: torch.Tensor, rank: int, owners):
+    """all_counts [G, E] (CUDA tensor, the all-gathered counts) -> ([E] base
+    address inside the owner's receive buffer of rank `rank`'s first slot
+    for every expert, [G] rows each owner receives), both int32 on the same
+    device, computed by the library (moe_rank_bases)."""
+    from . import moe
+    if not all_counts.is_cuda:
+        raise ValueError("all_counts must be a CUDA tensor: the library computes the bases on the device")
     G, E = all_counts.shape
-    per_expert = all_counts.sum(dim=0)
-    seg_start = torch.zeros(E, dtype=torch.int64)
-    run = {}
-    for e in range(E):
-        o = owners[e]
-        seg_start[e] = run.get(o, 0)
-        run[o] = run.get(o, 0) + int(per_expert[e])
-    lower = all_counts[:rank].sum(dim=0) if rank > 0 else torch.zeros(E, dtype=torch.int64)
-    return seg_start + lower
-
-
-def receive_sizes(all_counts: torch.Tensor, owners, G: int):
-    """Rows each owner receives (the size of its expert buffer)."""
-    per_expert = all_counts.sum(dim=0)
-    sizes = [0] * G
-    for e, o in enumerate(owners):
-        sizes[o] += int(per_expert[e])
-    return sizes
+    dev = all_counts.device
+    counts = all_counts.to(torch.int32).contiguous()
+    owner = torch.tensor(list(owners), dtype=torch.int32, device=dev)
+    base = torch.empty(E, dtype=torch.int32, device=dev)
+    rows = torch.empty(G, dtype=torch.int32, device=dev)
+    moe.moe_rank_bases(counts, owner, rank, base, rows)
+    return base, rows
 
 
 def all_gather_counts(local_counts: torch.Tensor) -> torch.Tensor:

@@ -50,6 +50,7 @@ _SIGS = {
     "moe_route": ([_CFG, _P, _P, _P, _P, _P], _I),
     "moe_dispatch": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_token_addresses": ([_CFG] + [_P] * 7, _I),
+    "moe_rank_bases": ([_P, _I, _I, _P, _I, _P, _P, _P], _I),
     "moe_dispatch_noalloc": ([_CFG] + [_P] * 9, _I),
     "moe_group_gemm_swiglu": ([_CFG] + [_P] * 13, _I),
     "moe_combine": ([_CFG, _P, _P, _P, _P, _P], _I),
@@ -152,6 +153,13 @@ def moe_dispatch_noalloc(cfg, topk_idx, x, counts, offsets, dest, row_token, row
 def moe_token_addresses(cfg, topk_idx, rank_base, counts, offsets, dest, ws, stream=None):
     _call("moe_token_addresses", _cfg(cfg), _ptr(topk_idx), _ptr(rank_base), _ptr(counts), _ptr(offsets),
           _ptr(dest), _ptr(ws), _stream(stream))
+
+
+def moe_rank_bases(all_counts, owner, rank, rank_base, recv_rows=None, stream=None):
+    """all_counts [G, E] int32, owner [E] int32 -> rank_base [E] int32 (and recv_rows [G] int32)."""
+    G, E = all_counts.shape
+    _call("moe_rank_bases", _ptr(all_counts), int(G), int(E), _ptr(owner), int(rank), _ptr(rank_base),
+          _ptr(recv_rows), _stream(stream))
 
 
 def moe_group_gemm_swiglu(cfg, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, H, AB, Oprime, ws, stream=None):

@@ -119,17 +119,28 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
  * arguments minus ws; Xp gathered when x and Xp are both non-NULL), but
  * keeps its scratch (expert histogram, block bases, error word) in a 4 MiB
  * array inside the library, held by every GPU that loads it until exit.
- * It allocates nothing and calls no allocating routine.
+ * After its first call on a device (below) it allocates nothing and calls
+ * no allocating routine.
  *  - Limit: E * ceil(T / 32) <= 524,256 (e.g. 64 experts and 262,144
  *    tokens); larger shapes return MOE_ERR_SHAPE before any work.
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - The first call on a device sets up (with that device current): it
+ *    loads this library's dispatch kernels and the array if the CUDA
+ *    runtime has not loaded them yet (under lazy module loading that is
+ *    when the 4 MiB array is placed in device memory, an allocation made by
+ *    the driver) and looks up the array's device address.  Make that first
+ *    call before any stream capture and before any stretch of code in which
+ *    nothing may allocate; every later call on that device allocates
+ *    nothing.  The set-up is thread-safe; after a device reset the process
+ *    must restart before calling this again on that device.
  *  - Every call shares the one array, which keeps the last call's contents:
  *    two calls whose work can overlap on the GPU (e.g. issued on different
  *    streams with no ordering between them) race and produce wrong tables;
  *    order them on one stream or with events.
- *  - Out-of-range expert indices are clamped as in moe_dispatch; the error
- *    record stays inside the array (there is no workspace to read it from). */
+ *  - Out-of-range expert indices are clamped as in moe_dispatch (the tables
+ *    are the ones moe_dispatch gives for the same indices); the call still
+ *    returns MOE_OK, and the error record stays inside the array (there is
+ *    no workspace to read it from): validate indices beforehand, or use
+ *    moe_dispatch and moe_get_device_error, where that matters. */
 int moe_dispatch_noalloc(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
                          int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* row_token,
                          int32_t* row_slot, uint16_t* Xp, void* stream);
@@ -147,6 +158,24 @@ int moe_dispatch_noalloc(const moe_cfg* cfg, const int32_t* topk_idx, const uint
  * only. */
 int moe_token_addresses(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* rank_base,
                         int32_t* counts, int32_t* offsets, int32_t* dest, void* ws, void* stream);
+
+/* Cross-rank bases of the multi-rank token mapping (UniEP page, section 2.2,
+ * Algorithm 1: the per-expert counts of every rank are all-gathered, and
+ * each rank's slots to expert e are placed after those of the lower ranks).
+ * all_counts [G][E] int32: rank g's slots routed to expert e (each rank's
+ * moe_token_addresses counts, gathered in rank order).  owner [E] int32:
+ * the rank that holds expert e (values outside [0, G) are clamped); the
+ * experts of one owner are laid out in its receive buffer in index order.
+ * Writes rank_base [E] for rank `rank`:
+ *   rank_base[e] = sum of all ranks' counts of the experts u < e with
+ *                  owner[u] == owner[e]  +  sum over g < rank of counts[g][e]
+ * (the input moe_token_addresses takes), and, if recv_rows [G] is non-NULL,
+ * the rows each owner receives.  Device memory, one small launch on
+ * `stream`; every sum runs in ascending order, so the result is exact
+ * (int32: the total rows per owner must stay below 2^31).
+ * Limits: 1 <= E <= 256, 1 <= G <= 65536, 0 <= rank < G (MOE_ERR_SHAPE). */
+int moe_rank_bases(const int32_t* all_counts, int G, int E, const int32_t* owner, int rank,
+                   int32_t* rank_base, int32_t* recv_rows, void* stream);
 
 /* Expert FFN as two grouped GEMMs over the ragged expert segments
  * (UniEP page, section 1.1 "GroupGEMM -> SwiGLU -> GroupGEMM"; padding-free

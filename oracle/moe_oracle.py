@@ -21,7 +21,7 @@ Every value is computed in float64 from the exact bf16/fp32 input bits.  No
 intermediate is rounded.  Matrix products use numpy's matmul as a library
 step; there is no blocking or reordering beyond the definitions below.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   * softmax over all E experts, then top-k; the routing weight is the
     probability itself (renorm=0) or renormalised over the k picks (renorm=1);
   * top-k is chosen on the fp32 logits, larger first, ties to the lower expert

@@ -26,3 +26,27 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _gpu_guards_and_margins(request):
+    """GPU tests: the test id under which tolerance checks record their
+    errors, and afterwards the check that no kernel wrote outside a buffer
+    allocated by the test helpers."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    from tests import gpu_util
+    gpu_util.CURRENT_TEST["id"] = request.node.nodeid
+    yield
+    gpu_util.check_guards()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    out = os.environ.get("MOE_MARGINS_OUT")
+    mod = sys.modules.get("tests.gpu_util")
+    if not out or mod is None or not mod.MARGINS:
+        return
+    import json
+    with open(out, "w") as fh:
+        json.dump(mod.MARGINS, fh, indent=0)

@@ -4,7 +4,10 @@ global addresses they assign must (1) be unique and fill every owner's
 receive buffer exactly, and (2) equal the single-GPU mapping of the
 concatenated batch (rank 0's tokens first) re-expressed per owner.  The
 local stable ranks come from the oracle's permutation (test
-infrastructure)."""
+infrastructure), and so do the cross-rank bases: on CPU ranks there is no
+device for the library's moe_rank_bases, so the test restates its
+definition (the GPU test checks the library's bases against the same
+restatement)."""
 import os
 import socket
 
@@ -24,6 +27,24 @@ def _free_port():
     return p
 
 
+def bases_restated(all_counts, rank, owners):
+    """Algorithm 1's cross-rank base of every expert for `rank`: the rows of
+    the lower experts of the same owner, plus the lower ranks' slots to it."""
+    G, E = all_counts.shape
+    per_expert = all_counts.sum(dim=0).tolist()
+    start, run = [0] * E, {}
+    for e in range(E):
+        start[e] = run.get(owners[e], 0)
+        run[owners[e]] = start[e] + per_expert[e]
+    lower = all_counts[:rank].sum(dim=0).tolist() if rank > 0 else [0] * E
+    return torch.tensor([start[e] + lower[e] for e in range(E)], dtype=torch.int64)
+
+
+def receive_rows_restated(all_counts, owners, G):
+    per_expert = all_counts.sum(dim=0).tolist()
+    return [sum(per_expert[e] for e in range(len(owners)) if owners[e] == o) for o in range(G)]
+
+
 def _local_sel(rank, T, E, k, seed=0):
     g = torch.Generator().manual_seed(seed * 100 + rank)
     z = torch.randn(T, E, generator=g)
@@ -36,7 +57,7 @@ def _global_addresses(rank, G, T, E, k, all_counts):
     sel = _local_sel(rank, T, E, k)
     perm = O.permute(sel, E)  # local stable order: row r of expert e has local rank r - offsets[e]
     owners = ep.owner_of(E, G)
-    base = ep.rank_bases(all_counts, rank, owners)
+    base = bases_restated(all_counts, rank, owners)
     flat = sel.reshape(-1)
     local_rank = perm.dest - perm.offsets[flat]
     addr = base.numpy()[flat] + local_rank
@@ -71,7 +92,7 @@ def test_two_rank_mapping_matches_single_gpu_mapping(E, k):
         assert p.exitcode == 0
     all_counts = torch.tensor(res[0][3])
     owners = ep.owner_of(E, G)
-    sizes = ep.receive_sizes(all_counts, owners, G)
+    sizes = receive_rows_restated(all_counts, owners, G)
     # (1) every owner's buffer is filled exactly once
     for o in range(G):
         got = sorted(a for r in range(G) for ow, a in zip(res[r][1], res[r][2]) if ow == o)
@@ -91,6 +112,6 @@ def test_one_rank_reduces_to_offsets():
     E, T, k = 7, 40, 3
     sel = _local_sel(0, T, E, k)
     counts = torch.bincount(torch.from_numpy(sel.reshape(-1)), minlength=E)
-    base = ep.rank_bases(counts[None].to(torch.int64), 0, ep.owner_of(E, 1))
+    base = bases_restated(counts[None].to(torch.int64), 0, ep.owner_of(E, 1))
     from oracle import moe_oracle as O
     assert base.tolist() == O.permute(sel, E).offsets[:-1].tolist()

@@ -11,6 +11,7 @@ from combine_fp32_softmax_gb300 import ep, moe
 from combine_fp32_softmax_gb300.configs import MoEConfig
 from combine_fp32_softmax_gb300.inputs import make_logits
 from tests.gpu_util import DEV, device_error
+from tests.test_ep_mapping import bases_restated, receive_rows_restated
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +37,9 @@ def test_multi_rank_addresses_match_concatenated_batch(G, E, k):
     owners = ep.owner_of(E, G)
     got = []
     for r in range(G):
-        rb = ep.rank_bases(all_counts, r, owners).to(torch.int32).to(DEV)
+        rb, rows = ep.rank_bases(all_counts.to(DEV), r, owners)
+        assert rb.cpu().tolist() == bases_restated(all_counts, r, owners).tolist()
+        assert rows.cpu().tolist() == receive_rows_restated(all_counts, owners, G)
         c = torch.empty(E, dtype=torch.int32, device=DEV)
         off = torch.empty(E + 1, dtype=torch.int32, device=DEV)
         dest = torch.empty(T * k, dtype=torch.int32, device=DEV)

@@ -69,3 +69,45 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     t = {n: idx for n in NAMES}
     t["Xp"] = torch.zeros(1, dtype=torch.bfloat16, device=DEV)
     assert _noalloc(cfg, idx, t["Xp"], t) == moe.MOE_ERR_SHAPE
+
+
+def test_noalloc_calls_after_the_first_leave_device_memory_unchanged():
+    # the first call on the device may load the library's kernels and place
+    # the scratch array; after it, calls must not change the device's free
+    # memory (nothing allocated, nothing freed)
+    cfg = MoEConfig("na3", 4096, 256, 64, 64, 6)
+    idx, _ = _route(cfg, 3)
+    x = make_x(cfg, 3).to(DEV)
+    t = _tables(cfg)
+    assert _noalloc(cfg, idx, x, t) == moe.MOE_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        assert _noalloc(cfg, idx, x, t) == moe.MOE_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+
+
+def test_noalloc_clamps_out_of_range_indices_like_moe_dispatch():
+    # one index past the last expert and one below 0: both entry points clamp
+    # them into range and give the same tables; moe_dispatch reports the
+    # first bad slot in its workspace's error word
+    cfg = MoEConfig("na4", 500, 128, 64, 16, 2)
+    idx, _ = _route(cfg, 4)
+    flat = idx.view(-1)
+    flat[37] = cfg.E
+    flat[401] = -3
+    x = make_x(cfg, 4).to(DEV)
+    ws = moe.alloc_workspace(cfg, DEV)
+    want = _tables(cfg)
+    moe.moe_dispatch(cfg, idx, x, want["counts"], want["offsets"], want["dest"], want["row_token"],
+                     want["row_slot"], want["Xp"], ws)
+    code, info = moe.moe_get_device_error(ws)
+    assert code == moe.MOE_ERR_ARG and info in (37, 401), (code, info)
+    got = _tables(cfg)
+    assert _noalloc(cfg, idx, x, got) == moe.MOE_OK
+    torch.cuda.synchronize()
+    for n in NAMES:
+        assert torch.equal(got[n], want[n]), n
+    assert torch.equal(got["Xp"], want["Xp"])
