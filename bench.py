@@ -358,7 +358,10 @@ def run_ours(args):
     if not args.no_autotune:
         tuning = moe.moe_autotune(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], g["dy"], out["y"], out["idx"],
                                   out["w"], out["dx"], out["dz"], out["dW1"], out["dW3"], out["dW2"], ws)
-        tuning = {k: {"pair": v[0], "prefetch_kb": v[1], "us": round(v[2], 1)} for k, v in tuning.items()}
+        for v in tuning["kinds"].values():
+            v["us"] = round(v["us"], 1)
+        tuning["fwd_us"] = [round(v, 1) for v in tuning["fwd_us"]]
+        tuning["bwd_us"] = [round(v, 1) for v in tuning["bwd_us"]]
     pair_kinds = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
     moe.moe_set_gemm_pair_kinds(pair_kinds)
 
@@ -539,14 +542,14 @@ def run_ours(args):
     # ---- roofline of every kernel, and of the dominant one (largest share of
     # device time).  GEMMs against the measured bf16 peak, memory-bound kernels
     # against the measured copy rate.  The kernels were timed one launch at a
-    # time over a pass well under a second: the burst figure applies, unless
-    # the pass was long or the clocks inside the timed window showed the power
-    # cap, when the sustained figure does.
+    # time over a pass well under a second: the burst figure applies; only a
+    # pass of a second or more under the power cap is compared with the
+    # sustained figure.
     peaks, peak_src = load_peaks()
     flops = gemm_flops_per_launch(cfg)
     mem = memory_bytes_per_launch(cfg)
     capped = bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
-    sustained = trace_wall_s >= 1.0 or capped
+    sustained = trace_wall_s >= 1.0 and capped
     bf16_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops",
                           FALLBACK_PEAKS["bf16_tflops_sustained" if sustained else "bf16_tflops"])
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])

@@ -14,6 +14,11 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+# Debug build: the same sources with -DMOE_DEBUG (index, segment and TMA
+# coordinate checks that record MOE_ERR_ARG instead of touching memory
+# outside a buffer); used by the tests, never by the benchmark.
+DEBUG_OUT_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(DEBUG_OUT_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-diag-suppress", "1160"]
@@ -44,15 +49,17 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose: bool = False, debug: bool = False) -> str:
+    out_dir, lib_path = (DEBUG_OUT_DIR, DEBUG_LIB_PATH) if debug else (OUT_DIR, LIB_PATH)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = sources()
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    flags = FLAGS + (["-DMOE_DEBUG"] if debug else [])
 
     def compile_one(pair):
         src, obj = pair
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, r.returncode, r.stdout + r.stderr
 
@@ -64,13 +71,13 @@ def build(verbose: bool = False) -> str:
             sys.stderr.write(f"== {os.path.basename(s)} ==\n{log}\n")
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(s) for s, _ in failed))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -114,7 +114,7 @@ int build_tables(const moe_cfg& c, const WsLayout& L, void* ws, const int32_t* t
   const int R = c.T * c.k;
   MOE_TRY_CUDA(launch_scan(at<int32_t>(ws, L.hist), c.E, L.nb_route, R, at<int32_t>(ws, L.base), counts, offsets, s));
   MOE_TRY_CUDA(launch_scatter(topk_idx, at<int32_t>(ws, L.base), c.T, c.E, c.k, L.nb_route, dest, row_token,
-                              row_slot, s));
+                              row_slot, at<int>(ws, L.err), s));
   return MOE_OK;
 }
 
@@ -206,6 +206,28 @@ int moe_set_gemm_prefetch(int kind, int kblocks) {
   return set_gemm_prefetch(static_cast<GemmKind>(kind), kblocks);
 }
 
+int moe_set_gemm_tile_order(int kind, int order) {
+  if (kind != kDW13 && kind != kDW2) return MOE_ERR_ARG;
+  if (order != 0 && order != 1) return MOE_ERR_ARG;
+  return set_gemm_tile_order(static_cast<GemmKind>(kind), order);
+}
+
+int moe_set_gemm_epilogue(int kind, int direct) {
+  if ((kind != kG2 && kind != kDX && kind != kDW13 && kind != kDW2) || (direct != 0 && direct != 1))
+    return MOE_ERR_ARG;
+  return set_gemm_epilogue(static_cast<GemmKind>(kind), direct);
+}
+
+int moe_set_gemm_stages(int kind, int stages) {
+  if (kind < kG1 || kind > kDW2 || stages < 0) return MOE_ERR_ARG;
+  return set_gemm_stages(static_cast<GemmKind>(kind), stages);
+}
+
+int moe_gemm_max_stages(int kind, int cta_group) {
+  if (kind < kG1 || kind > kDW2 || (cta_group != 1 && cta_group != 2)) return 0;
+  return gemm_max_stages(static_cast<GemmKind>(kind), cta_group);
+}
+
 int moe_gemm_pair_capacity(int kind) {
   if (kind < kG1 || kind > kDW2) return 0;
   return gemm_pair_capacity(static_cast<GemmKind>(kind));
@@ -230,7 +252,7 @@ int moe_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const uint16_t* x,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_TRY_CUDA(launch_hist(topk_idx, c.T, c.E, c.k, at<int32_t>(ws, L.hist), L.nb_route, at<int>(ws, L.err), s));
   MOE_TRY(build_tables(c, L, ws, topk_idx, counts, offsets, dest, row_token, row_slot, s));
-  if (x && Xp) MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, s));
+  if (x && Xp) MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, at<int>(ws, L.err), s));
   return MOE_OK;
 }
 
@@ -245,7 +267,7 @@ int moe_token_addresses(const moe_cfg* cfg, const int32_t* topk_idx, const int32
   MOE_TRY_CUDA(launch_hist(topk_idx, c.T, c.E, c.k, at<int32_t>(ws, L.hist), L.nb_route, at<int>(ws, L.err), s));
   MOE_TRY_CUDA(launch_scan(at<int32_t>(ws, L.hist), c.E, L.nb_route, c.T * c.k, base, counts, offsets, s));
   if (rank_base) MOE_TRY_CUDA(launch_rebase(base, offsets, rank_base, c.E, L.nb_route, s));
-  MOE_TRY_CUDA(launch_scatter(topk_idx, base, c.T, c.E, c.k, L.nb_route, dest, nullptr, nullptr, s));
+  MOE_TRY_CUDA(launch_scatter(topk_idx, base, c.T, c.E, c.k, L.nb_route, dest, nullptr, nullptr, at<int>(ws, L.err), s));
   return MOE_OK;
 }
 
@@ -274,7 +296,7 @@ int moe_combine(const moe_cfg* cfg, const float* Oprime, const int32_t* dest, fl
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({Oprime, dest, y}, {}, ws));
   const moe_cfg& c = *cfg;
-  MOE_TRY_CUDA(launch_sum_rows_f32(Oprime, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, static_cast<cudaStream_t>(stream)));
+  MOE_TRY_CUDA(launch_sum_rows_f32(Oprime, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, at<int>(ws, 0), static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -296,10 +318,10 @@ int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x, co
     return megakernel_fwd(c, L, static_cast<uint8_t*>(ws), x, W1, W3, W2, topk_w, y, persistent_grid(), s);
   uint16_t* Xp = at<uint16_t>(ws, L.Xp);
   float* Op = at<float>(ws, L.Op);
-  MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, s));
+  MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, at<int>(ws, L.err), s));
   MOE_TRY(fwd_gemms(c, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, at<uint16_t>(ws, L.H),
                     at<uint16_t>(ws, L.AB), Op, s));
-  MOE_TRY_CUDA(launch_sum_rows_f32(Op, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, s));
+  MOE_TRY_CUDA(launch_sum_rows_f32(Op, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, at<int>(ws, L.err), s));
   return MOE_OK;
 }
 
@@ -308,7 +330,7 @@ int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_t
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({dy, row_token, G}, {}, ws));
   const moe_cfg& c = *cfg;
-  MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, c.T * c.k, c.d_model, G, MOE_K_COMBINE_BWD, static_cast<cudaStream_t>(stream)));
+  MOE_TRY_CUDA(launch_gather_rows_bf16(dy, row_token, c.T, c.T * c.k, c.d_model, G, MOE_K_COMBINE_BWD, at<int>(ws, 0), static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -350,7 +372,7 @@ int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint1
   a.dW2_out = dW2;
   if (which & 1) {
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
-    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, c.T * c.k, L.nt_dh, dw, s));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, c.T * c.k, L.nt_dh, dw, at<int>(ws, L.err), s));
     MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
   }
   if (which & 2) {
@@ -364,7 +386,7 @@ int moe_dispatch_bwd(const moe_cfg* cfg, const float* dXp, const int32_t* dest, 
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({dXp, dest, dx}, {}, ws));
   const moe_cfg& c = *cfg;
-  MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, static_cast<cudaStream_t>(stream)));
+  MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, at<int>(ws, 0), static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -373,7 +395,7 @@ int moe_route_bwd(const moe_cfg* cfg, const float* logits, const int32_t* topk_i
   MOE_TRY(check_cfg(cfg));
   MOE_TRY(check_ptrs({logits, topk_idx, topk_w, dw, dlogits}, {}, ws));
   const moe_cfg& c = *cfg;
-  MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits,
+  MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, at<int>(ws, 0),
                                 static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
@@ -440,14 +462,14 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
       MOE_TRY(launch_gemm(kDW2, a, side->s, persistent_grid()));
       MOE_TRY_CUDA(cudaEventRecord(side->join, side->s));
     }
-    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
-    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, at<int>(ws, L.err), s));
+    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, at<int>(ws, L.err), s));
     if (side) {
       MOE_TRY_CUDA(cudaStreamWaitEvent(s, side->join, 0));
       return MOE_OK;
     }
   } else if (which & 1) {  // B part: input gradients (critical path)
-    MOE_TRY_CUDA(launch_scatter_rows_bf16(dy, dest, c.T, c.k, c.d_model, G, MOE_K_COMBINE_BWD, s));
+    MOE_TRY_CUDA(launch_scatter_rows_bf16(dy, dest, c.T, c.k, c.d_model, G, MOE_K_COMBINE_BWD, at<int>(ws, L.err), s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
     if (side) {
       MOE_TRY_CUDA(cudaEventRecord(side->fork, s));
@@ -456,17 +478,17 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
       MOE_TRY(launch_gemm(kDW13, a, side->s, persistent_grid()));
       MOE_TRY(launch_gemm(kDW2, a, side->s, persistent_grid()));
       MOE_TRY_CUDA(cudaEventRecord(side->join, side->s));
-      MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
-      MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+      MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, at<int>(ws, L.err), s));
+      MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, at<int>(ws, L.err), s));
       MOE_TRY_CUDA(
-          launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, s));
+          launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, at<int>(ws, L.err), s));
       MOE_TRY_CUDA(cudaStreamWaitEvent(s, side->join, 0));
       return MOE_OK;
     }
-    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, s));
-    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, s));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, at<int>(ws, L.err), s));
+    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, at<int>(ws, L.err), s));
     MOE_TRY(launch_gemm(kDX, a, s, persistent_grid()));
-    MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, s));
+    MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, at<int>(ws, L.err), s));
   }
   if (which & 2) {  // W part: weight gradients (deferrable)
     MOE_TRY(launch_gemm(kDW13, a, s, persistent_grid()));

@@ -24,6 +24,40 @@ __device__ __forceinline__ void record_error(int* err, int code, int info) {
 }
 #endif
 
+// Checks of the debug build (compiled with -DMOE_DEBUG; the release build
+// compiles them out).  A failed check records MOE_ERR_ARG with the site and
+// a detail in the device error word, info = site << 24 | (detail & 0xFFFFFF);
+// the kernel then skips the access it guards.  No check traps: the launch
+// still returns normally and the context stays usable.
+#ifdef MOE_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+enum DebugSite : int {
+  kDbgGatherRow = 0x41,     // gathered row index outside the source rows
+  kDbgScatterRow = 0x42,    // destination row outside the gathered rows
+  kDbgSumRow = 0x43,        // summed row outside the rows
+  kDbgDwReduce = 0x44,      // dw partial row outside the routed rows
+  kDbgRouteBwd = 0x45,      // expert index outside [0, E)
+  kDbgPermRow = 0x46,       // permutation row outside [0, R)
+  kDbgSegments = 0x50,      // + GEMM kind: segment table not monotone / not ending at R
+  kDbgTmaCoord = 0x58,      // + GEMM kind: TMA box start misaligned or negative
+  kDbgEpiRow = 0x60,        // + GEMM kind: epilogue row outside the GEMM rows, or its slot outside [0, R)
+  kDbgMegaGather = 0x68,    // MegaKernel gather: token outside [0, T)
+  kDbgMegaCombine = 0x69,   // MegaKernel token sum: row outside the rows
+};
+#ifdef __CUDACC__
+__device__ __forceinline__ bool debug_ok(bool cond, int* err, int site, long long detail) {
+  if constexpr (kDebug) {
+    if (!cond && err) record_error(err, MOE_ERR_ARG, site << 24 | static_cast<int>(detail & 0xFFFFFF));
+    return cond;
+  } else {
+    return true;
+  }
+}
+#endif
+
 // Words of the 64-byte error region (int index) that hold the grid barrier
 // of the fused routing + permutation kernel: the arrival count (back to 0
 // after every completed barrier) and the generation.  moe_ws_init zeroes

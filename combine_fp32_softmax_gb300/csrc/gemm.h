@@ -60,6 +60,22 @@ int set_gemm_pair_kinds(int mask);
 // value, or -1 for an unknown kind.
 int set_gemm_prefetch(GemmKind kind, int kblocks);
 
+// Tile order of a ragged-K kind (kDW13, kDW2): 0 = longest segments first,
+// 1 = the long segments' tiles interleaved with the short ones.  Returns
+// the previous order, or -1 for another kind.
+int set_gemm_tile_order(GemmKind kind, int order);
+
+// Epilogue stores of an fp32-output kind (kG2, kDX, kDW13, kDW2): 0 = staged
+// through shared memory and written by TMA, 1 = straight from registers.
+// Returns the previous mode, or -1 for another kind.
+int set_gemm_epilogue(GemmKind kind, int direct);
+
+// Pipeline stages kind `kind` uses (0 or out of range: as many as fit; at
+// least 2).  Returns the previous request, or -1 for an unknown kind.
+int set_gemm_stages(GemmKind kind, int stages);
+// Stages that fit for `kind` with `cta_group` CTAs per tile.
+int gemm_max_stages(GemmKind kind, int cta_group);
+
 // CTA pairs of `kind` that fit on the device at once (0 on error).
 int gemm_pair_capacity(GemmKind kind);
 

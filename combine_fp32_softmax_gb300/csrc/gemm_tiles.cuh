@@ -79,6 +79,9 @@ struct GemmParams {
   int nt_dh;   // dH: column tiles per row (number of partial dot products)
   int has_ab;  // GEMM 1: save [a|b]
   int prefetch_kb;  // K blocks of a CTA's next tile brought into L2 ahead of its loads
+  int tile_order;   // ragged-K kinds: 0 = longest segments first, 1 = long segments' tiles interleaved
+  int nst;          // pipeline stages in use (at most Pipe<KIND, CG>::STAGES)
+  int epi_direct;   // fp32-output kinds: 1 = epilogue stores straight from registers (no staging)
   const int32_t* offsets;
   const int32_t* row_slot;
   const float* topk_w;
@@ -129,6 +132,8 @@ struct SharedState {
   int nseg;
   int total_tiles;
   int tiles_per_seg;  // ragged-K kinds: every segment has the same tile count
+  int long_tiles;     // ragged-K kinds, interleaved order: tiles of the long segments (0: plain order)
+  int long_span;      // ... spread evenly over the first long_span tickets
   int seg_row0[kMaxSeg];
   union {
     int prefix[kMaxSeg + 1];  // ragged-M kinds: tiles before each segment
@@ -185,6 +190,11 @@ __device__ void build_segments(const GemmParams& p, SharedState& ss) {
   for (int s = threadIdx.x; s < nseg; s += blockDim.x)
     ss.seg_row0[s] = (s < p.E) ? p.offsets[s] : p.R + (s - p.E) * p.T;
   __syncthreads();
+  if (kDebug && threadIdx.x == 0) {  // the routing tables' segment starts: 0, non-decreasing, ending at R
+    bool ok = ss.seg_row0[0] == 0 && p.offsets[p.E] == p.R;
+    for (int s = 1; s < p.E; ++s) ok = ok && ss.seg_row0[s] >= ss.seg_row0[s - 1];
+    debug_ok(ok, p.err, kDbgSegments + KIND, blockIdx.x);
+  }
   if constexpr (Traits<KIND>::RAGGED_K) {
     // Longest segments first: their tiles (K = their rows) are spread over
     // the CTAs before the short ones fill in, so no long tile ends the
@@ -202,6 +212,30 @@ __device__ void build_segments(const GemmParams& p, SharedState& ss) {
       ss.tiles_per_seg = tiles_of<KIND, CG>(p, 0);
       ss.total_tiles = ss.tiles_per_seg * nseg;
       ss.nseg = nseg;
+      // Interleaved order: a segment is long if it has more than twice the
+      // mean rows of the non-empty segments.  The long segments (first in
+      // `order`) are compute-heavy per output byte, the short ones
+      // write-heavy; spreading the long ones' tiles over the first 3/4 of
+      // the tickets keeps both kinds running side by side, and the last
+      // long tile still starts early enough to end with the rest.
+      ss.long_tiles = 0;
+      ss.long_span = 0;
+      if (p.tile_order == 1) {
+        long long total_rows = 0;
+        int nonempty = 0;
+        for (int u = 0; u < nseg; ++u) {
+          const int m = seg_rows(p, ss, u);
+          total_rows += m;
+          nonempty += m > 0 ? 1 : 0;
+        }
+        int nlong = 0;
+        while (nlong < nseg && static_cast<long long>(seg_rows(p, ss, ss.order[nlong])) * nonempty > 2 * total_rows)
+          ++nlong;
+        if (nlong > 0 && nlong < nseg) {
+          ss.long_tiles = nlong * ss.tiles_per_seg;
+          ss.long_span = max(ss.long_tiles, static_cast<int>((3ll * ss.total_tiles) / 4));
+        }
+      }
     }
   } else if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -234,8 +268,18 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
                                                 int rank = 0) {
   using Tr = Traits<KIND>;
   int lo = 0, hi = ss.nseg;
+  int pos = tile;  // ragged-K kinds: position in the segment order (segment-major)
   if constexpr (Tr::RAGGED_K) {  // equal tile counts per segment, taken in ss.order
-    lo = ss.order[tile / ss.tiles_per_seg];
+    if (ss.long_tiles > 0) {
+      // Long tile j sits at ticket floor(j * span / NL); the count of long
+      // positions <= i is ceil((i + 1) * NL / span), capped at NL.  Short
+      // tiles fill the other tickets in order.
+      const long long NL = ss.long_tiles, span = ss.long_span;
+      auto nlong_upto = [&](long long i) { return i < 0 ? 0ll : min(NL, ((i + 1) * NL + span - 1) / span); };
+      const long long c = nlong_upto(tile), cprev = nlong_upto(tile - 1);
+      pos = static_cast<int>(c > cprev ? c - 1 : NL + (tile - c));
+    }
+    lo = ss.order[pos / ss.tiles_per_seg];
   } else {
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -248,7 +292,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
   TileInfo t;
   t.seg = lo;
   t.shared = lo >= p.E;
-  const int local = Tr::RAGGED_K ? tile % ss.tiles_per_seg : tile - ss.prefix[lo];
+  const int local = Tr::RAGGED_K ? pos % ss.tiles_per_seg : tile - ss.prefix[lo];
   const int ntn = (p.N + Tr::BNE - 1) / Tr::BNE;
   const int mb = local / ntn, nb = local - mb * ntn;
   t.m0 = mb * Pipe<KIND, CG>::TILE_M + rank * kBM;
@@ -263,6 +307,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Share
     t.grow0 = ss.seg_row0[lo] + t.m0;
     t.nkb = p.K / kBK;
     t.active = t.rows > 0;
+  }
+  if constexpr (kDebug) {  // the tile's rows lie inside the GEMM rows (TMA boxes start inside their tensor)
+    const long long rs = static_cast<long long>(p.R) + static_cast<long long>(p.S) * p.T;
+    const bool ok = t.grow0 >= 0 && (!t.active || static_cast<long long>(t.grow0) + t.rows <= rs);
+    if (!debug_ok(ok, p.err, kDbgTmaCoord + KIND, tile)) t.active = false;
   }
   return t;
 }
@@ -354,6 +403,20 @@ __device__ __forceinline__ void tmem_ld_32x16(uint32_t taddr, uint32_t (&r)[16])
       : "memory");
 }
 
+// 16 TMEM lanes x 4 repetitions of 256 bits (8 consecutive 32-bit columns
+// each): thread t of the warp gets, for repetition j, lane (base + t/4)
+// columns 8j + 2(t%4) + {0, 1} in r[4j], r[4j+1] and lane (base + 8 + t/4)
+// the same columns in r[4j+2], r[4j+3].
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // One row of a 32-row x 64-byte staging chunk in the TMA 64-byte swizzle
 // layout: 16-byte piece c of row r sits at piece c ^ ((r >> 1) & 3).  A
 // warp writing or reading one row per lane touches every bank once per
@@ -398,7 +461,10 @@ struct EpiState {
 // segment), read while the tile's main loop still runs.
 __device__ __forceinline__ float row_weight(const GemmParams& p, const TileInfo& t, int q) {
   const int r = 32 * q + (threadIdx.x & 31);
-  return (r < t.rows && !t.shared) ? p.topk_w[p.row_slot[static_cast<size_t>(t.grow0) + r]] : 1.f;
+  if (!(r < t.rows && !t.shared)) return 1.f;
+  const int slot = p.row_slot[static_cast<size_t>(t.grow0) + r];
+  if (!debug_ok(static_cast<unsigned>(slot) < static_cast<unsigned>(p.R), p.err, kDbgEpiRow, t.grow0 + r)) return 0.f;
+  return p.topk_w[slot];
 }
 
 // Staging helper: lane 0 waits until earlier chunks stopped reading the
@@ -493,6 +559,99 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
       for (int i = 0; i < 16; ++i) cur[i] = zero ? 0u : nxt[i];
     }
   }
+}
+
+// fp32 outputs written straight from registers (no shared-memory staging).
+// Each group of 32 accumulator columns is read as two 16-lane halves in the
+// 16x256b shape, and one exchange between neighbouring threads leaves every
+// thread 4 consecutive columns of one row: a warp store then covers 8 rows x
+// 64 contiguous bytes (two full 32-byte sectors per row).  Rows and columns
+// outside the output are not written; the same values as epilogue_f32.
+template <int KIND>
+__device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
+                                                    EpiState& es) {
+  const int lane = threadIdx.x & 31;
+  const int quad = lane >> 2, c = lane & 3;
+  int N;
+  float* base;       // output element (row 32q of this warp, column 0)
+  long long ld;      // row stride in elements
+  int valid_rows;    // rows of this warp (from 32q) that exist
+  if constexpr (KIND == kG2 || KIND == kDX) {
+    N = p.d;
+    ld = N;
+    base = static_cast<float*>(p.out0) + (static_cast<size_t>(t.grow0) + 32 * q) * N;
+    valid_rows = t.rows - 32 * q;
+  } else if constexpr (KIND == kDW13) {
+    N = p.d;
+    ld = N;
+    const int mw0 = t.m0 + 32 * q;
+    const bool second = mw0 >= p.f;
+    base = static_cast<float*>(second ? p.out1 : p.out0) +
+           (static_cast<size_t>(t.seg) * p.f + (second ? mw0 - p.f : mw0)) * N;
+    valid_rows = 32;
+  } else {  // kDW2
+    N = p.f;
+    ld = N;
+    base = static_cast<float*>(p.out0) + (static_cast<size_t>(t.seg) * p.d + t.m0 + 32 * q) * N;
+    valid_rows = p.d - t.m0 - 32 * q;
+  }
+  const bool zero = Traits<KIND>::RAGGED_K && t.nkb == 0;  // empty expert: exact zeros
+  // routing weight of each row this thread writes (GEMM 2 only)
+  float wrow[4] = {1.f, 1.f, 1.f, 1.f};
+  if constexpr (KIND == kG2) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) wrow[h] = __shfl_sync(0xffffffffu, es.w, 16 * (h >> 1) + 8 * (h & 1) + quad);
+  }
+  const int ncols = min(256, N - t.n0);
+#pragma unroll 1
+  for (int g = 0; g < ncols; g += 32) {
+    uint32_t v[2][16];
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
+    } else {
+      tmem_ld_16x256b_x4(tacc + g, v[0]);
+      tmem_ld_16x256b_x4(tacc + (16u << 16) + g, v[1]);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {       // rows quad (sub 0) and quad + 8 (sub 1) of this half
+        const int h = 2 * half + sub;
+        const int row = 16 * half + 8 * sub + quad;
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {        // repetitions 2jp and 2jp + 1
+          const int j0 = 2 * jp, j1 = 2 * jp + 1;
+          const uint32_t* a = &v[half][4 * j0 + 2 * sub];
+          const uint32_t* b = &v[half][4 * j1 + 2 * sub];
+          // even threads keep repetition j0 and take the odd neighbour's j0;
+          // odd threads keep j1 and take the even neighbour's j1
+          const bool odd = c & 1;
+          const uint32_t s0 = __shfl_xor_sync(0xffffffffu, odd ? a[0] : b[0], 1);
+          const uint32_t s1 = __shfl_xor_sync(0xffffffffu, odd ? a[1] : b[1], 1);
+          float4 o;
+          int col;
+          if (!odd) {
+            o = make_float4(__uint_as_float(a[0]), __uint_as_float(a[1]), __uint_as_float(s0), __uint_as_float(s1));
+            col = g + 8 * j0 + 2 * c;
+          } else {
+            o = make_float4(__uint_as_float(s0), __uint_as_float(s1), __uint_as_float(b[0]), __uint_as_float(b[1]));
+            col = g + 8 * j1 + 2 * (c - 1);
+          }
+          if constexpr (KIND == kG2) {
+            o.x *= wrow[h];
+            o.y *= wrow[h];
+            o.z *= wrow[h];
+            o.w *= wrow[h];
+          }
+          if (row < valid_rows && t.n0 + col < N)
+            *reinterpret_cast<float4*>(base + static_cast<long long>(row) * ld + t.n0 + col) = o;
+        }
+      }
+    }
+  }
+  es.chunks = 0;
 }
 
 // GEMM 1: columns [0,128) of the accumulator hold a (gate), [128,256) hold b
@@ -712,9 +871,9 @@ struct ProducerState {
 // odd CTA's data and the MMA.  A ragged-K tail is the exception: each CTA's
 // loads complete on its own full[s], each zeroes its own rows past the
 // segment end, and the odd CTA then arrives on the even CTA's ready[s].
-template <int KIND, int NST, int CG = 1>
+template <int KIND, int CG = 1>
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
-                                             ProducerState& ps, volatile int* abort, int where, int rank = 0) {
+                                             ProducerState& ps, volatile int* abort, int where, int NST, int rank = 0) {
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
   for (int kb = 0; kb < t.nkb; ++kb) {
     if (!mbar_wait(&ss.empty[ps.stage], ps.phase ^ 1, abort, p.err, where)) return false;
@@ -792,9 +951,9 @@ __device__ __forceinline__ void zero_k_tail(const TileInfo& t, int kb, uint8_t* 
 // CTAs of a pair), and the finished accumulator to the epilogues (both
 // CTAs).  The odd CTA's MMA warp only handles ragged-K tails: waits for its
 // own stage, zeroes its rows past the segment end and tells the even CTA.
-template <int KIND, int NST, int CG = 1>
+template <int KIND, int CG = 1>
 __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
-                                         uint32_t tmem, MmaState& ms, volatile int* abort, int where,
+                                         uint32_t tmem, MmaState& ms, volatile int* abort, int where, int NST,
                                          int rank = 0) {
   using Tr = Traits<KIND>;
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
@@ -916,7 +1075,12 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   else if constexpr (KIND == kDH)
     ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where);
   else
-    epilogue_f32<KIND>(p, t, q, tacc, stg, es);
+  {
+    if (p.epi_direct)
+      epilogue_f32_direct<KIND>(p, t, q, tacc, es);
+    else
+      epilogue_f32<KIND>(p, t, q, tacc, stg, es);
+  }
   tc_fence_before();
   __syncwarp();
   if (ok && lane == 0) {

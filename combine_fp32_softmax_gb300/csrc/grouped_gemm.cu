@@ -61,7 +61,7 @@ __device__ __forceinline__ int feed_get(SharedState& ss, int i, int rank, volati
 // 256-row tile per pair; the even CTA issues the MMAs for both.
 template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int NST = Pipe<KIND, CG>::STAGES;
+  const int NST = p.nst;  // at most Pipe<KIND, CG>::STAGES (checked by the launcher)
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The 128-byte-swizzled stages need a 1024-byte-aligned base; the dynamic
@@ -130,8 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           if (!feed_put<CG>(ss, i, tile, abort, p.err, wfeed | (i & 0xfffff)) || tile < 0) break;
           if (p.prefetch_kb > 0 && next < total)
             prefetch_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, next, rank), rank);
-          if (!produce_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
-                                           where0 | tile, rank))
+          if (!produce_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
+                                       where0 | tile, NST, rank))
             break;
         }
         // The last ticket taker to finish sets the counters back to 0 for
@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           if (tile < 0) break;
           if (!DYN && p.prefetch_kb > 0 && tile + step < total)
             prefetch_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile + step, rank), rank);
-          if (!produce_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
-                                           where0 | tile, rank))
+          if (!produce_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, ps, abort,
+                                       where0 | tile, NST, rank))
             break;
         }
       }
@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     MmaState ms;
     for (int i = 0;; ++i) {
       const int tile = tile_of(i, wfeed | (1 << 19) | (i & 0x7ffff));
-      if (tile < 0 || !mma_tile<KIND, NST, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, tmem, ms,
-                                               abort, where0 | (2 << 20) | tile, rank))
+      if (tile < 0 || !mma_tile<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, smem, tmem, ms,
+                                          abort, where0 | (2 << 20) | tile, NST, rank))
         break;
     }
     if (*abort) mma_drain<CG>(ss, ms);
@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // per layer).
 int g_pair_kinds = (1 << 6) - 1;
 int g_prefetch_kb[6] = {0, 0, 0, 0, 0, 0};  // per kind: next-tile K blocks prefetched into L2
+int g_tile_order[6] = {0, 0, 0, 0, 0, 0};   // per ragged-K kind: 0 longest first, 1 long tiles interleaved
+int g_stages[6] = {0, 0, 0, 0, 0, 0};       // per kind: pipeline stages (0: as many as fit)
+int g_epi_direct[6] = {0, 0, 0, 0, 0, 0};   // per fp32-output kind: 1 = unstaged epilogue stores
 
 // Launch configuration of one kind; CG = 2 adds the cluster dimension.
 template <int KIND, int CG>
@@ -232,6 +235,12 @@ int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
   GemmParams p;
   if (!fill_params<KIND, CG>(a, p)) return MOE_ERR_CUDA;
   p.prefetch_kb = g_prefetch_kb[KIND];
+  p.tile_order = g_tile_order[KIND];
+  p.epi_direct = g_epi_direct[KIND];
+  // Fewer stages leave part of the ring unused; the launch still takes the
+  // whole shared-memory budget, so one CTA per SM stays resident.
+  constexpr int kMaxSt = Pipe<KIND, CG>::STAGES;
+  p.nst = (g_stages[KIND] >= 2 && g_stages[KIND] < kMaxSt) ? g_stages[KIND] : kMaxSt;
   constexpr int kSmem = smem_bytes<KIND, CG>();
   static_assert(kSmem <= 232448, "shared memory budget of one CTA");
   auto kern = grouped_gemm_kernel<KIND, CG>;
@@ -292,6 +301,39 @@ int set_gemm_prefetch(GemmKind kind, int kblocks) {
   const int prev = g_prefetch_kb[kind];
   g_prefetch_kb[kind] = kblocks < 0 ? 0 : (kblocks > 64 ? 64 : kblocks);
   return prev;
+}
+
+int set_gemm_tile_order(GemmKind kind, int order) {
+  if (kind != kDW13 && kind != kDW2) return -1;
+  const int prev = g_tile_order[kind];
+  g_tile_order[kind] = order ? 1 : 0;
+  return prev;
+}
+
+int set_gemm_epilogue(GemmKind kind, int direct) {
+  if (kind != kG2 && kind != kDX && kind != kDW13 && kind != kDW2) return -1;
+  const int prev = g_epi_direct[kind];
+  g_epi_direct[kind] = direct ? 1 : 0;
+  return prev;
+}
+
+int set_gemm_stages(GemmKind kind, int stages) {
+  if (kind < kG1 || kind > kDW2) return -1;
+  const int prev = g_stages[kind];
+  g_stages[kind] = stages < 0 ? 0 : stages;
+  return prev;
+}
+
+int gemm_max_stages(GemmKind kind, int cta_group) {
+  switch (kind) {
+    case kG1: return cta_group == 2 ? Pipe<kG1, 2>::STAGES : Pipe<kG1, 1>::STAGES;
+    case kG2: return cta_group == 2 ? Pipe<kG2, 2>::STAGES : Pipe<kG2, 1>::STAGES;
+    case kDH: return cta_group == 2 ? Pipe<kDH, 2>::STAGES : Pipe<kDH, 1>::STAGES;
+    case kDX: return cta_group == 2 ? Pipe<kDX, 2>::STAGES : Pipe<kDX, 1>::STAGES;
+    case kDW13: return cta_group == 2 ? Pipe<kDW13, 2>::STAGES : Pipe<kDW13, 1>::STAGES;
+    case kDW2: return cta_group == 2 ? Pipe<kDW2, 2>::STAGES : Pipe<kDW2, 1>::STAGES;
+  }
+  return 0;
 }
 
 int set_gemm_pair_kinds(int mask) {

@@ -158,7 +158,10 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
       uint8_t* buf = smem + b * kStageBytes;
       mbar_arrive_expect_tx(&ms.gbar[b], n * rb);
       for (int i = 0; i < n; ++i) {
-        const int tok = mp.row_token[r0 + c * rps + i];
+        int tok = mp.row_token[r0 + c * rps + i];
+        if (!debug_ok(static_cast<unsigned>(tok) < static_cast<unsigned>(mp.g1.T), mp.g1.err, kDbgMegaGather,
+                      r0 + c * rps + i))
+          tok = 0;
         bulk_load(buf + i * rb, mp.x + static_cast<size_t>(tok) * d, rb, &ms.gbar[b]);
       }
       gs.pending |= 1u << b;
@@ -207,9 +210,10 @@ __device__ void combine_token(const MegaParams& mp, int t) {
   const float4* rows = reinterpret_cast<const float4*>(mp.Op);
   {
     long long myrow = 0;
-    if (lane < k)
+    if (lane < k) {
       myrow = mp.dest[static_cast<size_t>(t) * k + lane];
-    else if (lane < nr)
+      if (!debug_ok(myrow >= 0 && myrow < R, mp.g1.err, kDbgMegaCombine, t)) myrow = 0;
+    } else if (lane < nr)
       myrow = R + static_cast<long long>(lane - k) * T + t;
     const float4* base[kMaxTokRows];
 #pragma unroll
@@ -344,13 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
             if (!ok) break;
             fence_proxy_async_global();
           }
-          if (!produce_tile<KA, NST>(mp.g1, t, ss, smem, ps, abort, where)) break;
+          if (!produce_tile<KA>(mp.g1, t, ss, smem, ps, abort, where, NST)) break;
         } else if (id < e2) {
           const int t2 = id - e1;
           const int mt = t2 / ms.ntn2;
           if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kEpiWarps * ms.ntn1, abort, err, where)) break;
           fence_proxy_async_global();
-          if (!produce_tile<KB, NST>(mp.g2, decode_g2<KA, KB>(mp, ms, t2), ss, smem, ps, abort, where)) break;
+          if (!produce_tile<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, t2), ss, smem, ps, abort, where, NST)) break;
         }
         trace_record(mp, 0, tn, id, t_claim);
       }
@@ -379,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       const int where = kW | (2 << 20) | (id & 0xFFFFF);
       bool ok = true;
       if (id >= NG && id < e1)
-        ok = mma_tile<KA, NST>(mp.g1, decode_tile<KA>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<KA>(mp.g1, decode_tile<KA>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where, NST);
       else if (id >= e1 && id < e2)
-        ok = mma_tile<KB, NST>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, smem, tmem, mst, abort, where);
+        ok = mma_tile<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, smem, tmem, mst, abort, where, NST);
       if (!ok) break;
     }
     if (*abort) mma_drain(ss, mst);

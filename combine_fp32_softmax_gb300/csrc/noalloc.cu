@@ -89,9 +89,9 @@ extern "C" int moe_dispatch_noalloc(const moe_cfg* cfg, const int32_t* topk_idx,
   const int R = c.T * c.k;
   if (launch_hist(topk_idx, c.T, c.E, c.k, hist, nb, err, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_scan(hist, c.E, nb, R, base, counts, offsets, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_scatter(topk_idx, base, c.T, c.E, c.k, nb, dest, row_token, row_slot, s) != cudaSuccess)
+  if (launch_scatter(topk_idx, base, c.T, c.E, c.k, nb, dest, row_token, row_slot, err, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (x && Xp && launch_gather_rows_bf16(x, row_token, c.T, R, c.d_model, Xp, MOE_K_GATHER, s) != cudaSuccess)
+  if (x && Xp && launch_gather_rows_bf16(x, row_token, c.T, R, c.d_model, Xp, MOE_K_GATHER, err, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

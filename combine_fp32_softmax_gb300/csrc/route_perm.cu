@@ -317,7 +317,8 @@ template <int NW>
 __device__ __forceinline__ void scatter_block(const int32_t* __restrict__ topk_idx, const int32_t* base,
                                               const int* off, int hb, int T, int E, int k, int nb,
                                               int (*wrun)[256], int32_t* __restrict__ dest,
-                                              int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot) {
+                                              int32_t* __restrict__ row_token, int32_t* __restrict__ row_slot,
+                                              int* err) {
   constexpr int TPW = kRouteTokensPerBlock / NW;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   for (int i = tid; i < NW * 256; i += NW * 32) (&wrun[0][0])[i] = 0;
@@ -355,7 +356,8 @@ __device__ __forceinline__ void scatter_block(const int32_t* __restrict__ topk_i
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) wrun[w][e] += __popc(peers);
     __syncwarp();
-    if (valid) {
+    if (valid && (row_token == nullptr ||
+                  debug_ok(static_cast<unsigned>(r) < static_cast<unsigned>(T * k), err, kDbgPermRow, slot0 + il))) {
       const size_t i = slot0 + il;
       dest[i] = r;
       if (row_token) {  // inverse tables only when the addresses are local rows
@@ -371,9 +373,10 @@ constexpr int kScatterWarps = 8;
 __global__ void __launch_bounds__(kScatterWarps * 32)
     scatter_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, int T, int E, int k,
                    int nb, int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
-                   int32_t* __restrict__ row_slot) {
+                   int32_t* __restrict__ row_slot, int* err) {
   __shared__ int wrun[kScatterWarps][256];
-  scatter_block<kScatterWarps>(topk_idx, base, nullptr, blockIdx.x, T, E, k, nb, wrun, dest, row_token, row_slot);
+  scatter_block<kScatterWarps>(topk_idx, base, nullptr, blockIdx.x, T, E, k, nb, wrun, dest, row_token, row_slot,
+                               err);
 }
 
 // Grid barrier of a cooperative launch (every block resident at once).
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 2 : 1)
   __syncthreads();
   for (int hb = blockIdx.x; hb < nb; hb += gridDim.x) {
     scatter_block<kRouteWarps>(topk_idx, base, sm.scatter.off, hb, T, E, k, nb, sm.scatter.wrun, dest, row_token,
-                               row_slot);
+                               row_slot, err);
     __syncthreads();  // the next block zeroes wrun
   }
 }
@@ -578,7 +581,7 @@ constexpr int kGatherVec = 8;
 
 __global__ void __launch_bounds__(256)
     gather_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ idx, int nsrc, int nrows,
-                            int nvec, uint4* __restrict__ dst) {
+                            int nvec, uint4* __restrict__ dst, int* err) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -587,6 +590,7 @@ __global__ void __launch_bounds__(256)
     const int rn = r + nwarps;
     const int sr_next = rn < nrows ? idx[rn] : 0;
     const bool ok = static_cast<unsigned>(sr) < static_cast<unsigned>(nsrc);
+    if (lane == 0) debug_ok(ok, err, kDbgGatherRow, r);
     const uint4* s = src + static_cast<size_t>(ok ? sr : 0) * nvec;
     uint4* o = dst + static_cast<size_t>(r) * nvec;
     for (int v = lane; v < nvec; v += 32 * kGatherVec) {
@@ -610,7 +614,7 @@ __global__ void __launch_bounds__(256)
 // capacity.  A destination outside [0, ndst) is skipped.
 __global__ void __launch_bounds__(256)
     scatter_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ dest, int T, int k,
-                             int ndst, int nvec, uint4* __restrict__ dst) {
+                             int ndst, int nvec, uint4* __restrict__ dst, int* err) {
   constexpr int kSpan = 32 * kGatherVec;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
@@ -627,6 +631,7 @@ __global__ void __launch_bounds__(256)
       if (v0 + 32 * i < nvec) val[i] = __ldg(s + v0 + 32 * i);
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(kFull, mydest, j);
+      if (lane == 0 && v0 == 0) debug_ok(static_cast<unsigned>(r) < static_cast<unsigned>(ndst), err, kDbgScatterRow, t);
       if (static_cast<unsigned>(r) >= static_cast<unsigned>(ndst)) continue;
       uint4* o = dst + static_cast<size_t>(r) * nvec;
 #pragma unroll
@@ -649,7 +654,7 @@ constexpr int kSumSpan = 128;
 template <int NR>
 __global__ void __launch_bounds__(256)
     sum_rows_f32_kernel(const float4* __restrict__ rows, const int32_t* __restrict__ sel, int T, int k, int S,
-                        int nvec, float4* __restrict__ out) {
+                        int nvec, float4* __restrict__ out, int* err) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const long long R = static_cast<long long>(T) * k;
@@ -663,6 +668,7 @@ __global__ void __launch_bounds__(256)
     long long myrow = 0;
     if (lane < k) {
       myrow = sel[static_cast<size_t>(t) * k + lane];
+      if (v0 == 0) debug_ok(myrow >= 0 && myrow < nrows, err, kDbgSumRow, t);
       if (myrow < 0 || myrow >= nrows) myrow = 0;
     } else if (lane < NR) {
       myrow = R + static_cast<long long>(lane - k) * T + t;
@@ -699,9 +705,10 @@ __global__ void __launch_bounds__(256)
 
 // dw[i] = sum over column tiles n (in order) of partial[dest[i] * nt + n].
 __global__ void dw_reduce_kernel(const float* __restrict__ partial, const int32_t* __restrict__ dest, int R, int nt,
-                                 float* __restrict__ dw) {
+                                 float* __restrict__ dw, int* err) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= R) return;
+  if (!debug_ok(static_cast<unsigned>(dest[i]) < static_cast<unsigned>(R), err, kDbgDwReduce, i)) return;
   const size_t r = static_cast<size_t>(dest[i]);
   float s = 0.f;
   for (int n = 0; n < nt; ++n) s += partial[r * nt + n];
@@ -714,7 +721,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256)
     route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                      const float* __restrict__ topk_w, const float* __restrict__ dw, int T, int E, int k, int renorm,
-                     float* __restrict__ dlogits) {
+                     float* __restrict__ dlogits, int* err) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -724,6 +731,7 @@ __global__ void __launch_bounds__(256)
     float my_w = 0.f, my_dw = 0.f;
     if (lane < k) {
       my_idx = topk_idx[static_cast<size_t>(t) * k + lane];
+      debug_ok(static_cast<unsigned>(my_idx) < static_cast<unsigned>(E), err, kDbgRouteBwd, t);
       my_w = topk_w[static_cast<size_t>(t) * k + lane];
       my_dw = dw[static_cast<size_t>(t) * k + lane];
     }
@@ -855,9 +863,9 @@ cudaError_t launch_scan(const int32_t* hist, int E, int nb, int R, int32_t* base
 }
 
 cudaError_t launch_scatter(const int32_t* topk_idx, const int32_t* base, int T, int E, int k, int nb, int32_t* dest,
-                           int32_t* row_token, int32_t* row_slot, cudaStream_t s) {
+                           int32_t* row_token, int32_t* row_slot, int* err, cudaStream_t s) {
   TraceScope trace_scope(MOE_K_SCATTER, s);
-  scatter_kernel<<<nb, 256, 0, s>>>(topk_idx, base, T, E, k, nb, dest, row_token, row_slot);
+  scatter_kernel<<<nb, 256, 0, s>>>(topk_idx, base, T, E, k, nb, dest, row_token, row_slot, err);
   return cudaGetLastError();
 }
 
@@ -876,7 +884,7 @@ cudaError_t launch_rank_bases(const int32_t* counts, int G, int E, const int32_t
 }
 
 cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int nsrc, int nrows, int d,
-                                    uint16_t* dst, int trace_kind, cudaStream_t s) {
+                                    uint16_t* dst, int trace_kind, int* err, cudaStream_t s) {
   if (nrows <= 0) return cudaSuccess;
   TraceScope trace_scope(trace_kind, s);
   static int resident = 0;  // blocks resident at once
@@ -889,12 +897,12 @@ cudaError_t launch_gather_rows_bf16(const uint16_t* src, const int32_t* idx, int
   }
   const int blocks = min(ceil_div(nrows, 8), resident);
   gather_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), idx, nsrc, nrows, d / 8,
-                                                 reinterpret_cast<uint4*>(dst));
+                                                 reinterpret_cast<uint4*>(dst), err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_scatter_rows_bf16(const uint16_t* src, const int32_t* dest, int T, int k, int d, uint16_t* dst,
-                                     int trace_kind, cudaStream_t s) {
+                                     int trace_kind, int* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const long long units = static_cast<long long>(T) * ceil_div(d / 8, 32 * kGatherVec);
   if (units >= (1ll << 31) || static_cast<long long>(T) * k >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -909,12 +917,12 @@ cudaError_t launch_scatter_rows_bf16(const uint16_t* src, const int32_t* dest, i
   }
   const int blocks = static_cast<int>(std::min<long long>(ceil_div(units, 8), resident));
   scatter_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dest, T, k, T * k, d / 8,
-                                                  reinterpret_cast<uint4*>(dst));
+                                                  reinterpret_cast<uint4*>(dst), err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
-                                int trace_kind, cudaStream_t s) {
+                                int trace_kind, int* err, cudaStream_t s) {
   TraceScope trace_scope(trace_kind, s);
   const long long units = static_cast<long long>(T) * ceil_div(d / 4, kSumSpan);
   if (units >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -935,7 +943,7 @@ cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, in
   switch (k + S) {
 #define MOE_SUM_ROWS_CASE(N) \
   case N:                                                                                           \
-    sum_rows_f32_kernel<N><<<grid_for(sum_rows_f32_kernel<N>, N), 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4); \
+    sum_rows_f32_kernel<N><<<grid_for(sum_rows_f32_kernel<N>, N), 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4, err); \
     break;
     MOE_SUM_ROWS_CASE(1)
     MOE_SUM_ROWS_CASE(2)
@@ -956,24 +964,25 @@ cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, int nt, float* dw, cudaStream_t s) {
+cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, int nt, float* dw, int* err,
+                             cudaStream_t s) {
   TraceScope trace_scope(MOE_K_DW_REDUCE, s);
-  dw_reduce_kernel<<<ceil_div(R, 256), 256, 0, s>>>(partial, dest, R, nt, dw);
+  dw_reduce_kernel<<<ceil_div(R, 256), 256, 0, s>>>(partial, dest, R, nt, dw, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const float* topk_w, const float* dw,
-                             int T, int E, int k, int renorm, float* dlogits, cudaStream_t s) {
+                             int T, int E, int k, int renorm, float* dlogits, int* err, cudaStream_t s) {
   TraceScope trace_scope(MOE_K_ROUTE_BWD, s);
   const int blocks = min(ceil_div(T, 8), num_sms() * 8);
   if (E <= 32)
-    route_bwd_kernel<1><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+    route_bwd_kernel<1><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
   else if (E <= 64)
-    route_bwd_kernel<2><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+    route_bwd_kernel<2><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
   else if (E <= 128)
-    route_bwd_kernel<4><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+    route_bwd_kernel<4><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
   else
-    route_bwd_kernel<8><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits);
+    route_bwd_kernel<8><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,7 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+from .build import DEBUG_LIB_PATH, LIB_PATH
 from .configs import MoEConfig
 
 CODES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGN",
@@ -29,7 +29,10 @@ class MoeError(RuntimeError):
 
 
 class moe_tune_result(ctypes.Structure):
-    _fields_ = [("pair", ctypes.c_int * 6), ("prefetch_kb", ctypes.c_int * 6), ("us", ctypes.c_float * 6)]
+    _fields_ = [("pair", ctypes.c_int * 6), ("prefetch_kb", ctypes.c_int * 6), ("us", ctypes.c_float * 6),
+                ("tile_order", ctypes.c_int * 6), ("stages", ctypes.c_int * 6), ("epi_direct", ctypes.c_int * 6),
+                ("fwd_megakernel", ctypes.c_int),
+                ("bwd_megakernel", ctypes.c_int), ("fwd_us", ctypes.c_float * 2), ("bwd_us", ctypes.c_float * 2)]
 
 
 class moe_cfg(ctypes.Structure):
@@ -66,6 +69,10 @@ _SIGS = {
     "moe_set_gemm_pair_kinds": ([_I], _I),
     "moe_gemm_pair_capacity": ([_I], _I),
     "moe_set_gemm_prefetch": ([_I, _I], _I),
+    "moe_set_gemm_tile_order": ([_I, _I], _I),
+    "moe_set_gemm_stages": ([_I, _I], _I),
+    "moe_set_gemm_epilogue": ([_I, _I], _I),
+    "moe_gemm_max_stages": ([_I, _I], _I),
     "moe_set_bwd_overlap": ([_I], _I),
     "moe_set_route_fusion": ([_I], _I),
     "moe_autotune": ([_CFG] + [_P] * 15 + [_I, _P, ctypes.POINTER(moe_tune_result)], _I),
@@ -90,10 +97,12 @@ def lib() -> ctypes.CDLL:
     """The loaded library.  Raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+        # MOE_GB300_DEBUG_LIB=1 loads the debug build (tests only)
+        path = DEBUG_LIB_PATH if os.environ.get("MOE_GB300_DEBUG_LIB") == "1" else LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        handle = ctypes.CDLL(LIB_PATH)
+        handle = ctypes.CDLL(path)
         for name, (args, res) in _SIGS.items():
             fn = getattr(handle, name)
             fn.argtypes = args
@@ -240,13 +249,46 @@ def moe_set_gemm_prefetch(kind: int, kblocks: int) -> int:
 
 def moe_autotune(cfg, logits, x, W1, W3, W2, dy, y, topk_idx, topk_w, dx, dlogits, dW1, dW3, dW2, ws,
                  reps=0, stream=None) -> dict:
-    """Times each grouped-GEMM kind under every candidate on this layer, applies the fastest
-    per kind, and returns {kind name: (pair, prefetch_kb, us)}."""
+    """Runs the library's measured autotuner on this layer (applying its GEMM choices process-wide) and
+    returns {"kinds": {kind name: {pair, prefetch_kb, tile_order, stages, us}}, "fwd_megakernel",
+    "bwd_megakernel", "fwd_us": [chain, MegaKernel], "bwd_us": [chain, MegaKernel]}."""
     res = moe_tune_result()
     _call("moe_autotune", _cfg(cfg), _ptr(logits), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), _ptr(y),
           _ptr(topk_idx), _ptr(topk_w), _ptr(dx), _ptr(dlogits), _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(ws),
           int(reps), _stream(stream), ctypes.byref(res))
-    return {name: (res.pair[i], res.prefetch_kb[i], res.us[i]) for i, name in enumerate(GEMM_KINDS)}
+    kinds = {name: {"pair": res.pair[i], "prefetch_kb": res.prefetch_kb[i], "tile_order": res.tile_order[i],
+                    "stages": res.stages[i], "epi_direct": res.epi_direct[i], "us": res.us[i]}
+             for i, name in enumerate(GEMM_KINDS)}
+    return {"kinds": kinds, "fwd_megakernel": res.fwd_megakernel, "bwd_megakernel": res.bwd_megakernel,
+            "fwd_us": list(res.fwd_us), "bwd_us": list(res.bwd_us)}
+
+
+def moe_set_gemm_tile_order(kind: int, order: int) -> int:
+    """Tile order of a weight-gradient kind (4 or 5): 0 longest first, 1 interleaved. Returns the previous order."""
+    r = int(lib().moe_set_gemm_tile_order(int(kind), int(order)))
+    if r < 0:
+        raise MoeError("moe_set_gemm_tile_order", r)
+    return r
+
+
+def moe_set_gemm_epilogue(kind: int, direct: int) -> int:
+    """Epilogue stores of an fp32-output kind (1, 3, 4, 5): 0 staged (TMA), 1 direct. Returns the previous mode."""
+    r = int(lib().moe_set_gemm_epilogue(int(kind), int(direct)))
+    if r < 0:
+        raise MoeError("moe_set_gemm_epilogue", r)
+    return r
+
+
+def moe_set_gemm_stages(kind: int, stages: int) -> int:
+    """Pipeline stages of grouped-GEMM kind `kind` (0: as many as fit). Returns the previous request."""
+    r = int(lib().moe_set_gemm_stages(int(kind), int(stages)))
+    if r < 0:
+        raise MoeError("moe_set_gemm_stages", r)
+    return r
+
+
+def moe_gemm_max_stages(kind: int, cta_group: int) -> int:
+    return int(lib().moe_gemm_max_stages(int(kind), int(cta_group)))
 
 
 def moe_set_bwd_overlap(on: bool) -> int:

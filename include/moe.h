@@ -344,17 +344,55 @@ int moe_set_gemm_pair_kinds(int mask);
  * unknown kind.  Process-wide, not thread-safe. */
 int moe_set_gemm_prefetch(int kind, int kblocks);
 
+/* Tile order of the weight-gradient grouped GEMMs (kinds 4 dW1/dW3 and 5
+ * dW2, numbered as above).  order 0 (the default): tiles handed out longest
+ * segments first.  order 1: the tiles of the long segments (more than twice
+ * the mean rows of the non-empty segments, e.g. the shared experts) are
+ * spread evenly over the first three quarters of the tickets, between the
+ * short segments' tiles, so compute-heavy tiles (long K, few output bytes per
+ * flop) and write-heavy ones (short K, the same fp32 output per tile) run
+ * side by side.  A performance knob only: each output element keeps its one
+ * producer and its K order.  Returns the previous order, or MOE_ERR_ARG for
+ * another kind or order.  Process-wide, not thread-safe. */
+int moe_set_gemm_tile_order(int kind, int order);
+
+/* Epilogue stores of the fp32-output grouped GEMMs (kinds 1 GEMM 2, 3 dX,
+ * 4 dW1/dW3, 5 dW2).  direct 0 (the default): each warp stages its rows
+ * through shared memory and a TMA tensor store writes them.  direct 1: the
+ * accumulator is read in a 16-lane shape and written straight from
+ * registers, 64 contiguous bytes per row and store, sparing the shared
+ * memory traffic of the staging.  Same values either way.  Returns the
+ * previous mode, or MOE_ERR_ARG for another kind or mode.  Process-wide,
+ * not thread-safe. */
+int moe_set_gemm_epilogue(int kind, int direct);
+
+/* Pipeline stages (shared-memory ring slots of one 64-deep K block each) of
+ * grouped-GEMM kind `kind`: 0 = as many as fit (the default), else at least
+ * 2 and at most moe_gemm_max_stages().  A performance knob only.  Returns
+ * the previous request, or MOE_ERR_ARG.  Process-wide, not thread-safe. */
+int moe_set_gemm_stages(int kind, int stages);
+/* Stages that fit for `kind` with cta_group (1 or 2) CTAs per tile; 0 for
+ * an unknown kind or group. */
+int moe_gemm_max_stages(int kind, int cta_group);
+
 /* ------------------------------------------------------------ autotuner
  * UniEP page ("Unified Expert-Parallel MoE MegaKernel for LLM Training"),
  * section 3 names autotuning and an analytical model without giving their
- * content.  moe_autotune measures instead: for each grouped-GEMM kind it times
- * the caller's own layer (forward + backward, kernel chain) under each
- * candidate (one CTA per tile or CTA pairs; next-tile L2 prefetch depth 0, 4
- * or 8 K blocks), keeps the fastest per kind, applies it process-wide through
- * moe_set_gemm_pair_kinds / moe_set_gemm_prefetch, and reports it.  CTA
- * pairs without prefetch are timed first, and a later candidate replaces the
- * one kept only if it is more than 1% faster, so near ties (within run-to-run
- * spread) do not flip the choice.
+ * content.  moe_autotune measures instead, on the caller's own layer
+ * (forward + backward), coordinate-wise:
+ *  1. per grouped-GEMM kind, the tile shape (one CTA per tile or CTA pairs)
+ *     x the next-tile L2 prefetch depth (0, 4 or 8 K blocks);
+ *  2. the weight-gradient kinds' tile order (longest first or interleaved),
+ *     then the fp32-output kinds' epilogue stores (staged or direct);
+ *  3. the pipeline depth (as many stages as fit, or one fewer);
+ *  4. kernel chain against MegaKernel, forward and backward.
+ * Phases 1-3 are applied process-wide (moe_set_gemm_pair_kinds,
+ * moe_set_gemm_prefetch, moe_set_gemm_tile_order, moe_set_gemm_epilogue,
+ * moe_set_gemm_stages);
+ * phase 4 is reported for the caller's use_megakernel / MOE_BWD_MEGAKERNEL
+ * arguments.  The library's defaults are timed first, and a later candidate
+ * replaces the one kept only if it is more than 1% faster, so near ties
+ * (within run-to-run spread) do not flip the choice.
  *
  * Arguments are those of moe_layer_fwd and moe_layer_bwd (all device memory
  * owned by the caller, layouts as there); every output and `ws` are
@@ -369,6 +407,13 @@ typedef struct {
   int pair[6];         /* per kind (numbered as above): 1 = CTA pairs */
   int prefetch_kb[6];  /* per kind: next-tile K blocks prefetched into L2 */
   float us[6];         /* per kind: measured microseconds per launch of the choice */
+  int tile_order[6];   /* per kind: tile order (kinds 4, 5; 0 for the others) */
+  int stages[6];       /* per kind: pipeline stages in use */
+  int epi_direct[6];   /* per kind: 1 = direct epilogue stores (kinds 1, 3, 4, 5) */
+  int fwd_megakernel;  /* 1: the forward MegaKernel measured faster than the kernel chain */
+  int bwd_megakernel;  /* 1: the backward input-part MegaKernel measured faster */
+  float fwd_us[2];     /* forward per call: kernel chain, MegaKernel (microseconds) */
+  float bwd_us[2];     /* backward per call: kernel chain, MegaKernel */
 } moe_tune_result;
 
 int moe_autotune(const moe_cfg* cfg, const float* logits, const uint16_t* x,

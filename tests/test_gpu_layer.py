@@ -167,18 +167,35 @@ def test_cta_pair_tiles_equal_single_cta_tiles_bitwise(cfg):
 def _gemm_settings():
     mask = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
     moe.moe_set_gemm_pair_kinds(mask)
-    depths = []
+    depths, stages, orders, epis = [], [], [], []
     for k in range(len(moe.GEMM_KINDS)):
         depths.append(moe.moe_set_gemm_prefetch(k, 0))
         moe.moe_set_gemm_prefetch(k, depths[-1])
-    return mask, depths
+        stages.append(moe.moe_set_gemm_stages(k, 0))
+        moe.moe_set_gemm_stages(k, stages[-1])
+    for k in (4, 5):
+        orders.append(moe.moe_set_gemm_tile_order(k, 0))
+        moe.moe_set_gemm_tile_order(k, orders[-1])
+    for k in FP32_KINDS:
+        epis.append(moe.moe_set_gemm_epilogue(k, 0))
+        moe.moe_set_gemm_epilogue(k, epis[-1])
+    return mask, depths, stages, orders, epis
+
+
+FP32_KINDS = (1, 3, 4, 5)  # GEMM 2, dX, dW1/dW3, dW2: fp32 outputs
 
 
 def _restore_gemm_settings(saved):
-    mask, depths = saved
+    mask, depths, stages, orders, epis = saved
+    for k, e in zip(FP32_KINDS, epis):
+        moe.moe_set_gemm_epilogue(k, e)
     moe.moe_set_gemm_pair_kinds(mask)
     for k, d in enumerate(depths):
         moe.moe_set_gemm_prefetch(k, d)
+    for k, n in enumerate(stages):
+        moe.moe_set_gemm_stages(k, n)
+    for k, o in zip((4, 5), orders):
+        moe.moe_set_gemm_tile_order(k, o)
 
 
 @pytest.mark.parametrize("depth", [4, 16])
@@ -199,10 +216,12 @@ def test_next_tile_l2_prefetch_keeps_bits(depth):
         assert torch.equal(a[k], b[k]), k
 
 
-def test_autotune_chooses_per_kind_and_keeps_bits():
+@pytest.mark.parametrize("cfg", [MID, SKEW], ids=lambda c: c.name)
+def test_autotune_chooses_per_kind_and_keeps_bits(cfg):
     """The measured autotuner returns a valid choice for every grouped-GEMM
-    kind, applies it, and the layer's outputs afterwards are the same bits."""
-    cfg = MID
+    kind (tile shape, prefetch depth, tile order, stages) and the forward and
+    backward variant, applies the GEMM choices, and the layer's outputs
+    afterwards are the same bits as the oracle-checked defaults'."""
     g = to_dev(make_layer_inputs(cfg, seed=19))
     saved = _gemm_settings()
     try:
@@ -211,18 +230,58 @@ def test_autotune_chooses_per_kind_and_keeps_bits():
         o = empty_outputs(cfg)
         res = moe.moe_autotune(cfg, g["logits"], g["x"], g["W1"], g["W3"], g["W2"], g["dy"], o["y"], o["topk_idx"],
                                o["topk_w"], o["dx"], o["dlogits"], o["dW1"], o["dW3"], o["dW2"], ws)
-        assert set(res) == set(moe.GEMM_KINDS)
-        for name, (pair, depth, us) in res.items():
-            assert pair in (0, 1) and depth in (0, 4, 8) and us > 0, (name, pair, depth, us)
-        mask, depths = _gemm_settings()
-        assert mask == sum(res[n][0] << i for i, n in enumerate(moe.GEMM_KINDS))
-        assert depths == [res[n][1] for n in moe.GEMM_KINDS]
+        kinds = res["kinds"]
+        assert set(kinds) == set(moe.GEMM_KINDS)
+        for i, (name, c) in enumerate(kinds.items()):
+            top = moe.moe_gemm_max_stages(i, 2 if c["pair"] else 1)
+            assert c["pair"] in (0, 1) and c["prefetch_kb"] in (0, 4, 8) and c["us"] > 0, (name, c)
+            assert c["tile_order"] in ((0, 1) if i >= 4 else (0,)) and top - 1 <= c["stages"] <= top, (name, c)
+        assert res["fwd_megakernel"] in (0, 1) and res["bwd_megakernel"] in (0, 1)
+        assert min(res["fwd_us"] + res["bwd_us"]) > 0, res
+        mask, depths, stages, orders, epis = _gemm_settings()
+        assert epis == [kinds[moe.GEMM_KINDS[k]]["epi_direct"] for k in FP32_KINDS]
+        assert mask == sum(kinds[n]["pair"] << i for i, n in enumerate(moe.GEMM_KINDS))
+        assert depths == [kinds[n]["prefetch_kb"] for n in moe.GEMM_KINDS]
+        assert orders == [kinds["dw13"]["tile_order"], kinds["dw2"]["tile_order"]]
         tuned, ws2 = run_layer(cfg, g, fill=float("nan"))
     finally:
         _restore_gemm_settings(saved)
     assert device_error(ws2) == (0, 0)
     for k in ref:
         assert torch.equal(ref[k], tuned[k]), k
+
+
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_tile_order_stage_count_and_epilogue_stores_keep_bits(cfg):
+    """The interleaved weight-gradient tile order, fewer pipeline stages (one
+    less than fits, and two) and the direct (unstaged) epilogue stores of the
+    fp32-output kinds, on both tile shapes, give the same bits: they change
+    which CTA computes a tile, when, and how its results travel to memory,
+    never the arithmetic.  The shapes include partial last tiles of every
+    kind, so the direct stores' row and column limits are exercised."""
+    g = to_dev(make_layer_inputs(cfg, seed=25))
+    saved = _gemm_settings()
+    try:
+        ref, ref_ws = run_layer(cfg, g)
+        ref = {k: v.clone() for k, v in ref.items()}
+        for mask in (moe.ALL_PAIR_KINDS, 0):
+            moe.moe_set_gemm_pair_kinds(mask)
+            for order, stages, epi in ((1, 0, 0), (0, -1, 1), (1, 2, 1), (0, 0, 1)):
+                for k in (4, 5):
+                    moe.moe_set_gemm_tile_order(k, order)
+                for k in FP32_KINDS:
+                    moe.moe_set_gemm_epilogue(k, epi)
+                for k in range(len(moe.GEMM_KINDS)):
+                    top = moe.moe_gemm_max_stages(k, 2 if mask else 1)
+                    moe.moe_set_gemm_stages(k, top - 1 if stages < 0 else stages)
+                out, ws = run_layer(cfg, g, fill=float("nan"))
+                assert device_error(ws) == (0, 0)
+                for k in ref:
+                    assert torch.equal(ref[k], out[k]), (mask, order, stages, epi, k)
+                for name in ("Op", "dXp"):
+                    assert torch.equal(moe.ws_view(ws, cfg, name), moe.ws_view(ref_ws, cfg, name)), name
+    finally:
+        _restore_gemm_settings(saved)
 
 
 @pytest.mark.parametrize("cfg", [MID, SKEW], ids=lambda c: c.name)
