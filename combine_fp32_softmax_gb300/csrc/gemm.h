@@ -54,6 +54,8 @@ int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_overr
 // Bit k set: kind k runs on CTA pairs (256-row tiles); clear: one CTA per
 // 128-row tile.  Returns the previous mask.
 int set_gemm_pair_kinds(int mask);
+// The current mask (as set_gemm_pair_kinds).
+int gemm_pair_kinds();
 
 // K blocks of each CTA's next tile that kind `kind` prefetches into L2 while
 // loading the current one (0 = none, at most 64).  Returns the previous

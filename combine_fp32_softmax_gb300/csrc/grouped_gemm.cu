@@ -336,6 +336,8 @@ int gemm_max_stages(GemmKind kind, int cta_group) {
   return 0;
 }
 
+int gemm_pair_kinds() { return g_pair_kinds; }
+
 int set_gemm_pair_kinds(int mask) {
   const int prev = g_pair_kinds;
   g_pair_kinds = mask & ((1 << 6) - 1);

@@ -33,6 +33,8 @@
 // grouped GEMM kernels and the token sums add in the same order as the
 // stand-alone sum kernel, so the outputs are bitwise equal to the unfused
 // chain.
+#include <algorithm>
+
 #include "gemm_tiles.cuh"
 
 namespace moe {
@@ -42,7 +44,7 @@ constexpr int kTq = 4;              // depth of the producer -> consumer task FI
 
 constexpr int kCtrXp = 8;
 constexpr int kMaxTokRows = 12;     // k <= 8 routed + S <= 4 shared rows per token
-constexpr int kMaxMegaStages = 4;
+constexpr int kMaxMegaStages = kMaxStages;
 
 struct MegaParams {
   GemmParams g1, g2;           // first (A) and second (B) grouped GEMM
@@ -80,12 +82,16 @@ __device__ __forceinline__ void trace_record(const MegaParams& mp, int role, int
   ++n;
 }
 
-// Shapes of one MegaKernel: its two GEMM kinds and its pipeline depth
-// (forward 4 stages of 48 KB; backward 3, as a fourth does not fit beside
-// dH's 12 KB a warp of epilogue staging).
-template <int KA, int KB, int NST>
+// Shapes of one MegaKernel: its two GEMM kinds, its pipeline depth and its
+// CTA group.  One CTA per tile: forward 4 stages of 48 KB, backward 3 (a
+// fourth does not fit beside dH's 12 KB a warp of epilogue staging).  CTA
+// pairs (256-row tiles, tcgen05 CTA group of two, as the stand-alone grouped
+// GEMMs run by default): 32 KB stages, forward 6, backward 5.
+template <int KA, int KB, int NST, int CG = 1>
 struct Mega {
   static constexpr int STAGES = NST;
+  static constexpr int STAGE_BYTES = Pipe<KA, CG>::STAGE_BYTES;
+  static_assert(Pipe<KA, CG>::STAGE_BYTES == Pipe<KB, CG>::STAGE_BYTES, "both GEMMs share the ring");
   // epilogue staging per warp: the larger of the two kinds'
   static constexpr int EPI_BYTES =
       Traits<KA>::EPI_BYTES > Traits<KB>::EPI_BYTES ? Traits<KA>::EPI_BYTES : Traits<KB>::EPI_BYTES;
@@ -98,12 +104,15 @@ struct MegaShared {
   int ntn1, ntn2, nt1, nt2, total;
 };
 
-template <int KA, int KB, int NST>
+template <int KA, int KB, int NST, int CG = 1>
 constexpr int mega_smem_bytes() {
-  return NST * kStageBytes + kEpiWarps * Mega<KA, KB, NST>::EPI_BYTES + static_cast<int>(sizeof(MegaShared));
+  return NST * Mega<KA, KB, NST, CG>::STAGE_BYTES + kEpiWarps * Mega<KA, KB, NST, CG>::EPI_BYTES +
+         static_cast<int>(sizeof(MegaShared));
 }
 static_assert(mega_smem_bytes<kG1, kG2, 4>() <= 232448, "shared memory budget of one CTA");
 static_assert(mega_smem_bytes<kDH, kDX, 3>() <= 232448, "shared memory budget of one CTA");
+static_assert(mega_smem_bytes<kG1, kG2, 6, 2>() <= 232448, "shared memory budget of one CTA");
+static_assert(mega_smem_bytes<kDH, kDX, 5, 2>() <= 232448, "shared memory budget of one CTA");
 
 // Bounded acquire-spin until *c >= target.
 __device__ bool wait_counter(const int* c, int target, volatile int* abort, int* err, int where) {
@@ -141,21 +150,27 @@ struct GatherState {
   uint32_t pending = 0;  // buffers with loads issued but not yet waited on
 };
 
-template <int NST>
+// With CTA pairs each CTA of the pair gathers its half of the block (`part`
+// of `nparts`) and signals the block's counter once (a block is complete
+// at nparts signals).
+template <int NST, int SB>
 __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem, int g, GatherState& gs,
-                            volatile int* abort, int where) {
+                            volatile int* abort, int where, int part = 0, int nparts = 1) {
   const int d = mp.g1.d;
   const uint32_t rb = 2u * d;
-  const int rps = min(mp.grows, kStageBytes / static_cast<int>(rb));
-  const int r0 = g * mp.grows;
-  const int nrows = min(mp.grows, mp.g1.R - r0);
+  const int rps = min(mp.grows, SB / static_cast<int>(rb));  // >= 1: checked on the host
+  const int blk0 = g * mp.grows;
+  const int blk_rows = min(mp.grows, mp.g1.R - blk0);
+  const int per = (blk_rows + nparts - 1) / nparts;
+  const int r0 = blk0 + min(blk_rows, part * per);
+  const int nrows = min(blk_rows, (part + 1) * per) - min(blk_rows, part * per);
   const int nchunk = (nrows + rps - 1) / rps;
   for (int c = 0; c <= nchunk; ++c) {
     if (c < nchunk) {
       const int b = c % NST;
       if (c >= NST) bulk_wait_read<NST - 2>();  // chunk c-NST finished reading buffer b
       const int n = min(rps, nrows - c * rps);
-      uint8_t* buf = smem + b * kStageBytes;
+      uint8_t* buf = smem + b * SB;
       mbar_arrive_expect_tx(&ms.gbar[b], n * rb);
       for (int i = 0; i < n; ++i) {
         int tok = mp.row_token[r0 + c * rps + i];
@@ -172,7 +187,7 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
       gs.par ^= 1u << b;
       gs.pending &= ~(1u << b);
       const int n = min(rps, nrows - pc * rps);
-      uint8_t* buf = smem + b * kStageBytes;
+      uint8_t* buf = smem + b * SB;
       // the chunk's destination rows are consecutive: one bulk store
       bulk_store(mp.Xp + static_cast<size_t>(r0 + pc * rps) * d, buf, n * rb);
       bulk_commit();
@@ -192,10 +207,10 @@ __device__ void gather_drain(MegaShared& ms, const GatherState& gs) {
 
 // Tile t2 of the second GEMM described with the first one's segment table
 // (both run over the same rows, so they share m-tiles).
-template <int KA, int KB>
-__device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaShared& ms, int t2) {
+template <int KA, int KB, int CG = 1>
+__device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaShared& ms, int t2, int rank = 0) {
   const int mt = t2 / ms.ntn2, nb = t2 - mt * ms.ntn2;
-  TileInfo t = decode_tile<KA>(mp.g1, ms.g, mt * ms.ntn1);
+  TileInfo t = decode_tile<KA, CG>(mp.g1, ms.g, mt * ms.ntn1, rank);
   t.n0 = nb * Traits<KB>::BNE;
   t.nkb = mp.g2.K / kBK;
   return t;
@@ -253,11 +268,11 @@ __device__ void combine_token(const MegaParams& mp, int t) {
 // space is done: after all GEMM-2 tiles are published, warps claim single
 // tokens from their own cursor (ctr[2]) until none are left, so the work
 // balances across all warps whatever the tickets each CTA ended up with.
-__device__ void combine_phase(const MegaParams& mp, int nt2, volatile int* abort, int* err) {
+__device__ void combine_phase(const MegaParams& mp, int nt2, int cg, volatile int* abort, int* err) {
   const int lane = threadIdx.x & 31;
   int ok = 1;
   if (lane == 0) {
-    ok = wait_counter(&mp.ctr[1], kEpiWarps * nt2, abort, err, (0x0F << 24) | (5 << 20)) ? 1 : 0;
+    ok = wait_counter(&mp.ctr[1], kEpiWarps * cg * nt2, abort, err, (0x0F << 24) | (5 << 20)) ? 1 : 0;
     __threadfence();
   }
   if (!__shfl_sync(0xffffffffu, ok, 0)) return;
@@ -270,34 +285,67 @@ __device__ void combine_phase(const MegaParams& mp, int nt2, volatile int* abort
   }
 }
 
-template <int KA, int KB, int NST>
+// Task FIFO of a CTA pair: the even CTA's producer claims each ticket and
+// writes it to both CTAs' rings; every other role of both CTAs (the odd
+// CTA's producer too) reads it and releases the slot on the even CTA's ring.
+template <int CG>
+__device__ __forceinline__ bool tq_put(MegaShared& ms, int slot, int id) {
+  ms.tq[slot] = id;
+  if constexpr (CG == 2) {
+    st_shared_rank(&ms.tq[slot], 1, id);
+    mbar_arrive_rank(&ms.tq_full[slot], 1);  // release at cluster scope: the store above is seen first
+  }
+  mbar_arrive(&ms.tq_full[slot]);
+  return true;
+}
+template <int CG>
+__device__ __forceinline__ int tq_get(MegaShared& ms, int slot, uint32_t par, int rank, volatile int* abort, int* err,
+                                      int where, bool* ok) {
+  *ok = mbar_wait<CG == 2>(&ms.tq_full[slot], par, abort, err, where);
+  if (!*ok) return 0;
+  const int id = *reinterpret_cast<volatile int*>(&ms.tq[slot]);
+  __syncwarp(__activemask());
+  if (lane_id() == 0) {
+    if (CG == 2 && rank != 0)
+      mbar_arrive_rank(&ms.tq_empty[slot], 0);
+    else
+      mbar_arrive(&ms.tq_empty[slot]);
+  }
+  return id;
+}
+
+template <int KA, int KB, int NST, int CG>
 __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant__ MegaParams mp) {
-  constexpr int EPI = Mega<KA, KB, NST>::EPI_BYTES;
+  constexpr int EPI = Mega<KA, KB, NST, CG>::EPI_BYTES;
+  constexpr int SB = Mega<KA, KB, NST, CG>::STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023) {  // see grouped_gemm_kernel: checked, not padded
     if (threadIdx.x == 0) record_error(mp.g1.err, MOE_ERR_CUDA, 0x5A11);
     return;
   }
   uint8_t* smem = smem_raw;
-  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + NST * kStageBytes + kEpiWarps * EPI);
+  MegaShared& ms = *reinterpret_cast<MegaShared*>(smem + NST * SB + kEpiWarps * EPI);
   SharedState& ss = ms.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
   int* err = mp.g1.err;
 
   if (threadIdx.x == 0) {
-    init_gemm_barriers(ss);
+    init_gemm_barriers<CG>(ss);
     for (int q = 0; q < kTq; ++q) {
       mbar_init(&ms.tq_full[q], 1);
-      mbar_init(&ms.tq_empty[q], 1 + kEpiWarps);  // MMA warp + epilogue warps
+      // readers of a slot: MMA warp + epilogue warps (of both CTAs of a pair,
+      // plus the odd CTA's producer)
+      mbar_init(&ms.tq_empty[q], CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 1 + kEpiWarps);
     }
     for (int b = 0; b < NST; ++b) mbar_init(&ms.gbar[b], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ss.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(&ss.tmem_base, kTmemCols);
+    tmem_relinquish<CG>();
   }
-  build_segments<KA>(mp.g1, ss);
+  build_segments<KA, CG>(mp.g1, ss);
   if (threadIdx.x == 0) {
     ms.ntn1 = (mp.g1.N + Traits<KA>::BNE - 1) / Traits<KA>::BNE;
     ms.ntn2 = (mp.g2.N + Traits<KB>::BNE - 1) / Traits<KB>::BNE;
@@ -307,12 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anything arrives on them
   tc_fence_after();
   const uint32_t tmem = ss.tmem_base;
   volatile int* abort = &ss.abort;
   const int NG = mp.NG, nt1 = ms.nt1, nt2 = ms.nt2, total = ms.total;
   const int e1 = NG + nt1, e2 = NG + nt1 + nt2;  // ends of the GEMM-1 and GEMM-2 ticket ranges
   constexpr int kW = 0x0F << 24;
+  // signals that complete a readiness counter: one per epilogue warp of the
+  // tile's CTAs (per first-GEMM n-tile for the m-tile counters)
+  constexpr int kTileSignals = kEpiWarps * CG;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -325,11 +377,19 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       int slot = 0, tn = 0;
       uint32_t tph = 0;
       while (!*abort) {
-        if (!mbar_wait(&ms.tq_empty[slot], tph ^ 1, abort, err, kW | (1 << 20))) break;
-        const int id = atomicAdd(&mp.ctr[0], 1);
-        const uint64_t t_claim = globaltimer_ns();
-        ms.tq[slot] = id;
-        mbar_arrive(&ms.tq_full[slot]);
+        int id;
+        uint64_t t_claim;
+        if (rank == 0) {
+          if (!mbar_wait<CG == 2>(&ms.tq_empty[slot], tph ^ 1, abort, err, kW | (1 << 20))) break;
+          id = atomicAdd(&mp.ctr[0], 1);
+          t_claim = globaltimer_ns();
+          tq_put<CG>(ms, slot, id);
+        } else {
+          bool ok;
+          id = tq_get<CG>(ms, slot, tph, rank, abort, err, kW | (1 << 20), &ok);
+          if (!ok) break;
+          t_claim = globaltimer_ns();
+        }
         if (++slot == kTq) {
           slot = 0;
           tph ^= 1;
@@ -338,23 +398,25 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
         if (id == mp.skip) continue;
         const int where = kW | (1 << 20) | (id & 0xFFFFF);
         if (id < NG) {
-          if (!gather_task<NST>(mp, ms, smem, id, gs, abort, where)) break;
+          if (!gather_task<NST, SB>(mp, ms, smem, id, gs, abort, where, rank, CG)) break;
         } else if (id < e1) {
-          const TileInfo t = decode_tile<KA>(mp.g1, ss, id - NG);
-          if (!t.shared) {  // routed rows come from the gathered rows: wait for their blocks
+          const TileInfo t = decode_tile<KA, CG>(mp.g1, ss, id - NG, rank);
+          if (t.active && !t.shared) {  // routed rows come from the gathered rows: wait for their blocks
             const int g0 = t.grow0 / mp.grows, g1 = (t.grow0 + t.rows - 1) / mp.grows;
             bool ok = true;
-            for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], 1, abort, err, where);
+            for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], CG, abort, err, where);
             if (!ok) break;
             fence_proxy_async_global();
           }
-          if (!produce_tile<KA>(mp.g1, t, ss, smem, ps, abort, where, NST)) break;
+          if (!produce_tile<KA, CG>(mp.g1, t, ss, smem, ps, abort, where, NST, rank)) break;
         } else if (id < e2) {
           const int t2 = id - e1;
           const int mt = t2 / ms.ntn2;
-          if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kEpiWarps * ms.ntn1, abort, err, where)) break;
+          if (!wait_counter(&mp.ctr[kCtrXp + NG + mt], kTileSignals * ms.ntn1, abort, err, where)) break;
           fence_proxy_async_global();
-          if (!produce_tile<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, t2), ss, smem, ps, abort, where, NST)) break;
+          if (!produce_tile<KB, CG>(mp.g2, decode_g2<KA, KB, CG>(mp, ms, t2, rank), ss, smem, ps, abort, where, NST,
+                                    rank))
+            break;
         }
         trace_record(mp, 0, tn, id, t_claim);
       }
@@ -364,16 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       }
     }
     __syncwarp();
-    if (!*abort) combine_phase(mp, nt2, abort, err);
+    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
   } else if (warp == 1) {
     MmaState mst;
     int slot = 0;
     uint32_t tph = 0;
     while (true) {
-      if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (2 << 20))) break;
-      const int id = ms.tq[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms.tq_empty[slot]);
+      bool ok;
+      const int id = tq_get<CG>(ms, slot, tph, rank, abort, err, kW | (2 << 20), &ok);
+      if (!ok) break;
       if (++slot == kTq) {
         slot = 0;
         tph ^= 1;
@@ -381,26 +442,26 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       if (id >= total) break;
       if (id == mp.skip) continue;
       const int where = kW | (2 << 20) | (id & 0xFFFFF);
-      bool ok = true;
       if (id >= NG && id < e1)
-        ok = mma_tile<KA>(mp.g1, decode_tile<KA>(mp.g1, ss, id - NG), ss, smem, tmem, mst, abort, where, NST);
+        ok = mma_tile<KA, CG>(mp.g1, decode_tile<KA, CG>(mp.g1, ss, id - NG, rank), ss, smem, tmem, mst, abort, where,
+                              NST, rank);
       else if (id >= e1 && id < e2)
-        ok = mma_tile<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, smem, tmem, mst, abort, where, NST);
+        ok = mma_tile<KB, CG>(mp.g2, decode_g2<KA, KB, CG>(mp, ms, id - e1, rank), ss, smem, tmem, mst, abort, where,
+                              NST, rank);
       if (!ok) break;
     }
-    if (*abort) mma_drain(ss, mst);
-    if (!*abort) combine_phase(mp, nt2, abort, err);
+    if (*abort) mma_drain<CG>(ss, mst);
+    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
   } else {
     EpiState es;
-    uint8_t* stg = smem + NST * kStageBytes + (warp & 3) * EPI;
+    uint8_t* stg = smem + NST * SB + (warp & 3) * EPI;
     int slot = 0, tn = 0;
     uint32_t tph = 0;
     while (true) {
-      if (!mbar_wait(&ms.tq_full[slot], tph, abort, err, kW | (3 << 20))) break;
-      const int id = ms.tq[slot];
+      bool ok;
+      const int id = tq_get<CG>(ms, slot, tph, rank, abort, err, kW | (3 << 20), &ok);
+      if (!ok) break;
       const uint64_t t_pop = globaltimer_ns();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms.tq_empty[slot]);
       if (++slot == kTq) {
         slot = 0;
         tph ^= 1;
@@ -410,34 +471,75 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       const int where = kW | (3 << 20) | (id & 0xFFFFF);
       if (id >= NG && id < e1) {
         const int t1 = id - NG;
-        if (!epilogue_step<KA>(mp.g1, decode_tile<KA>(mp.g1, ss, t1), ss, tmem, stg, es, abort, where)) break;
+        if (!epilogue_step<KA, CG>(mp.g1, decode_tile<KA, CG>(mp.g1, ss, t1, rank), ss, tmem, stg, es, abort, where,
+                                   rank))
+          break;
         warp_signal(&mp.ctr[kCtrXp + NG + t1 / ms.ntn1]);
       } else if (id >= e1 && id < e2) {
-        if (!epilogue_step<KB>(mp.g2, decode_g2<KA, KB>(mp, ms, id - e1), ss, tmem, stg, es, abort, where)) break;
+        if (!epilogue_step<KB, CG>(mp.g2, decode_g2<KA, KB, CG>(mp, ms, id - e1, rank), ss, tmem, stg, es, abort,
+                                   where, rank))
+          break;
         warp_signal(&mp.ctr[1]);
       }
       if (warp == 2 && lane == 0) trace_record(mp, 1, tn, id, t_pop);
     }
     epilogue_drain(ss, es);
-    if (!*abort) combine_phase(mp, nt2, abort, err);
+    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
   }
 
   tc_fence_before();
   __syncthreads();
+  // No CTA of a pair leaves (or frees TMEM) while the other may still arrive
+  // on its barriers or have MMAs read its shared memory.
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
 }
 
-// Launches MegaKernel <KA, KB, NST> with the two GEMMs' arguments `a`
-// (filled for both kinds), the gather (src rows by row_token into dst) and
-// the token sums (rows of ssrc by dest, into sdst).
+// Pairs of MegaKernel <KA, KB, NST, 2> resident at once (cached; 0 if the
+// query fails).
 template <int KA, int KB, int NST>
+int mega_pair_capacity() {
+  static int cached = -1;
+  if (cached < 0) {
+    auto kern = mega_kernel<KA, KB, NST, 2>;
+    constexpr int kSmem = mega_smem_bytes<KA, KB, NST, 2>();
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+      n = 0;
+    cached = n;
+  }
+  return cached;
+}
+
+// Launches MegaKernel <KA, KB, NST, CG> with the two GEMMs' arguments `a`
+// (filled for both kinds), the gather (src rows by row_token into dst) and
+// the token sums (rows of ssrc by dest, into sdst).  CG = 2 launches clusters
+// of two (as many pairs as are resident at once, fewer under a grid cap).
+template <int KA, int KB, int NST, int CG>
 int mega_launch(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs& a, const uint16_t* gsrc,
                 uint16_t* gdst, const float* ssrc, float* sdst, int grid, int trace_kind, cudaStream_t s) {
   MegaParams mp;
   std::memset(&mp, 0, sizeof(mp));
-  if (!fill_params<KA>(a, mp.g1) || !fill_params<KB>(a, mp.g2)) return MOE_ERR_CUDA;
+  if (!fill_params<KA, CG>(a, mp.g1) || !fill_params<KB, CG>(a, mp.g2)) return MOE_ERR_CUDA;
+  // the whole ring, one CTA per SM (the grouped GEMMs' stage-count and
+  // epilogue knobs do not apply here)
+  mp.g1.nst = mp.g2.nst = NST;
   const long long R = static_cast<long long>(c.T) * c.k;
+  // a gathered row must fit a ring stage
+  if (2ll * c.d_model > Mega<KA, KB, NST, CG>::STAGE_BYTES) return MOE_ERR_SHAPE;
   mp.x = gsrc;
   mp.row_token = reinterpret_cast<const int32_t*>(ws + L.row_token);
   mp.dest = reinterpret_cast<const int32_t*>(ws + L.dest);
@@ -456,13 +558,40 @@ int mega_launch(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs
   const long long need = kCtrXp + mp.NG + R / kBM + c.E + static_cast<long long>(c.n_shared) * ceil_div(c.T, kBM) + 2;
   if (need > L.mk_ints) return MOE_ERR_SHAPE;
   if (cudaMemsetAsync(mp.ctr, 0, sizeof(int) * L.mk_ints, s) != cudaSuccess) return MOE_ERR_CUDA;
-  constexpr int kSmem = mega_smem_bytes<KA, KB, NST>();
-  if (cudaFuncSetAttribute(mega_kernel<KA, KB, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-      cudaSuccess)
+  constexpr int kSmem = mega_smem_bytes<KA, KB, NST, CG>();
+  auto kern = mega_kernel<KA, KB, NST, CG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return MOE_ERR_CUDA;
+  int nblocks = grid > 0 ? grid : num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  if constexpr (CG == 2) {
+    const int cap = mega_pair_capacity<KA, KB, NST>();
+    if (cap <= 0) return MOE_ERR_CUDA;
+    nblocks = 2 * std::max(1, std::min(cap, nblocks / 2));
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cfg.gridDim = dim3(nblocks);
   TraceScope trace_scope(trace_kind, s);
-  mega_kernel<KA, KB, NST><<<grid > 0 ? grid : num_sms(), kThreads, kSmem, s>>>(mp);
+  if (cudaLaunchKernelEx(&cfg, kern, mp) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// CTA pairs when both of the MegaKernel's GEMM kinds run on pairs as
+// stand-alone kernels (moe_set_gemm_pair_kinds) and pairs can be resident.
+template <int KA, int KB, int NST2>
+bool mega_uses_pairs(int d) {
+  const int mask = gemm_pair_kinds();
+  return ((mask >> KA) & 1) && ((mask >> KB) & 1) && 2 * d <= Mega<KA, KB, NST2, 2>::STAGE_BYTES &&
+         mega_pair_capacity<KA, KB, NST2>() > 0;
 }
 
 }  // namespace
@@ -489,14 +618,20 @@ int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint1
   a.AB_out = reinterpret_cast<uint16_t*>(ws + L.AB);
   a.Op_out = reinterpret_cast<float*>(ws + L.Op);
   a.err = reinterpret_cast<int*>(ws + L.err);
-  return mega_launch<kG1, kG2, 4>(c, L, ws, a, x, reinterpret_cast<uint16_t*>(ws + L.Xp),
-                                  reinterpret_cast<const float*>(ws + L.Op), y, grid, MOE_K_MEGAKERNEL, s);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(ws + L.Xp);
+  const float* Op = reinterpret_cast<const float*>(ws + L.Op);
+  if (mega_uses_pairs<kG1, kG2, 6>(c.d_model))
+    return mega_launch<kG1, kG2, 6, 2>(c, L, ws, a, x, Xp, Op, y, grid, MOE_K_MEGAKERNEL, s);
+  return mega_launch<kG1, kG2, 4, 1>(c, L, ws, a, x, Xp, Op, y, grid, MOE_K_MEGAKERNEL, s);
 }
 
 int megakernel_bwd_input(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const GemmArgs& a, const uint16_t* dy,
                          float* dx, int grid, cudaStream_t s) {
-  return mega_launch<kDH, kDX, 3>(c, L, ws, a, dy, reinterpret_cast<uint16_t*>(ws + L.G),
-                                  reinterpret_cast<const float*>(ws + L.dXp), dx, grid, MOE_K_MEGAKERNEL_BWD, s);
+  uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.G);
+  const float* dXp = reinterpret_cast<const float*>(ws + L.dXp);
+  if (mega_uses_pairs<kDH, kDX, 5>(c.d_model))
+    return mega_launch<kDH, kDX, 5, 2>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
+  return mega_launch<kDH, kDX, 3, 1>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
 }
 
 }  // namespace moe

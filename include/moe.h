@@ -208,7 +208,12 @@ int moe_combine(const moe_cfg* cfg, const float* Oprime, const int32_t* dest,
  * runs dispatch..combine as one persistent launch that claims tasks from an
  * atomic ticket counter and orders them with device-side readiness counters
  * (UniEP page, section 2.2: persistent workers, scoreboard, dynamic SM
- * scheduling); its outputs are bitwise equal to use_megakernel = 0.
+ * scheduling); its outputs are bitwise equal to use_megakernel = 0.  Its
+ * tiles run on CTA pairs like the stand-alone GEMMs (see
+ * moe_set_gemm_pair_kinds): the pair's even CTA claims each ticket and
+ * hands it to the odd one, and the pair splits each gather task.
+ * use_megakernel = 1 needs d_model <= 24576 (a gathered row fits a pipeline
+ * stage; MOE_ERR_SHAPE otherwise).
  * Route and the permutation tables run as one cooperative launch with grid
  * barriers between histogram, scan and scatter (see moe_set_route_fusion). */
 int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x,
@@ -332,8 +337,11 @@ int moe_set_bwd_overlap(int on);
  * 0 GEMM 1 (gate/up), 1 GEMM 2 (down), 2 dH, 3 dX, 4 dW1/dW3, 5 dW2.  The
  * default is all six, what measures fastest on a DeepSeek-V2-Lite-like
  * layer (T=8192, d=2048, f=1408, E=64, k=6, S=2); moe_autotune picks per
- * layer.  Results are the same bits either way: every output element is the
- * same fp32 sum over K in the same order.  Returns the previous mask.
+ * layer.  The MegaKernels follow it: the forward one runs on CTA pairs when
+ * bits 0 and 1 are set, the backward one when bits 2 and 3 are (and a row
+ * of d_model bf16 fits a 32 KB pipeline stage), else one CTA per tile.
+ * Results are the same bits either way: every output element is the same
+ * fp32 sum over K in the same order.  Returns the previous mask.
  * Process-wide, not thread-safe. */
 int moe_set_gemm_pair_kinds(int mask);
 
