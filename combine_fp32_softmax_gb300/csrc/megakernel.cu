@@ -97,9 +97,14 @@ struct Mega {
       Traits<KA>::EPI_BYTES > Traits<KB>::EPI_BYTES ? Traits<KA>::EPI_BYTES : Traits<KB>::EPI_BYTES;
 };
 
+// Token sums after the GEMMs: each warp stages the rows of one (token,
+// column span) unit in its own 32 KB of the then idle pipeline ring.
+constexpr int kSumWarps = kThreads / 32;
+constexpr int kSumBytes = 32 * 1024;
+
 struct MegaShared {
   SharedState g;
-  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kMaxMegaStages];
+  uint64_t tq_full[kTq], tq_empty[kTq], gbar[kMaxMegaStages], sbar[kSumWarps];
   int tq[kTq];
   int ntn1, ntn2, nt1, nt2, total;
 };
@@ -113,6 +118,15 @@ static_assert(mega_smem_bytes<kG1, kG2, 4>() <= 232448, "shared memory budget of
 static_assert(mega_smem_bytes<kDH, kDX, 3>() <= 232448, "shared memory budget of one CTA");
 static_assert(mega_smem_bytes<kG1, kG2, 6, 2>() <= 232448, "shared memory budget of one CTA");
 static_assert(mega_smem_bytes<kDH, kDX, 5, 2>() <= 232448, "shared memory budget of one CTA");
+// the token sums' staging fits the ring and epilogue staging of every shape
+template <int KA, int KB, int NST, int CG>
+constexpr bool sum_staging_fits() {
+  return NST * Mega<KA, KB, NST, CG>::STAGE_BYTES + kEpiWarps * Mega<KA, KB, NST, CG>::EPI_BYTES >=
+         kSumWarps * kSumBytes;
+}
+static_assert(sum_staging_fits<kG1, kG2, 4, 1>() && sum_staging_fits<kDH, kDX, 3, 1>() &&
+                  sum_staging_fits<kG1, kG2, 6, 2>() && sum_staging_fits<kDH, kDX, 5, 2>(),
+              "token-sum staging");
 
 // Bounded acquire-spin until *c >= target.
 __device__ bool wait_counter(const int* c, int target, volatile int* abort, int* err, int where) {
@@ -216,72 +230,71 @@ __device__ __forceinline__ TileInfo decode_g2(const MegaParams& mp, const MegaSh
   return t;
 }
 
-// Sum of one token's rows by one warp: the same fp32 sum, in the same order,
-// as the stand-alone sum kernel.
-__device__ void combine_token(const MegaParams& mp, int t) {
-  const int lane = threadIdx.x & 31;
-  const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R;
-  const int nr = k + S, nvec = mp.g1.d / 4;
-  const float4* rows = reinterpret_cast<const float4*>(mp.Op);
-  {
-    long long myrow = 0;
-    if (lane < k) {
-      myrow = mp.dest[static_cast<size_t>(t) * k + lane];
-      if (!debug_ok(myrow >= 0 && myrow < R, mp.g1.err, kDbgMegaCombine, t)) myrow = 0;
-    } else if (lane < nr)
-      myrow = R + static_cast<long long>(lane - k) * T + t;
-    const float4* base[kMaxTokRows];
-#pragma unroll
-    for (int j = 0; j < kMaxTokRows; ++j) base[j] = rows + static_cast<size_t>(__shfl_sync(0xffffffffu, myrow, j)) * nvec;
-    float4* o = reinterpret_cast<float4*>(mp.y) + static_cast<size_t>(t) * nvec;
-    // two vectors per lane per step: twice the loads in flight for the few
-    // warps that run combine tasks; each element is summed in slot order.
-    for (int v = lane; v < nvec; v += 64) {
-      const bool two = v + 32 < nvec;
-      float4 val[kMaxTokRows], val2[kMaxTokRows];
-#pragma unroll
-      for (int j = 0; j < kMaxTokRows; ++j)
-        if (j < nr) {
-          val[j] = base[j][v];
-          if (two) val2[j] = base[j][v + 32];
-        }
-      float4 acc = val[0], acc2 = val2[0];
-#pragma unroll
-      for (int j = 1; j < kMaxTokRows; ++j)
-        if (j < nr) {
-          acc.x += val[j].x;
-          acc.y += val[j].y;
-          acc.z += val[j].z;
-          acc.w += val[j].w;
-          acc2.x += val2[j].x;
-          acc2.y += val2[j].y;
-          acc2.z += val2[j].z;
-          acc2.w += val2[j].w;
-        }
-      o[v] = acc;
-      if (two) o[v + 32] = acc2;
-    }
-  }
-}
-
-// Combine phase, run by every warp of every CTA once its part of the ticket
-// space is done: after all GEMM-2 tiles are published, warps claim single
-// tokens from their own cursor (ctr[2]) until none are left, so the work
-// balances across all warps whatever the tickets each CTA ended up with.
-__device__ void combine_phase(const MegaParams& mp, int nt2, int cg, volatile int* abort, int* err) {
-  const int lane = threadIdx.x & 31;
+// Token sums, run by every warp of every CTA once its part of the ticket
+// space is done and all second-GEMM tiles are published: warps claim units
+// of one token and one column span from their own cursor (ctr[2]) until
+// none are left.  A unit's rows (the token's k routed rows by dest, then its
+// shared rows) are brought into the warp's 32 KB of shared memory with one
+// bulk copy each -- with a handful of warps per SM, loads straight into
+// registers leave too few bytes in flight to stream at HBM rate -- and are
+// summed in slot order in fp32, the same order as the stand-alone sum
+// kernel, so the bits are the same.
+__device__ void combine_phase(const MegaParams& mp, int nt2, int cg, uint8_t* smem, MegaShared& ms,
+                              volatile int* abort, int* err) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int ok = 1;
   if (lane == 0) {
     ok = wait_counter(&mp.ctr[1], kEpiWarps * cg * nt2, abort, err, (0x0F << 24) | (5 << 20)) ? 1 : 0;
     __threadfence();
   }
   if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  const int T = mp.g1.T, k = mp.g1.k, S = mp.g1.S, R = mp.g1.R, d = mp.g1.d;
+  const int nr = k + S;
+  // span: columns per unit, a multiple of 64 floats whose nr rows fit the buffer
+  const int W = min(d, (kSumBytes / (4 * nr)) / 64 * 64);
+  const int nspan = (d + W - 1) / W;
+  const long long units = static_cast<long long>(T) * nspan;
+  float* buf = reinterpret_cast<float*>(smem + warp * kSumBytes);
+  uint64_t* bar = &ms.sbar[warp];
+  uint32_t par = 0;
+  int next = 0;
+  if (lane == 0) next = atomicAdd(&mp.ctr[2], 1);
   while (true) {
-    int t = 0;
-    if (lane == 0) t = atomicAdd(&mp.ctr[2], 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    if (t >= mp.g1.T) break;
-    combine_token(mp, t);
+    int u = __shfl_sync(0xffffffffu, next, 0);
+    if (u >= units) break;
+    if (lane == 0) next = atomicAdd(&mp.ctr[2], 1);  // the next claim's round trip overlaps this unit
+    const int t = u / nspan, c0 = (u - t * nspan) * W;
+    const int cols = min(W, d - c0);
+    long long myrow = 0;
+    if (lane < k) {
+      myrow = mp.dest[static_cast<size_t>(t) * k + lane];
+      if (!debug_ok(myrow >= 0 && myrow < R, err, kDbgMegaCombine, t)) myrow = 0;
+    } else if (lane < nr) {
+      myrow = R + static_cast<long long>(lane - k) * T + t;
+    }
+    // the buffer's previous reads (generic proxy) before the copies refill it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr * cols * 4));
+    __syncwarp();
+    if (lane < nr)
+      bulk_load(buf + lane * W, mp.Op + myrow * d + c0, static_cast<uint32_t>(cols * 4), bar);
+    if (!mbar_wait(bar, par, abort, err, (0x0F << 24) | (6 << 20) | (t & 0xFFFFF))) return;
+    par ^= 1;
+    const float4* rows4 = reinterpret_cast<const float4*>(buf);
+    float4* o = reinterpret_cast<float4*>(mp.y + static_cast<size_t>(t) * d + c0);
+    const int nv = cols / 4, wv = W / 4;
+    for (int v = lane; v < nv; v += 32) {
+      float4 acc = rows4[v];
+      for (int j = 1; j < nr; ++j) {
+        const float4 x = rows4[j * wv + v];
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      o[v] = acc;
+    }
   }
 }
 
@@ -339,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       mbar_init(&ms.tq_empty[q], CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 1 + kEpiWarps);
     }
     for (int b = 0; b < NST; ++b) mbar_init(&ms.gbar[b], 1);
+    for (int w = 0; w < kSumWarps; ++w) mbar_init(&ms.sbar[w], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       }
     }
     __syncwarp();
-    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
+    if (!*abort) combine_phase(mp, nt2, CG, smem, ms, abort, err);
   } else if (warp == 1) {
     MmaState mst;
     int slot = 0;
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       if (!ok) break;
     }
     if (*abort) mma_drain<CG>(ss, mst);
-    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
+    if (!*abort) combine_phase(mp, nt2, CG, smem, ms, abort, err);
   } else {
     EpiState es;
     uint8_t* stg = smem + NST * SB + (warp & 3) * EPI;
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       if (warp == 2 && lane == 0) trace_record(mp, 1, tn, id, t_pop);
     }
     epilogue_drain(ss, es);
-    if (!*abort) combine_phase(mp, nt2, CG, abort, err);
+    if (!*abort) combine_phase(mp, nt2, CG, smem, ms, abort, err);
   }
 
   tc_fence_before();
