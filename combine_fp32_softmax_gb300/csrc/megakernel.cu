@@ -19,6 +19,7 @@
 //   ctr[1]                   B warp-tiles finished (the token sums wait on all)
 //   ctr[2]                   sum cursor: after the last ticket every warp of
 //                            every CTA claims tokens one at a time from it
+//   ctr[3]                   gather parts finished (NG * CG: every block is in)
 //   ctr[kCtrXp + g]          gathered row block g (mp.grows rows) written
 //   ctr[kCtrXp + NG + mt]    A warp-tiles finished of m-tile mt
 //                            (B tiles of mt wait for all of them)
@@ -210,6 +211,7 @@ __device__ bool gather_task(const MegaParams& mp, MegaShared& ms, uint8_t* smem,
   bulk_wait_all();
   fence_proxy_async_global();
   red_release_gpu_add(&mp.ctr[kCtrXp + g], 1);
+  red_release_gpu_add(&mp.ctr[3], 1);
   return true;
 }
 
@@ -390,12 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
       GatherState gs;
       int slot = 0, tn = 0;
       uint32_t tph = 0;
+      // The even CTA holds the next ticket while it works on the current one,
+      // so the atomic's round trip is off the path between tiles (a CTA still
+      // runs its tickets in increasing order).
+      int next = rank == 0 ? atomicAdd(&mp.ctr[0], 1) : 0;
+      bool gathered = false;  // every gather block is in: no per-block waits any more
       while (!*abort) {
         int id;
         uint64_t t_claim;
         if (rank == 0) {
           if (!mbar_wait<CG == 2>(&ms.tq_empty[slot], tph ^ 1, abort, err, kW | (1 << 20))) break;
-          id = atomicAdd(&mp.ctr[0], 1);
+          id = next;
+          if (id < total) next = atomicAdd(&mp.ctr[0], 1);
           t_claim = globaltimer_ns();
           tq_put<CG>(ms, slot, id);
         } else {
@@ -415,11 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
           if (!gather_task<NST, SB>(mp, ms, smem, id, gs, abort, where, rank, CG)) break;
         } else if (id < e1) {
           const TileInfo t = decode_tile<KA, CG>(mp.g1, ss, id - NG, rank);
-          if (t.active && !t.shared) {  // routed rows come from the gathered rows: wait for their blocks
-            const int g0 = t.grow0 / mp.grows, g1 = (t.grow0 + t.rows - 1) / mp.grows;
-            bool ok = true;
-            for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], CG, abort, err, where);
-            if (!ok) break;
+          if (t.active && !t.shared && !gathered) {  // routed rows come from the gathered rows: wait for their blocks
+            if (ld_acquire_gpu(&mp.ctr[3]) >= NG * CG) {
+              gathered = true;
+            } else {
+              const int g0 = t.grow0 / mp.grows, g1 = (t.grow0 + t.rows - 1) / mp.grows;
+              bool ok = true;
+              for (int g = g0; g <= g1 && ok; ++g) ok = wait_counter(&mp.ctr[kCtrXp + g], CG, abort, err, where);
+              if (!ok) break;
+            }
             fence_proxy_async_global();
           }
           if (!produce_tile<KA, CG>(mp.g1, t, ss, smem, ps, abort, where, NST, rank)) break;
@@ -471,9 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
     uint8_t* stg = smem + NST * SB + (warp & 3) * EPI;
     int slot = 0, tn = 0;
     uint32_t tph = 0;
+    // A tile's readiness signal waits for its stores to complete; it is sent
+    // once the next task is in hand, while that tile's accumulator is still
+    // being computed, so the wait is off the epilogue's path.
+    int* pending = nullptr;
     while (true) {
       bool ok;
       const int id = tq_get<CG>(ms, slot, tph, rank, abort, err, kW | (3 << 20), &ok);
+      if (pending) {
+        warp_signal(pending);
+        pending = nullptr;
+      }
       if (!ok) break;
       const uint64_t t_pop = globaltimer_ns();
       if (++slot == kTq) {
@@ -488,12 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) mega_kernel(const __grid_constant
         if (!epilogue_step<KA, CG>(mp.g1, decode_tile<KA, CG>(mp.g1, ss, t1, rank), ss, tmem, stg, es, abort, where,
                                    rank))
           break;
-        warp_signal(&mp.ctr[kCtrXp + NG + t1 / ms.ntn1]);
+        pending = &mp.ctr[kCtrXp + NG + t1 / ms.ntn1];
       } else if (id >= e1 && id < e2) {
         if (!epilogue_step<KB, CG>(mp.g2, decode_g2<KA, KB, CG>(mp, ms, id - e1, rank), ss, tmem, stg, es, abort,
                                    where, rank))
           break;
-        warp_signal(&mp.ctr[1]);
+        pending = &mp.ctr[1];
       }
       if (warp == 2 && lane == 0) trace_record(mp, 1, tn, id, t_pop);
     }
