@@ -41,7 +41,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv2lite_T8192_d2048_f1408_E64_k6_S2")
     ap.add_argument("--megakernel", type=int, default=-1, help="1: forward MegaKernel, 0: kernel chain, "
-                    "-1: MegaKernel when the library provides it")
+                    "-1: the faster of the two, timed during set-up (same bits)")
     ap.add_argument("--bwd-megakernel", type=int, default=-1, help="1: backward input part as one MegaKernel, "
                     "0: kernel chain, -1: the faster of the two (same bits)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -365,9 +365,10 @@ def run_ours(args):
     pair_kinds = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
     moe.moe_set_gemm_pair_kinds(pair_kinds)
 
-    fwd_times = best_of(fwd_ms)
     mk = args.megakernel
+    fwd_times = None
     if mk < 0:  # the faster forward of the two (same bits either way)
+        fwd_times = best_of(fwd_ms)
         mk = 1 if fwd_times["megakernel"] < fwd_times["chain"] else 0
 
     def bwd_ms(use_mk):
@@ -377,9 +378,10 @@ def run_ours(args):
                                                    out["idx"], out["w"], ws, out["dx"], out["dz"], out["dW1"],
                                                    out["dW3"], out["dW2"], which=which))
 
-    bwd_times = best_of(bwd_ms)
     bmk = args.bwd_megakernel
+    bwd_times = None
     if bmk < 0:
+        bwd_times = best_of(bwd_ms)
         bmk = 1 if bwd_times["megakernel"] < bwd_times["chain"] else 0
     bwd_which = 3 | (moe.MOE_BWD_MEGAKERNEL if bmk else 0)
 
