@@ -603,16 +603,23 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
     for (int h = 0; h < 4; ++h) wrow[h] = __shfl_sync(0xffffffffu, es.w, 16 * (h >> 1) + 8 * (h & 1) + quad);
   }
   const int ncols = min(256, N - t.n0);
+  // Software pipeline: group g+1's two TMEM loads are in flight while group
+  // g is exchanged and stored.
+  uint32_t v[2][16], nv[2][16];
+  if (zero) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
+  } else {
+    tmem_ld_16x256b_x4(tacc, v[0]);
+    tmem_ld_16x256b_x4(tacc + (16u << 16), v[1]);
+    tmem_ld_wait();
+  }
 #pragma unroll 1
   for (int g = 0; g < ncols; g += 32) {
-    uint32_t v[2][16];
-    if (zero) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
-    } else {
-      tmem_ld_16x256b_x4(tacc + g, v[0]);
-      tmem_ld_16x256b_x4(tacc + (16u << 16) + g, v[1]);
-      tmem_ld_wait();
+    const bool more = g + 32 < ncols;
+    if (more && !zero) {
+      tmem_ld_16x256b_x4(tacc + g + 32, nv[0]);
+      tmem_ld_16x256b_x4(tacc + (16u << 16) + g + 32, nv[1]);
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -648,6 +655,14 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
           if (row < valid_rows && t.n0 + col < N)
             *reinterpret_cast<float4*>(base + static_cast<long long>(row) * ld + t.n0 + col) = o;
         }
+      }
+    }
+    if (more) {
+      if (!zero) tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        v[0][i] = zero ? 0u : nv[0][i];
+        v[1][i] = zero ? 0u : nv[1][i];
       }
     }
   }
