@@ -63,7 +63,8 @@ constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB (one CTA per tile)
 constexpr int kBoxBytes = 64 * 64 * 2;          // one MN-major box: 64 x 64 bf16
 constexpr int kMaxSeg = 256 + 4;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;                  // epilogue warps of most kinds (one per TMEM lane quadrant)
+constexpr int kMaxEpiWarps = 8;               // the weight-gradient kinds: two per quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 32 * 64;  // one staged chunk: 32 rows x 64 bytes (SW64)
@@ -97,6 +98,11 @@ struct Traits {
   static constexpr bool B_MN = (KIND == kDH || KIND == kDX || KIND == kDW13 || KIND == kDW2);
   static constexpr bool RAGGED_K = (KIND == kDW13 || KIND == kDW2);
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
+  // Epilogue warps: the weight-gradient kinds' short-K tiles finish their
+  // MMAs about as fast as four warps can move 256 fp32 columns out, so two
+  // warps per TMEM lane quadrant each take half of the columns.
+  static constexpr int EPI_WARPS = (KIND == kDW13 || KIND == kDW2) ? kMaxEpiWarps : kEpiWarps;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
   // fp32 kinds: 16-column chunks, two staging buffers in flight.
   static constexpr int F32_ROUNDS = 2;
@@ -124,7 +130,7 @@ struct Pipe {
 struct SharedState {
   uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain;
   uint64_t ready[kMaxStages];  // CG = 2, even CTA: the odd CTA's stage has landed
-  uint64_t aux[kEpiWarps][2];  // dH epilogue input buffers of each warp
+  uint64_t aux[kMaxEpiWarps][2];  // dH epilogue input buffers of each warp
   uint64_t tile_full[kTileRing], tile_empty[kTileRing];  // tile-number ring
   int tile_ring[kTileRing];
   uint32_t tmem_base;
@@ -150,7 +156,7 @@ __device__ __forceinline__ int seg_rows(const GemmParams& p, const SharedState& 
 
 template <int KIND, int CG = 1>
 constexpr int smem_bytes() {
-  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + kEpiWarps * Traits<KIND>::EPI_BYTES +
+  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + Traits<KIND>::EPI_WARPS * Traits<KIND>::EPI_BYTES +
          static_cast<int>(sizeof(SharedState));
 }
 
@@ -484,7 +490,7 @@ __device__ __forceinline__ void staging_publish() {
 // fp32 outputs (GEMM 2, dX, dW1/dW3, dW2): 16-column chunks, double-buffered.
 template <int KIND>
 __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
-                                             uint8_t* stg, EpiState& es) {
+                                             uint8_t* stg, EpiState& es, int part = 0, int nparts = 1) {
   const int lane = threadIdx.x & 31;
   const int r = 32 * q + lane;  // tile row of this lane
   const CUtensorMap* map = &p.tmO0;
@@ -519,8 +525,11 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
   }
   const bool zero = Traits<KIND>::RAGGED_K && t.nkb == 0;  // empty expert: exact zeros
   constexpr int NR = Traits<KIND>::F32_ROUNDS;
-  const int nchunks = min(16, (N - t.n0 + 15) / 16);
+  // this warp's chunks: [j0, j1) of the tile's 16-column chunks
+  const int per = 16 / nparts;
+  const int j0 = part * per, j1 = min(min(16, (N - t.n0 + 15) / 16), j0 + per);
   es.chunks = 0;
+  if (j0 >= j1) return;
   // Software pipeline: chunk j+1's TMEM load is in flight while chunk j is
   // staged and its TMA store issued.
   uint32_t cur[16], nxt[16];
@@ -528,12 +537,12 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
 #pragma unroll
     for (int i = 0; i < 16; ++i) cur[i] = 0u;
   } else {
-    tmem_ld_32x16(tacc, cur);
+    tmem_ld_32x16(tacc + 16 * j0, cur);
     tmem_ld_wait();
   }
 #pragma unroll 1
-  for (int j = 0; j < nchunks; ++j) {
-    const bool more = j + 1 < nchunks;
+  for (int j = j0; j < j1; ++j) {
+    const bool more = j + 1 < j1;
     if (more && !zero) tmem_ld_32x16(tacc + 16 * (j + 1), nxt);
     if constexpr (KIND == kG2) {
 #pragma unroll
@@ -569,7 +578,7 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
 // outside the output are not written; the same values as epilogue_f32.
 template <int KIND>
 __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
-                                                    EpiState& es) {
+                                                    EpiState& es, int part = 0, int nparts = 1) {
   const int lane = threadIdx.x & 31;
   const int quad = lane >> 2, c = lane & 3;
   int N;
@@ -602,7 +611,12 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
 #pragma unroll
     for (int h = 0; h < 4; ++h) wrow[h] = __shfl_sync(0xffffffffu, es.w, 16 * (h >> 1) + 8 * (h & 1) + quad);
   }
-  const int ncols = min(256, N - t.n0);
+  // this warp's columns: [g0, ncols) of the tile, in groups of 32
+  const int span = 256 / nparts;
+  const int g0 = part * span;
+  const int ncols = min(min(256, N - t.n0), g0 + span);
+  es.chunks = 0;
+  if (g0 >= ncols) return;
   // Software pipeline: group g+1's two TMEM loads are in flight while group
   // g is exchanged and stored.
   uint32_t v[2][16], nv[2][16];
@@ -610,12 +624,12 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[0][i] = v[1][i] = 0u;
   } else {
-    tmem_ld_16x256b_x4(tacc, v[0]);
-    tmem_ld_16x256b_x4(tacc + (16u << 16), v[1]);
+    tmem_ld_16x256b_x4(tacc + g0, v[0]);
+    tmem_ld_16x256b_x4(tacc + (16u << 16) + g0, v[1]);
     tmem_ld_wait();
   }
 #pragma unroll 1
-  for (int g = 0; g < ncols; g += 32) {
+  for (int g = g0; g < ncols; g += 32) {
     const bool more = g + 32 < ncols;
     if (more && !zero) {
       tmem_ld_16x256b_x4(tacc + g + 32, nv[0]);
@@ -666,7 +680,6 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
       }
     }
   }
-  es.chunks = 0;
 }
 
 // GEMM 1: columns [0,128) of the accumulator hold a (gate), [128,256) hold b
@@ -849,11 +862,11 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
 // tile_empty (used in the even CTA, or the only one) counts every role that
 // reads a tile number from the ring: the MMA warp and the epilogue warps of
 // both CTAs, and the odd CTA's producer.
-template <int CG = 1>
+template <int CG = 1, int EW = kEpiWarps>
 __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
   for (int i = 0; i < kTileRing; ++i) {
     mbar_init(&ss.tile_full[i], 1);
-    mbar_init(&ss.tile_empty[i], CG == 2 ? 2 * (1 + kEpiWarps) + 1 : 1 + kEpiWarps);
+    mbar_init(&ss.tile_empty[i], CG == 2 ? 2 * (1 + EW) + 1 : 1 + EW);
   }
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&ss.full[s], 1);
@@ -862,9 +875,9 @@ __device__ __forceinline__ void init_gemm_barriers(SharedState& ss) {
   }
   for (int a = 0; a < 2; ++a) {
     mbar_init(&ss.tfull[a], 1);
-    mbar_init(&ss.tempty[a], kEpiWarps * CG);
+    mbar_init(&ss.tempty[a], EW * CG);
   }
-  for (int w = 0; w < kEpiWarps; ++w) {
+  for (int w = 0; w < EW; ++w) {
     mbar_init(&ss.aux[w][0], 1);
     mbar_init(&ss.aux[w][1], 1);
   }
@@ -1091,10 +1104,13 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
     ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where);
   else
   {
+    // with two warps per TMEM lane quadrant, each takes half of the columns
+    constexpr int NP = Traits<KIND>::EPI_WARPS / kEpiWarps;
+    const int part = NP > 1 ? (warp - 2) / kEpiWarps : 0;
     if (p.epi_direct)
-      epilogue_f32_direct<KIND>(p, t, q, tacc, es);
+      epilogue_f32_direct<KIND>(p, t, q, tacc, es, part, NP);
     else
-      epilogue_f32<KIND>(p, t, q, tacc, stg, es);
+      epilogue_f32<KIND>(p, t, q, tacc, stg, es, part, NP);
   }
   tc_fence_before();
   __syncwarp();

@@ -60,7 +60,8 @@ __device__ __forceinline__ int feed_get(SharedState& ss, int i, int rank, volati
 // CG = 1: one CTA per SM and tile.  CG = 2: CTA pairs (clusters of two), one
 // 256-row tile per pair; the even CTA issues the MMAs for both.
 template <int KIND, int CG>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(Traits<KIND>::THREADS, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int EW = Traits<KIND>::EPI_WARPS;
   const int NST = p.nst;  // at most Pipe<KIND, CG>::STAGES (checked by the launcher)
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -75,12 +76,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   }
   uint8_t* smem = smem_raw;
   uint8_t* stg_base = smem + NST * SB;  // epilogue staging, Traits::EPI_BYTES per epilogue warp
-  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + kEpiWarps * Traits<KIND>::EPI_BYTES);
+  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + EW * Traits<KIND>::EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
 
   if (threadIdx.x == 0) {
-    init_gemm_barriers<CG>(ss);
+    init_gemm_barriers<CG, EW>(ss);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (*abort) mma_drain<CG>(ss, ms);
   } else {
     EpiState es;
-    uint8_t* stg = stg_base + (warp & 3) * Traits<KIND>::EPI_BYTES;
+    uint8_t* stg = stg_base + (warp - 2) * Traits<KIND>::EPI_BYTES;
     for (int i = 0;; ++i) {
       const int tile = tile_of(i, wfeed | (2 << 19) | (i & 0x7ffff));
       if (tile < 0 || !epilogue_step<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, tmem, stg, es,
@@ -197,7 +198,7 @@ int g_epi_direct[6] = {0, 0, 0, 0, 0, 0};   // per fp32-output kind: 1 = unstage
 template <int KIND, int CG>
 void launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t s) {
   cfg = {};
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Traits<KIND>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes<KIND, CG>();
   cfg.stream = s;
   if constexpr (CG == 2) {
