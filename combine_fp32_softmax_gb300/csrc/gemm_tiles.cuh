@@ -66,6 +66,8 @@ constexpr int kMaxSeg = 256 + 4;
 constexpr int kEpiWarps = 4;                  // epilogue warps of most kinds (one per TMEM lane quadrant)
 constexpr int kMaxEpiWarps = 8;               // the weight-gradient kinds: two per quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Position of the calling warp among the epilogue warps (warps 2, 3, ...).
+__device__ __forceinline__ int epi_warp() { return static_cast<int>(threadIdx.x >> 5) - 2; }
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 32 * 64;  // one staged chunk: 32 rows x 64 bytes (SW64)
 
@@ -98,11 +100,7 @@ struct Traits {
   static constexpr bool B_MN = (KIND == kDH || KIND == kDX || KIND == kDW13 || KIND == kDW2);
   static constexpr bool RAGGED_K = (KIND == kDW13 || KIND == kDW2);
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
-  // Epilogue warps: the weight-gradient kinds' short-K tiles finish their
-  // MMAs about as fast as four warps can move 256 fp32 columns out, so two
-  // warps per TMEM lane quadrant each take half of the columns.
-  static constexpr int EPI_WARPS = (KIND == kDW13 || KIND == kDW2) ? kMaxEpiWarps : kEpiWarps;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+
   static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
   // fp32 kinds: 16-column chunks, two staging buffers in flight.
   static constexpr int F32_ROUNDS = 2;
@@ -124,13 +122,24 @@ struct Pipe {
   static constexpr int B_BYTES = kBBytes / CG;
   static constexpr int B_BOXES = 4 / CG;  // MN-major B: 64-column boxes per CTA
   static constexpr int STAGE_BYTES = kABytes + B_BYTES;
-  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 5 : 6);
+  // Epilogue warps of the stand-alone kernel: two per TMEM lane quadrant,
+  // each taking half of a tile's columns, for the weight-gradient kinds
+  // (their short-K tiles finish the MMAs about as fast as four warps move
+  // 256 fp32 columns out) and for dH on CTA pairs (twice the elementwise
+  // inputs in flight for its HBM-heavy epilogue; it then fits four stages).
+  static constexpr int EPI_WARPS =
+      (KIND == kDW13 || KIND == kDW2 || (KIND == kDH && CG == 2)) ? kMaxEpiWarps : kEpiWarps;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 4 : 6);
 };
 
 struct SharedState {
   uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain;
   uint64_t ready[kMaxStages];  // CG = 2, even CTA: the odd CTA's stage has landed
-  uint64_t aux[kMaxEpiWarps][2];  // dH epilogue input buffers of each warp
+  // dH epilogue input buffers, two per epilogue warp (indexed by the warp's
+  // position among the epilogue warps, never by its TMEM lane quadrant: two
+  // warps share a quadrant when a kind runs eight)
+  uint64_t aux[kMaxEpiWarps][2];
   uint64_t tile_full[kTileRing], tile_empty[kTileRing];  // tile-number ring
   int tile_ring[kTileRing];
   uint32_t tmem_base;
@@ -156,7 +165,7 @@ __device__ __forceinline__ int seg_rows(const GemmParams& p, const SharedState& 
 
 template <int KIND, int CG = 1>
 constexpr int smem_bytes() {
-  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + Traits<KIND>::EPI_WARPS * Traits<KIND>::EPI_BYTES +
+  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + Pipe<KIND, CG>::EPI_WARPS * Traits<KIND>::EPI_BYTES +
          static_cast<int>(sizeof(SharedState));
 }
 
@@ -746,13 +755,18 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
 __device__ __forceinline__ int dh_chunks(const GemmParams& p, const TileInfo& t) {
   return min(8, (p.f - t.n0 + 31) / 32);
 }
+// This warp's chunks [c0, c1): all of them, or half with two warps per quadrant.
+__device__ __forceinline__ int2 dh_range(const GemmParams& p, const TileInfo& t, int part, int nparts) {
+  const int nch = dh_chunks(p, t), per = 8 / nparts;
+  return make_int2(min(nch, part * per), min(nch, (part + 1) * per));
+}
 __device__ __forceinline__ void dh_issue_inputs(const GemmParams& p, const TileInfo& t, int q, int c, uint8_t* stg,
                                                 SharedState& ss, EpiState& es) {
   const int buf = es.auxn & 1;
   ++es.auxn;
   if ((threadIdx.x & 31) == 0) {
     uint8_t* in = stg + buf * 3 * kChunkBytes;
-    uint64_t* bar = &ss.aux[q][buf];
+    uint64_t* bar = &ss.aux[epi_warp()][buf];
     const int n = t.n0 + 32 * c, row0 = t.grow0 + 32 * q;
     mbar_arrive_expect_tx(bar, 3 * kChunkBytes);
     tma_load_2d(in, &p.tmX0, bar, n, row0);                    // a
@@ -763,15 +777,17 @@ __device__ __forceinline__ void dh_issue_inputs(const GemmParams& p, const TileI
 }
 // Issued before the tile's accumulator is ready so the loads overlap the wait.
 __device__ __forceinline__ void dh_prefetch(const GemmParams& p, const TileInfo& t, int q, uint8_t* stg,
-                                            SharedState& ss, EpiState& es) {
-  const int nch = dh_chunks(p, t);
-  dh_issue_inputs(p, t, q, 0, stg, ss, es);
-  if (nch > 1) dh_issue_inputs(p, t, q, 1, stg, ss, es);
+                                            SharedState& ss, EpiState& es, int part, int nparts) {
+  const int2 r = dh_range(p, t, part, nparts);
+  if (r.x < r.y) dh_issue_inputs(p, t, q, r.x, stg, ss, es);
+  if (r.x + 1 < r.y) dh_issue_inputs(p, t, q, r.x + 1, stg, ss, es);
 }
 
+// The dw partial dot of a row is summed per 128 columns (4 chunks, in order)
+// and stored at index (column / 128), whether one warp or two cover the row.
 __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
                                             uint8_t* stg, SharedState& ss, EpiState& es, volatile int* abort,
-                                            int where) {
+                                            int where, int part, int nparts) {
   const int lane = threadIdx.x & 31;
   const int r = 32 * q + lane;
   const bool rowok = r < t.rows, full = t.rows >= 32 * q + 32;
@@ -780,15 +796,16 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
   const float w = es.w;
   uint16_t* dAB = static_cast<uint16_t*>(p.out0);
   uint16_t* Hw = static_cast<uint16_t*>(p.out1);
-  const int nch = dh_chunks(p, t);
-  const uint32_t first = es.auxn - (nch > 1 ? 2 : 1);  // input chunk index of chunk 0
+  const int2 range = dh_range(p, t, part, nparts);
+  const int c0 = range.x, c1 = range.y;
+  const uint32_t first = es.auxn - min(2, c1 - c0);  // input chunk index of chunk c0
   float dot = 0.f;
   es.chunks = 0;
 #pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
+  for (int c = c0; c < c1; ++c) {
     const int n = t.n0 + 32 * c;
-    const int buf = (first + c) & 1;
-    if (!mbar_wait(&ss.aux[q][buf], (es.auxpar >> buf) & 1, abort, p.err, where)) return false;
+    const int buf = (first + (c - c0)) & 1;
+    if (!mbar_wait(&ss.aux[epi_warp()][buf], (es.auxpar >> buf) & 1, abort, p.err, where)) return false;
     es.auxpar ^= 1u << buf;
     es.auxpend &= ~(1u << buf);
     uint32_t g[32];
@@ -834,7 +851,7 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
         tma_store_2d(&p.tmO0, out + kChunkBytes, p.f + n, orow0);
         tma_store_2d(&p.tmO1, out + 2 * kChunkBytes, n, orow0);
         bulk_commit();
-        if (c + 2 < nch) bulk_wait_read<0>();  // the stores have read the buffer before it is refilled
+        if (c + 2 < c1) bulk_wait_read<0>();  // the stores have read the buffer before it is refilled
       }
       __syncwarp();
       ++es.chunks;
@@ -847,9 +864,12 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
       fence_proxy_async_smem();  // the inputs' generic reads before the refill's TMA writes
       __syncwarp();
     }
-    if (c + 2 < nch) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
+    if (c + 2 < c1) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
+    if ((c & 3) == 3 || c == c1 - 1) {  // end of a 128-column group
+      if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + (t.n0 + 32 * c) / 128] = dot;
+      dot = 0.f;
+    }
   }
-  if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + t.n0 / kBN] = dot;
   return true;
 }
 
@@ -1080,17 +1100,20 @@ __device__ __forceinline__ void mma_drain(SharedState& ss, const MmaState& ms) {
 // In a pair the odd CTA's warps release the buffer on the even CTA's
 // barrier.  A part with no valid row still waits for the accumulator, so its
 // release cannot count toward an earlier phase of the barrier.
-template <int KIND, int CG = 1>
+template <int KIND, int CG = 1, int EW = kEpiWarps>
 __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInfo& t, SharedState& ss, uint32_t tmem,
                                               uint8_t* stg, EpiState& es, volatile int* abort, int where,
                                               int rank = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are reachable from this warp
+  // with two warps per TMEM lane quadrant, each takes half of the columns
+  constexpr int NP = EW / kEpiWarps;
+  const int part = NP > 1 ? (warp - 2) / kEpiWarps : 0;
   const int acc = es.it & 1;
   const uint32_t aph = (es.it >> 1) & 1;
   ++es.it;
   if constexpr (KIND == kDH)
-    if (t.active) dh_prefetch(p, t, q, stg, ss, es);
+    if (t.active) dh_prefetch(p, t, q, stg, ss, es, part, NP);
   if constexpr (KIND == kG2 || KIND == kDH)
     if (t.active) es.w = row_weight(p, t, q);
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
@@ -1101,12 +1124,9 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   } else if constexpr (KIND == kG1)
     epilogue_g1(p, t, q, tacc, stg, es);
   else if constexpr (KIND == kDH)
-    ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where);
+    ok = epilogue_dh(p, t, q, tacc, stg, ss, es, abort, where, part, NP);
   else
   {
-    // with two warps per TMEM lane quadrant, each takes half of the columns
-    constexpr int NP = Traits<KIND>::EPI_WARPS / kEpiWarps;
-    const int part = NP > 1 ? (warp - 2) / kEpiWarps : 0;
     if (p.epi_direct)
       epilogue_f32_direct<KIND>(p, t, q, tacc, es, part, NP);
     else
@@ -1128,11 +1148,10 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
 // Before an epilogue warp may leave: its TMA stores complete and its
 // in-flight input loads landed.
 __device__ __forceinline__ void epilogue_drain(SharedState& ss, const EpiState& es) {
-  const int q = (threadIdx.x >> 5) & 3;
   if ((threadIdx.x & 31) == 0) {
     bulk_wait_all();
     for (int b = 0; b < 2; ++b)
-      if (es.auxpend & (1u << b)) mbar_wait_drain(&ss.aux[q][b], (es.auxpar >> b) & 1);
+      if (es.auxpend & (1u << b)) mbar_wait_drain(&ss.aux[epi_warp()][b], (es.auxpar >> b) & 1);
   }
   __syncwarp();
 }
@@ -1215,7 +1234,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
   p.row_slot = a.row_slot;
   p.topk_w = a.topk_w;
   p.err = a.err;
-  p.nt_dh = ceil_div(a.f, kBN);
+  p.nt_dh = ceil_div(a.f, 128);
   bool ok = true;
   auto alt = [](const void* want, const void* fallback) { return want ? want : fallback; };
   if constexpr (KIND == kG1) {

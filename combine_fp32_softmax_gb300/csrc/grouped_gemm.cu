@@ -60,8 +60,8 @@ __device__ __forceinline__ int feed_get(SharedState& ss, int i, int rank, volati
 // CG = 1: one CTA per SM and tile.  CG = 2: CTA pairs (clusters of two), one
 // 256-row tile per pair; the even CTA issues the MMAs for both.
 template <int KIND, int CG>
-__global__ void __launch_bounds__(Traits<KIND>::THREADS, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int EW = Traits<KIND>::EPI_WARPS;
+__global__ void __launch_bounds__(Pipe<KIND, CG>::THREADS, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int EW = Pipe<KIND, CG>::EPI_WARPS;
   const int NST = p.nst;  // at most Pipe<KIND, CG>::STAGES (checked by the launcher)
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(Traits<KIND>::THREADS, 1) grouped_gemm_kernel(
     uint8_t* stg = stg_base + (warp - 2) * Traits<KIND>::EPI_BYTES;
     for (int i = 0;; ++i) {
       const int tile = tile_of(i, wfeed | (2 << 19) | (i & 0x7ffff));
-      if (tile < 0 || !epilogue_step<KIND, CG>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, tmem, stg, es,
+      if (tile < 0 || !epilogue_step<KIND, CG, EW>(p, decode_tile<KIND, CG>(p, ss, tile, rank), ss, tmem, stg, es,
                                                abort, where0 | (4 << 20) | tile, rank))
         break;
     }
@@ -198,7 +198,7 @@ int g_epi_direct[6] = {0, 0, 0, 0, 0, 0};   // per fp32-output kind: 1 = unstage
 template <int KIND, int CG>
 void launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t s) {
   cfg = {};
-  cfg.blockDim = dim3(Traits<KIND>::THREADS);
+  cfg.blockDim = dim3(Pipe<KIND, CG>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes<KIND, CG>();
   cfg.stream = s;
   if constexpr (CG == 2) {
