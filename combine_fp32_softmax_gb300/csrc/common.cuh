@@ -94,7 +94,7 @@ struct WsLayout {
   size_t Xp, AB, H, Op, G, dAB, Hw, dXp, partial, dw, mk;
   size_t total;
   int nb_route;  // router/permutation blocks
-  int nt_dh;     // partial dot products per row of the dH GEMM (one per 128 columns)
+  int nt_dh;     // column tiles of the dH GEMM (partial dot products per row)
   int mk_ints;   // ints in the MegaKernel counter region
 };
 
@@ -103,7 +103,7 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   const size_t T = c.T, d = c.d_model, f = c.d_ff, E = c.E, k = c.k, S = c.n_shared;
   const size_t R = T * k, Rs = R + S * T;
   L.nb_route = ceil_div(c.T, kRouteTokensPerBlock);
-  L.nt_dh = ceil_div(c.d_ff, 128);  // dw partial dots: one per 128 columns of a row
+  L.nt_dh = ceil_div(c.d_ff, kBN);  // dw partial dots: one per 256-column tile of a row
   // MegaKernel counters: cursor + 3 phase counters, one readiness counter
   // per gathered row block (kMegaGatherRows rows), one per first-GEMM m-tile
   // (bounded by the m-tiles of every segment), padding.
@@ -131,7 +131,7 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.dAB = take(2 * Rs * 2 * f);
   L.Hw = take(2 * Rs * f);
   L.dXp = take(4 * Rs * d);
-  L.partial = take(4 * R * L.nt_dh);  // one partial dot per (row, 128 columns)
+  L.partial = take(4 * R * L.nt_dh);  // one partial dot per (row, 256-column tile)
   L.dw = take(4 * T * k);
   L.mk = take(sizeof(int) * L.mk_ints);
   L.total = o;

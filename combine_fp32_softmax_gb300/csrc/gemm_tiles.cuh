@@ -125,12 +125,11 @@ struct Pipe {
   // Epilogue warps of the stand-alone kernel: two per TMEM lane quadrant,
   // each taking half of a tile's columns, for the weight-gradient kinds
   // (their short-K tiles finish the MMAs about as fast as four warps move
-  // 256 fp32 columns out) and for dH on CTA pairs (twice the elementwise
-  // inputs in flight for its HBM-heavy epilogue; it then fits four stages).
-  static constexpr int EPI_WARPS =
-      (KIND == kDW13 || KIND == kDW2 || (KIND == kDH && CG == 2)) ? kMaxEpiWarps : kEpiWarps;
+  // 256 fp32 columns out).  dH keeps four: eight would cost it a pipeline
+  // stage, which measured 11-16% slower.
+  static constexpr int EPI_WARPS = (KIND == kDW13 || KIND == kDW2) ? kMaxEpiWarps : kEpiWarps;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 4 : 6);
+  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 5 : 6);
 };
 
 struct SharedState {
@@ -783,8 +782,8 @@ __device__ __forceinline__ void dh_prefetch(const GemmParams& p, const TileInfo&
   if (r.x + 1 < r.y) dh_issue_inputs(p, t, q, r.x + 1, stg, ss, es);
 }
 
-// The dw partial dot of a row is summed per 128 columns (4 chunks, in order)
-// and stored at index (column / 128), whether one warp or two cover the row.
+// The dw partial dot of a row is summed over the tile's 256 columns in chunk
+// order by the one warp that covers the row, and stored at index n0 / 256.
 __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
                                             uint8_t* stg, SharedState& ss, EpiState& es, volatile int* abort,
                                             int where, int part, int nparts) {
@@ -865,11 +864,8 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
       __syncwarp();
     }
     if (c + 2 < c1) dh_issue_inputs(p, t, q, c + 2, stg, ss, es);
-    if ((c & 3) == 3 || c == c1 - 1) {  // end of a 128-column group
-      if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + (t.n0 + 32 * c) / 128] = dot;
-      dot = 0.f;
-    }
   }
+  if (rowok && !t.shared) p.out_partial[grow * p.nt_dh + t.n0 / kBN] = dot;
   return true;
 }
 
@@ -1109,6 +1105,7 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   // with two warps per TMEM lane quadrant, each takes half of the columns
   constexpr int NP = EW / kEpiWarps;
   const int part = NP > 1 ? (warp - 2) / kEpiWarps : 0;
+  static_assert(KIND != kDH || NP == 1, "one warp sums a row's dw partial dot over the whole tile");
   const int acc = es.it & 1;
   const uint32_t aph = (es.it >> 1) & 1;
   ++es.it;
@@ -1234,7 +1231,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
   p.row_slot = a.row_slot;
   p.topk_w = a.topk_w;
   p.err = a.err;
-  p.nt_dh = ceil_div(a.f, 128);
+  p.nt_dh = ceil_div(a.f, kBN);
   bool ok = true;
   auto alt = [](const void* want, const void* fallback) { return want ? want : fallback; };
   if constexpr (KIND == kG1) {

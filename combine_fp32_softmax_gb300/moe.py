@@ -353,7 +353,7 @@ def ws_offsets(cfg: MoEConfig) -> dict:
     T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
     R, Rs = T * k, T * k + S * T
     nb = -(-T // 32)
-    nt = -(-f // 128)  # dw partial dots per row: one per 128 columns
+    nt = -(-f // 256)  # dw partial dots per row: one per 256-column tile
     o = 0
     out = {}
 
