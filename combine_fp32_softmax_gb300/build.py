@@ -35,17 +35,31 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def source_digest() -> str:
-    """First 16 hex digits of a SHA-256 over the library's CUDA/C++ sources
-    and its public header: names a build of the kernels, so a profile taken
-    of one build is not read as a measurement of another."""
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed
+    (string literals kept as they are)."""
+    import re
+    token = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+    code = token.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(code.split())
+
+
+def source_digest(root: str = None) -> str:
+    """First 16 hex digits of a SHA-256 over the code (comments and
+    whitespace aside) of the library's CUDA/C++ sources and its public
+    header: names a build of the kernels, so a profile taken of one build is
+    not read as a measurement of another.  `root`: a directory holding
+    csrc/ and include/moe.h laid out as in the repository (default: this
+    package)."""
     import hashlib
+    csrc = os.path.join(root, "csrc") if root else CSRC
+    header = os.path.join(root, "include", "moe.h") if root else os.path.join(HERE, "..", "include", "moe.h")
     h = hashlib.sha256()
-    names = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
+    names = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
     for f in names:
         h.update(f.encode())
-        h.update(open(os.path.join(CSRC, f), "rb").read())
-    h.update(open(os.path.join(HERE, "..", "include", "moe.h"), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
+    h.update(_code_only(open(header, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

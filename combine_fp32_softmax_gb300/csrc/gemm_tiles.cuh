@@ -33,6 +33,10 @@
 //               their valid rows directly.  The dH epilogue TMA-loads its
 //               elementwise inputs ([a|b], H) per warp, double-buffered,
 //               and stages its outputs in the buffer the inputs came in.
+//               The weight-gradient kinds run warps 2-9: two per TMEM lane
+//               quadrant, each on half of the tile's columns.  The fp32
+//               kinds can instead store straight from registers
+//               (epilogue_f32_direct, a runtime option).
 //   The accumulator is double-buffered in TMEM (2 x 256 columns) so the
 //   epilogue of tile i overlaps the main loop of tile i+1.
 // Tiles of equal length are taken in a static round-robin over CTAs, those of
