@@ -59,3 +59,26 @@ def test_multi_rank_addresses_match_concatenated_batch(G, E, k):
     flat = torch.cat(sels).cpu().numpy().reshape(-1)
     want = t["dest"].cpu().numpy() - np.array(first)[np.array(owners)[flat]]
     assert np.array_equal(np.concatenate(got), want)
+
+
+def test_rank_bases_single_rank_and_owner_clamp():
+    """One rank: the bases are the exclusive prefix sums of the counts (the
+    single-GPU offsets) and one owner receives every row.  Owner indices
+    outside [0, G) are clamped into range, so the bases equal those of the
+    clamped owner table."""
+    E = 40
+    g = torch.Generator().manual_seed(3)
+    counts = torch.randint(0, 50, (1, E), generator=g, dtype=torch.int32)
+    base, rows = ep.rank_bases(counts.to(DEV), 0, [0] * E)
+    want = torch.cumsum(counts[0], 0) - counts[0]
+    assert base.cpu().tolist() == want.tolist()
+    assert rows.cpu().tolist() == [int(counts.sum())]
+    G = 3
+    all_counts = torch.randint(0, 50, (G, E), generator=g, dtype=torch.int32)
+    wild = [(-2 if e % 7 == 0 else (5 if e % 5 == 0 else e % G)) for e in range(E)]
+    clamped = [min(max(o, 0), G - 1) for o in wild]
+    for r in range(G):
+        b1, r1 = ep.rank_bases(all_counts.to(DEV), r, wild)
+        b2, r2 = ep.rank_bases(all_counts.to(DEV), r, clamped)
+        assert torch.equal(b1, b2) and torch.equal(r1, r2)
+        assert b1.cpu().tolist() == bases_restated(all_counts.to(torch.int64), r, clamped).tolist()

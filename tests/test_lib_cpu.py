@@ -78,3 +78,46 @@ def test_workspace_layout_matches_binding_mirror(lib, cfg):
     assert total % 256 == 0
     # every region is 256-byte aligned (TMA needs 16)
     assert all(v % 256 == 0 for v in offs.values())
+
+
+def test_gemm_knobs_reject_bad_kinds_and_values(lib):
+    # tile order: weight-gradient kinds (4, 5) only, order 0 or 1
+    for kind in (0, 1, 2, 3, 6, -1):
+        assert lib.moe_set_gemm_tile_order(kind, 1) == moe.MOE_ERR_ARG
+    assert lib.moe_set_gemm_tile_order(4, 2) == moe.MOE_ERR_ARG
+    # epilogue stores: fp32-output kinds (1, 3, 4, 5) only, 0 or 1
+    for kind in (0, 2, 6, -1):
+        assert lib.moe_set_gemm_epilogue(kind, 1) == moe.MOE_ERR_ARG
+    assert lib.moe_set_gemm_epilogue(3, 7) == moe.MOE_ERR_ARG
+    # stages: known kinds, non-negative
+    assert lib.moe_set_gemm_stages(6, 3) == moe.MOE_ERR_ARG
+    assert lib.moe_set_gemm_stages(0, -1) == moe.MOE_ERR_ARG
+    assert lib.moe_gemm_max_stages(9, 1) == 0 and lib.moe_gemm_max_stages(0, 3) == 0
+
+
+def test_gemm_knobs_round_trip_and_stage_limits(lib):
+    """Each setter returns the previous value; the stage limits are those of
+    the shared-memory ring (one CTA per tile: 48 KB stages, CTA pairs: 32 KB)."""
+    assert [lib.moe_gemm_max_stages(k, 1) for k in range(6)] == [4, 4, 3, 4, 4, 4]
+    assert [lib.moe_gemm_max_stages(k, 2) for k in range(6)] == [6, 6, 5, 6, 6, 6]
+    for kind in (4, 5):
+        prev = lib.moe_set_gemm_tile_order(kind, 1)
+        assert lib.moe_set_gemm_tile_order(kind, prev) == 1
+    for kind in (1, 3, 4, 5):
+        prev = lib.moe_set_gemm_epilogue(kind, 1)
+        assert lib.moe_set_gemm_epilogue(kind, prev) == 1
+    for kind in range(6):
+        prev = lib.moe_set_gemm_stages(kind, 3)
+        assert lib.moe_set_gemm_stages(kind, prev) == 3
+
+
+def test_rank_bases_rejects_bad_arguments(lib):
+    ok = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_rank_bases(ok, 2, 8, ok, 2, ok, None, None) == moe.MOE_ERR_SHAPE   # rank >= G
+    assert lib.moe_rank_bases(ok, 0, 8, ok, 0, ok, None, None) == moe.MOE_ERR_SHAPE   # G = 0
+    assert lib.moe_rank_bases(ok, 2, 257, ok, 0, ok, None, None) == moe.MOE_ERR_SHAPE  # E > 256
+    assert lib.moe_rank_bases(None, 2, 8, ok, 0, ok, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_rank_bases(ok, 2, 8, ok, 0, None, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_rank_bases(odd, 2, 8, ok, 0, ok, None, None) == moe.MOE_ERR_ALIGN
+    assert lib.moe_rank_bases(ok, 2, 8, ok, 0, ok, odd, None) == moe.MOE_ERR_ALIGN
