@@ -25,6 +25,7 @@ namespace {
 int g_grid_limit = 0;
 int g_route_fusion = 1;
 int g_bwd_overlap = 1;
+int g_bwd_fused = 0;
 
 // Per device: a second stream and two events for the backward's fork/join
 // (weight gradients beside the input-gradient tail).  Created on first use,
@@ -192,6 +193,12 @@ int moe_set_gemm_pair_kinds(int mask) { return set_gemm_pair_kinds(mask); }
 int moe_set_route_fusion(int on) {
   const int prev = g_route_fusion;
   g_route_fusion = on != 0;
+  return prev;
+}
+
+int moe_set_bwd_fused_gemms(int on) {
+  const int prev = g_bwd_fused;
+  g_bwd_fused = on != 0;
   return prev;
 }
 
@@ -468,6 +475,14 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
       MOE_TRY_CUDA(cudaStreamWaitEvent(s, side->join, 0));
       return MOE_OK;
     }
+  } else if (which == 3 && g_bwd_fused) {  // dX and the W GEMMs interleaved in one launch
+    MOE_TRY_CUDA(launch_scatter_rows_bf16(dy, dest, c.T, c.k, c.d_model, G, MOE_K_COMBINE_BWD, at<int>(ws, L.err), s));
+    MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));
+    MOE_TRY_CUDA(launch_dw_reduce(a.partial_out, dest, R, L.nt_dh, dw, at<int>(ws, L.err), s));
+    MOE_TRY_CUDA(launch_route_bwd(logits, topk_idx, topk_w, dw, c.T, c.E, c.k, c.renorm, dlogits, at<int>(ws, L.err), s));
+    MOE_TRY(launch_bwd_gemms(a, s, persistent_grid()));
+    MOE_TRY_CUDA(launch_sum_rows_f32(dXp, dest, c.T, c.k, c.n_shared, c.d_model, dx, MOE_K_DISPATCH_BWD, at<int>(ws, L.err), s));
+    return MOE_OK;
   } else if (which & 1) {  // B part: input gradients (critical path)
     MOE_TRY_CUDA(launch_scatter_rows_bf16(dy, dest, c.T, c.k, c.d_model, G, MOE_K_COMBINE_BWD, at<int>(ws, L.err), s));
     MOE_TRY(launch_gemm(kDH, a, s, persistent_grid()));

@@ -51,6 +51,11 @@ struct GemmArgs {
 // Returns MOE_OK or a negative MOE_ERR_* (tensor-map encoding or launch).
 int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_override = 0);
 
+// dX, dW1/dW3 and dW2 as one persistent launch with their tiles interleaved
+// (same outputs, bit for bit, as the three separate launches).  CTA pairs
+// when all three kinds run on pairs.
+int launch_bwd_gemms(const GemmArgs& a, cudaStream_t s, int grid_override = 0);
+
 // Bit k set: kind k runs on CTA pairs (256-row tiles); clear: one CTA per
 // 128-row tile.  Returns the previous mask.
 int set_gemm_pair_kinds(int mask);

@@ -1008,8 +1008,11 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
   const int lane = threadIdx.x & 31;
   if (CG == 2 && rank == 1) {
-    if constexpr (Tr::RAGGED_K) {
-      for (int kb = 0; kb < t.nkb; ++kb) {
+    // The odd CTA's MMA warp only zeroes its part of ragged-K tails, but it
+    // walks every tile's K blocks, so its ring position stays that of the
+    // pair when a launch mixes kinds.
+    for (int kb = 0; kb < t.nkb; ++kb) {
+      if constexpr (Tr::RAGGED_K) {
         if (is_k_tail<KIND>(t, kb)) {
           const uint32_t bit = 1u << ms.stage;
           if (!mbar_wait(&ss.full[ms.stage], (ms.tail_par & bit) ? 1u : 0u, abort, p.err, where | (1 << 20)))
@@ -1020,10 +1023,10 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
           if (lane == 0) mbar_arrive_rank(&ss.ready[ms.stage], 0);
           __syncwarp();
         }
-        if (++ms.stage == NST) {
-          ms.stage = 0;
-          ms.phase ^= 1;
-        }
+      }
+      if (++ms.stage == NST) {
+        ms.stage = 0;
+        ms.phase ^= 1;
       }
     }
     return true;

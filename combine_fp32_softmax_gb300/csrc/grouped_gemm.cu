@@ -14,6 +14,7 @@
 // result: every output element is produced by exactly one tile with a fixed
 // K order.
 #include <algorithm>
+#include <cstring>
 
 #include "gemm_tiles.cuh"
 
@@ -185,6 +186,187 @@ __global__ void __launch_bounds__(Pipe<KIND, CG>::THREADS, 1) grouped_gemm_kerne
   if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------------
+// The backward's dX, dW1/dW3 and dW2 GEMMs as one persistent launch.  dX is
+// tensor-heavy and writes little; the weight-gradient kinds' short-K tiles
+// write 256 KB of fp32 per tile after a few microseconds of MMAs.  Run one
+// after the other, the write-heavy phase throttles the main loops of every
+// SM at once; here one ticket counter hands out both kinds interleaved, so
+// each SM alternates between them and the memory system sees a mix.  All
+// three only read what dH (and the forward) wrote, so no tile waits on
+// another.  Each output element is still produced by one tile with its fixed
+// K order: the bits are those of the separate launches.
+struct BwdGemmParams {
+  GemmParams x, w13, w2;  // dX, dW1/dW3, dW2
+};
+
+// Ticket i -> (kind: 0 dX, 1 dW1/dW3, 2 dW2; tile of that kind).  The dX
+// tiles sit at tickets floor(j * total / nX), spread over the whole range;
+// the other tickets take the weight-gradient tiles segment by segment in
+// the longest-first order, each segment's dW1/dW3 tiles then its dW2 tiles.
+struct MixMap {
+  int nX, tps13, tps2, total;
+};
+__device__ __forceinline__ int2 mix_decode(const MixMap& m, int i) {
+  const long long NL = m.nX, span = m.total;
+  auto upto = [&](long long v) { return v < 0 ? 0ll : min(NL, ((v + 1) * NL + span - 1) / span); };
+  const long long c = upto(i), cp = upto(i - 1);
+  if (c > cp) return make_int2(0, static_cast<int>(c - 1));
+  const int pos = static_cast<int>(i - c), per = m.tps13 + m.tps2;
+  const int oi = pos / per, local = pos - oi * per;
+  if (local < m.tps13) return make_int2(1, oi * m.tps13 + local);
+  return make_int2(2, oi * m.tps2 + (local - m.tps13));
+}
+
+constexpr int kBwdEpiBytes = Traits<kDX>::EPI_BYTES > Traits<kDW13>::EPI_BYTES
+                                 ? Traits<kDX>::EPI_BYTES
+                                 : (Traits<kDW13>::EPI_BYTES > Traits<kDW2>::EPI_BYTES ? Traits<kDW13>::EPI_BYTES
+                                                                                        : Traits<kDW2>::EPI_BYTES);
+template <int CG>
+constexpr int bwd_gemms_smem_bytes() {
+  return Pipe<kDX, CG>::STAGES * Pipe<kDX, CG>::STAGE_BYTES + kEpiWarps * kBwdEpiBytes +
+         3 * static_cast<int>(sizeof(SharedState));
+}
+constexpr int kMixSched = 6;  // scheduling words of the error region: after the six kinds'
+
+template <int CG>
+__global__ void __launch_bounds__(kThreads, 1) bwd_gemms_kernel(const __grid_constant__ BwdGemmParams bp) {
+  static_assert(Pipe<kDX, CG>::STAGE_BYTES == Pipe<kDW13, CG>::STAGE_BYTES &&
+                    Pipe<kDX, CG>::STAGE_BYTES == Pipe<kDW2, CG>::STAGE_BYTES,
+                "the three kinds share the ring");
+  constexpr int SB = Pipe<kDX, CG>::STAGE_BYTES;
+  const int NST = bp.x.nst;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  int* err = bp.x.err;
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) record_error(err, MOE_ERR_CUDA, 0x5A11);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint8_t* stg_base = smem + NST * SB;
+  SharedState* tables = reinterpret_cast<SharedState*>(stg_base + kEpiWarps * kBwdEpiBytes);
+  SharedState& ss = tables[0];   // barriers and the dX segment table
+  SharedState& s13 = tables[1];  // weight-gradient tables (segment order, tiles per segment)
+  SharedState& s2 = tables[2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+
+  if (threadIdx.x == 0) {
+    init_gemm_barriers<CG, kEpiWarps>(ss);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(&ss.tmem_base, kTmemCols);
+    tmem_relinquish<CG>();
+  }
+  build_segments<kDX, CG>(bp.x, ss);
+  build_segments<kDW13, CG>(bp.w13, s13);
+  build_segments<kDW2, CG>(bp.w2, s2);
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem_base;
+  MixMap mm;
+  mm.nX = ss.total_tiles;
+  mm.tps13 = s13.tiles_per_seg;
+  mm.tps2 = s2.tiles_per_seg;
+  mm.total = ss.total_tiles + s13.total_tiles + s2.total_tiles;
+  const int total = mm.total;
+  volatile int* abort = &ss.abort;
+  const int where0 = (kMixSched + 1) << 24 | rank << 23;
+  const int wfeed = where0 | (6 << 20);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&bp.x.tmA0);
+      tma_prefetch_desc(&bp.w13.tmA0);
+      tma_prefetch_desc(&bp.w2.tmA0);
+      ProducerState ps;
+      auto produce = [&](int ticket) {
+        const int2 kt = mix_decode(mm, ticket);
+        const int where = where0 | ticket;
+        if (kt.x == 0)
+          return produce_tile<kDX, CG>(bp.x, decode_tile<kDX, CG>(bp.x, ss, kt.y, rank), ss, smem, ps, abort, where,
+                                       NST, rank);
+        if (kt.x == 1)
+          return produce_tile<kDW13, CG>(bp.w13, decode_tile<kDW13, CG>(bp.w13, s13, kt.y, rank), ss, smem, ps,
+                                         abort, where, NST, rank);
+        return produce_tile<kDW2, CG>(bp.w2, decode_tile<kDW2, CG>(bp.w2, s2, kt.y, rank), ss, smem, ps, abort,
+                                      where, NST, rank);
+      };
+      if (rank == 0) {
+        int* ctr = err + kErrSchedWord + 2 * kMixSched;
+        int next = atomicAdd(ctr, 1);
+        for (int i = 0;; ++i) {
+          const int tile = (next < total && !*abort) ? next : -1;
+          if (tile >= 0) next = atomicAdd(ctr, 1);
+          if (!feed_put<CG>(ss, i, tile, abort, err, wfeed | (i & 0xfffff)) || tile < 0) break;
+          if (!produce(tile)) break;
+        }
+        const int takers = static_cast<int>(gridDim.x) / CG;
+        if (atomicAdd(ctr + 1, 1) == takers - 1) {
+          atomicExch(ctr, 0);
+          atomicExch(ctr + 1, 0);
+        }
+      } else {
+        for (int i = 0;; ++i) {
+          const int tile = feed_get<CG>(ss, i, rank, abort, err, wfeed | (i & 0xfffff));
+          if (tile < 0 || !produce(tile)) break;
+        }
+      }
+      if (*abort) producer_drain(ss, ps);
+    }
+  } else if (warp == 1) {
+    MmaState ms;
+    for (int i = 0;; ++i) {
+      const int tile = feed_get<CG>(ss, i, rank, abort, err, wfeed | (1 << 19) | (i & 0x7ffff));
+      if (tile < 0) break;
+      const int2 kt = mix_decode(mm, tile);
+      const int where = where0 | (2 << 20) | tile;
+      bool ok;
+      if (kt.x == 0)
+        ok = mma_tile<kDX, CG>(bp.x, decode_tile<kDX, CG>(bp.x, ss, kt.y, rank), ss, smem, tmem, ms, abort, where,
+                               NST, rank);
+      else if (kt.x == 1)
+        ok = mma_tile<kDW13, CG>(bp.w13, decode_tile<kDW13, CG>(bp.w13, s13, kt.y, rank), ss, smem, tmem, ms, abort,
+                                 where, NST, rank);
+      else
+        ok = mma_tile<kDW2, CG>(bp.w2, decode_tile<kDW2, CG>(bp.w2, s2, kt.y, rank), ss, smem, tmem, ms, abort,
+                                where, NST, rank);
+      if (!ok) break;
+    }
+    if (*abort) mma_drain<CG>(ss, ms);
+  } else {
+    EpiState es;
+    uint8_t* stg = stg_base + (warp - 2) * kBwdEpiBytes;
+    for (int i = 0;; ++i) {
+      const int tile = feed_get<CG>(ss, i, rank, abort, err, wfeed | (2 << 19) | (i & 0x7ffff));
+      if (tile < 0) break;
+      const int2 kt = mix_decode(mm, tile);
+      const int where = where0 | (4 << 20) | tile;
+      bool ok;
+      if (kt.x == 0)
+        ok = epilogue_step<kDX, CG>(bp.x, decode_tile<kDX, CG>(bp.x, ss, kt.y, rank), ss, tmem, stg, es, abort, where,
+                                    rank);
+      else if (kt.x == 1)
+        ok = epilogue_step<kDW13, CG>(bp.w13, decode_tile<kDW13, CG>(bp.w13, s13, kt.y, rank), ss, tmem, stg, es,
+                                      abort, where, rank);
+      else
+        ok = epilogue_step<kDW2, CG>(bp.w2, decode_tile<kDW2, CG>(bp.w2, s2, kt.y, rank), ss, tmem, stg, es, abort,
+                                     where, rank);
+      if (!ok) break;
+    }
+    epilogue_drain(ss, es);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc<CG>(tmem, kTmemCols);
+}
+
 // Kinds that run on CTA pairs (bit = GemmKind): measured at the 8192-token
 // DeepSeek-V2-Lite-like shape, pairs win for all six (moe_autotune re-decides
 // per layer).
@@ -265,6 +447,47 @@ int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+template <int CG>
+int launch_bwd_gemms_cg(const GemmArgs& a, cudaStream_t s, int grid_override) {
+  BwdGemmParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  if (!fill_params<kDX, CG>(a, bp.x) || !fill_params<kDW13, CG>(a, bp.w13) || !fill_params<kDW2, CG>(a, bp.w2))
+    return MOE_ERR_CUDA;
+  bp.x.nst = bp.w13.nst = bp.w2.nst = Pipe<kDX, CG>::STAGES;
+  constexpr int kSmem = bwd_gemms_smem_bytes<CG>();
+  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
+  auto kern = bwd_gemms_kernel<CG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  int grid = grid_override > 0 ? grid_override : num_sms();
+  if constexpr (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int cap = 0;
+    if (cap == 0) {
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2 * (num_sms() / 2));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) return MOE_ERR_CUDA;
+      cap = n;
+    }
+    grid = 2 * std::max(1, std::min(cap, grid / 2));
+  }
+  cfg.gridDim = dim3(grid);
+  TraceScope trace_scope(MOE_K_BWD_GEMMS, s);
+  if (cudaLaunchKernelEx(&cfg, kern, bp) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 template <int KIND>
 int launch_any(const GemmArgs& a, cudaStream_t s, int grid_override) {
   return (g_pair_kinds >> KIND) & 1 ? launch_kind<KIND, 2>(a, s, grid_override)
@@ -283,6 +506,11 @@ int launch_gemm(GemmKind kind, const GemmArgs& a, cudaStream_t s, int grid_overr
     case kDW2: return launch_any<kDW2>(a, s, grid_override);
   }
   return MOE_ERR_ARG;
+}
+
+int launch_bwd_gemms(const GemmArgs& a, cudaStream_t s, int grid_override) {
+  const bool pairs = ((g_pair_kinds >> kDX) & 1) && ((g_pair_kinds >> kDW13) & 1) && ((g_pair_kinds >> kDW2) & 1);
+  return pairs ? launch_bwd_gemms_cg<2>(a, s, grid_override) : launch_bwd_gemms_cg<1>(a, s, grid_override);
 }
 
 int gemm_pair_capacity(GemmKind kind) {

@@ -50,7 +50,7 @@ void settle_locked() {
 const char* kNames[MOE_K_COUNT] = {"route",     "hist",          "scan",      "scatter",   "gather",
                                    "gemm1_swiglu", "gemm2_scale", "combine",   "combine_bwd", "gemm_dh",
                                    "dw_reduce", "route_bwd",     "gemm_dx",   "dispatch_bwd", "gemm_dw13",
-                                   "gemm_dw2",  "megakernel", "megakernel_bwd", "route_tables"};
+                                   "gemm_dw2",  "megakernel", "megakernel_bwd", "route_tables", "bwd_gemms"};
 
 }  // namespace
 

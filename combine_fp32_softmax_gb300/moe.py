@@ -75,6 +75,7 @@ _SIGS = {
     "moe_gemm_max_stages": ([_I, _I], _I),
     "moe_set_bwd_overlap": ([_I], _I),
     "moe_set_route_fusion": ([_I], _I),
+    "moe_set_bwd_fused_gemms": ([_I], _I),
     "moe_autotune": ([_CFG] + [_P] * 15 + [_I, _P, ctypes.POINTER(moe_tune_result)], _I),
     "moe_debug_skip_megakernel_task": ([_I], _I),
     "moe_debug_megakernel_trace": ([_P, _I], _I),
@@ -88,7 +89,7 @@ _SIGS = {
 TRACE_KINDS = ["route", "hist", "scan", "scatter", "gather", "gemm1_swiglu", "gemm2_scale", "combine",
                "combine_bwd", "gemm_dh", "dw_reduce", "route_bwd", "gemm_dx", "dispatch_bwd", "gemm_dw13",
                "gemm_dw2", "megakernel", "megakernel_bwd",
-               "route_tables"]
+               "route_tables", "bwd_gemms"]
 
 _lib = None
 
@@ -294,6 +295,11 @@ def moe_gemm_max_stages(kind: int, cta_group: int) -> int:
 def moe_set_bwd_overlap(on: bool) -> int:
     """Weight-gradient GEMMs of the backward on a second stream beside the dX tail. Returns the previous setting."""
     return int(lib().moe_set_bwd_overlap(int(bool(on))))
+
+
+def moe_set_bwd_fused_gemms(on: bool) -> int:
+    """dX, dW1/dW3 and dW2 of the layer backward as one interleaved launch. Returns the previous setting."""
+    return int(lib().moe_set_bwd_fused_gemms(int(bool(on))))
 
 
 def moe_set_route_fusion(on: bool) -> int:

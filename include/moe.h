@@ -330,6 +330,24 @@ int moe_set_route_fusion(int on);
  * Process-wide, not thread-safe. */
 int moe_set_bwd_overlap(int on);
 
+/* Backward GEMMs of moe_layer_bwd with which == 3 (without
+ * MOE_BWD_MEGAKERNEL).  On, dX, dW1/dW3 and dW2 run as one persistent
+ * launch whose single ticket counter interleaves their tiles: dX's tiles are
+ * spread evenly over the tickets, and the weight-gradient tiles fill the rest,
+ * longest segments first.  The tensor-heavy dX tiles and the write-heavy
+ * short-K weight-gradient tiles then share the SMs and the memory system
+ * instead of taking turns (GraphPP page, section 2: the W part is deferrable
+ * work that can fill the B part's gaps; UniEP page, section 2.2: dynamic SM
+ * scheduling over one task space).  The dw reduce and router backward run
+ * before it, and the dx sum after it, on the caller's stream.  Off (the
+ * default): dX, then the weight-gradient GEMMs on the B/W overlap's second
+ * stream.  Same bits either way.  The one launch is shorter than the
+ * three kernels back to back, but the whole step measured slower than the
+ * default at every layer tried, since the default overlaps the W GEMMs with
+ * dX and the dx sum.  Returns the previous setting.
+ * Process-wide, not thread-safe. */
+int moe_set_bwd_fused_gemms(int on);
+
 /* Selects, per grouped-GEMM kind, the tile shape: bit k of `mask` set runs
  * kind k on CTA pairs (thread-block clusters of two; the pair computes a
  * 256 x 256 tile with tcgen05 MMAs of the CTA group of two, each CTA holding
@@ -463,7 +481,8 @@ enum {
   MOE_K_MEGAKERNEL = 16,  /* forward MegaKernel */
   MOE_K_MEGAKERNEL_BWD = 17, /* backward (input-gradient) MegaKernel */
   MOE_K_ROUTE_TABLES = 18, /* router + histogram + scan + scatter, one launch */
-  MOE_K_COUNT = 19
+  MOE_K_BWD_GEMMS = 19,   /* dX, dW1/dW3 and dW2 interleaved in one launch */
+  MOE_K_COUNT = 20
 };
 /* Testing aid for failure detection (no device fault involved): the forward
  * MegaKernel claims task `ticket` but never runs or signals it, so the

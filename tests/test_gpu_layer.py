@@ -67,7 +67,8 @@ def _sched_words_clear(ws, cfg):
     """The routing grid barrier's arrival count and every grouped-GEMM kind's
     tile-ticket counter and finished-CTA count are back at 0."""
     err = moe.ws_view(ws, cfg, "err").cpu().numpy()
-    return err[8] == 0 and not err[16:16 + 2 * len(moe.GEMM_KINDS)].any()
+    # six kinds' words, then the interleaved backward GEMMs' pair
+    return err[8] == 0 and not err[16:16 + 2 * (len(moe.GEMM_KINDS) + 1)].any()
 
 
 def test_results_do_not_depend_on_grid_size():
@@ -314,6 +315,46 @@ def test_b_and_w_parts_split():
                       part["topk_w"], ws, None, None, part["dW1"], part["dW3"], part["dW2"], which=2)
     for k in full:
         assert torch.equal(full[k], part[k]), k
+
+
+@pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
+def test_interleaved_backward_gemms_equal_separate_launches(cfg):
+    """dX, dW1/dW3 and dW2 as one launch with interleaved tiles (both tile
+    shapes) give the bits of the separate launches: every output, dXp, and
+    the scheduling words back at 0."""
+    g = to_dev(make_layer_inputs(cfg, seed=26))
+    ref, ref_ws = run_layer(cfg, g)
+    ref = {k: v.clone() for k, v in ref.items()}
+    prev = moe.moe_set_bwd_fused_gemms(True)
+    saved = moe.moe_set_gemm_pair_kinds(moe.ALL_PAIR_KINDS)
+    try:
+        for mask in (moe.ALL_PAIR_KINDS, 0):
+            moe.moe_set_gemm_pair_kinds(mask)
+            out, ws = run_layer(cfg, g, fill=float("nan"))
+            assert device_error(ws) == (0, 0)
+            assert _sched_words_clear(ws, cfg)
+            for k in ref:
+                assert torch.equal(ref[k], out[k]), (mask, k)
+            assert torch.equal(moe.ws_view(ws, cfg, "dXp"), moe.ws_view(ref_ws, cfg, "dXp"))
+    finally:
+        moe.moe_set_bwd_fused_gemms(bool(prev))
+        moe.moe_set_gemm_pair_kinds(saved)
+
+
+def test_interleaved_backward_gemms_do_not_depend_on_grid_size():
+    cfg = SKEW
+    g = to_dev(make_layer_inputs(cfg, seed=27))
+    ref = _digest(run_layer(cfg, g)[0])
+    prev = moe.moe_set_bwd_fused_gemms(True)
+    try:
+        for n in (1, 7, 0):
+            moe.moe_set_grid_limit(n)
+            out, ws = run_layer(cfg, g)
+            assert device_error(ws) == (0, 0) and _sched_words_clear(ws, cfg)
+            assert _digest(out) == ref, n
+    finally:
+        moe.moe_set_grid_limit(0)
+        moe.moe_set_bwd_fused_gemms(bool(prev))
 
 
 @pytest.mark.parametrize("cfg", LAYER_CFGS, ids=lambda c: c.name)
