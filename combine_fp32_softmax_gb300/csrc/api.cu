@@ -145,7 +145,7 @@ int route_tables(const moe_cfg& c, const WsLayout& L, void* ws, const float* log
 
 int fwd_gemms(const moe_cfg& c, const WsLayout& L, void* ws, const uint16_t* Xp, const uint16_t* x,
               const int32_t* offsets, const int32_t* row_slot, const float* topk_w, const uint16_t* W1,
-              const uint16_t* W3, const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Op, cudaStream_t s) {
+              const uint16_t* W3, const uint16_t* W2, uint16_t* Hw, uint16_t* AB, float* Op, cudaStream_t s) {
   GemmArgs a = base_args(c, ws, L);
   a.offsets = offsets;
   a.row_slot = row_slot;
@@ -155,8 +155,8 @@ int fwd_gemms(const moe_cfg& c, const WsLayout& L, void* ws, const uint16_t* Xp,
   a.W1 = W1;
   a.W3 = W3;
   a.W2 = W2;
-  a.H = H;
-  a.H_out = H;
+  a.Hw = Hw;
+  a.Hw_out = Hw;
   a.AB_out = AB;
   a.Op_out = Op;
   MOE_TRY(launch_gemm(kG1, a, s, persistent_grid()));
@@ -290,12 +290,12 @@ int moe_rank_bases(const int32_t* all_counts, int G, int E, const int32_t* owner
 
 int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x, const int32_t* offsets,
                           const int32_t* row_slot, const float* topk_w, const uint16_t* W1, const uint16_t* W3,
-                          const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime, void* ws, void* stream) {
+                          const uint16_t* W2, uint16_t* Hw, uint16_t* AB, float* Oprime, void* ws, void* stream) {
   MOE_TRY(check_cfg(cfg));
-  MOE_TRY(check_ptrs({Xp, offsets, row_slot, topk_w, W1, W3, W2, H, Oprime}, {x, AB}, ws));
+  MOE_TRY(check_ptrs({Xp, offsets, row_slot, topk_w, W1, W3, W2, Hw, Oprime}, {x, AB}, ws));
   if (cfg->n_shared > 0 && !x) return MOE_ERR_ARG;
   const WsLayout L = ws_layout(*cfg);
-  return fwd_gemms(*cfg, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, H, AB, Oprime,
+  return fwd_gemms(*cfg, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, Hw, AB, Oprime,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -326,7 +326,7 @@ int moe_layer_fwd(const moe_cfg* cfg, const float* logits, const uint16_t* x, co
   uint16_t* Xp = at<uint16_t>(ws, L.Xp);
   float* Op = at<float>(ws, L.Op);
   MOE_TRY_CUDA(launch_scatter_rows_bf16(x, dest, c.T, c.k, c.d_model, Xp, MOE_K_GATHER, at<int>(ws, L.err), s));
-  MOE_TRY(fwd_gemms(c, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, at<uint16_t>(ws, L.H),
+  MOE_TRY(fwd_gemms(c, L, ws, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, at<uint16_t>(ws, L.Hw),
                     at<uint16_t>(ws, L.AB), Op, s));
   MOE_TRY_CUDA(launch_sum_rows_f32(Op, dest, c.T, c.k, c.n_shared, c.d_model, y, MOE_K_COMBINE, at<int>(ws, L.err), s));
   return MOE_OK;
@@ -344,13 +344,13 @@ int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_t
 int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint16_t* dy, const uint16_t* Xp,
                               const uint16_t* x, const int32_t* offsets, const int32_t* row_slot, const int32_t* dest,
                               const float* topk_w, const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
-                              const uint16_t* H, const uint16_t* AB, uint16_t* dAB, uint16_t* Hw, float* dw,
+                              const uint16_t* Hw, const uint16_t* AB, uint16_t* dAB, float* dw,
                               float* dXp, float* dW1, float* dW3, float* dW2, int which, void* ws, void* stream) {
   MOE_TRY(check_cfg(cfg));
   if (which < 1 || which > 3) return MOE_ERR_ARG;
-  MOE_TRY(check_ptrs({G, dy, offsets, row_slot, dAB, Hw}, {Xp, x, dest, topk_w, W1, W3, W2, H, AB, dw, dXp, dW1, dW3, dW2}, ws));
-  if ((which & 1) && !(dest && topk_w && W1 && W3 && W2 && H && AB && dw && dXp)) return MOE_ERR_ARG;
-  if ((which & 2) && !(Xp && dW1 && dW3 && dW2)) return MOE_ERR_ARG;
+  MOE_TRY(check_ptrs({G, dy, offsets, row_slot, dAB}, {Xp, x, dest, topk_w, W1, W3, W2, Hw, AB, dw, dXp, dW1, dW3, dW2}, ws));
+  if ((which & 1) && !(dest && topk_w && W1 && W3 && W2 && AB && dw && dXp)) return MOE_ERR_ARG;
+  if ((which & 2) && !(Xp && Hw && dW1 && dW3 && dW2)) return MOE_ERR_ARG;
   if (cfg->n_shared > 0 && (which & 2) && !x) return MOE_ERR_ARG;
   const moe_cfg& c = *cfg;
   const WsLayout L = ws_layout(c);
@@ -364,14 +364,12 @@ int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint1
   a.W1 = W1;
   a.W3 = W3;
   a.W2 = W2;
-  a.H = H;
   a.AB = AB;
   a.G = G;
   a.dy = dy;
   a.dAB = dAB;
   a.Hw = Hw;
   a.dAB_out = dAB;
-  a.Hw_out = Hw;
   a.partial_out = at<float>(ws, L.partial);
   a.dXp_out = dXp;
   a.dW1_out = dW1;
@@ -427,7 +425,7 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
   const int32_t* dest = at<int32_t>(ws, L.dest);
   uint16_t* G = at<uint16_t>(ws, L.G);
   uint16_t* dAB = at<uint16_t>(ws, L.dAB);
-  uint16_t* Hw = at<uint16_t>(ws, L.Hw);
+  const uint16_t* Hw = at<uint16_t>(ws, L.Hw);
   float* dXp = at<float>(ws, L.dXp);
   float* dw = at<float>(ws, L.dw);
   GemmArgs a = base_args(c, ws, L);
@@ -439,14 +437,12 @@ int moe_layer_bwd(const moe_cfg* cfg, const uint16_t* dy, const float* logits, c
   a.W1 = W1;
   a.W3 = W3;
   a.W2 = W2;
-  a.H = at<uint16_t>(ws, L.H);
   a.AB = at<uint16_t>(ws, L.AB);
   a.G = G;
   a.dy = dy;
   a.dAB = dAB;
   a.Hw = Hw;
   a.dAB_out = dAB;
-  a.Hw_out = Hw;
   a.partial_out = at<float>(ws, L.partial);
   a.dXp_out = dXp;
   a.dW1_out = dW1;

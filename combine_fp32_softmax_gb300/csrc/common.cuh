@@ -91,7 +91,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Offsets of the regions inside the caller's workspace (bytes from ws).
 struct WsLayout {
   size_t err, hist, base, counts, offsets, dest, row_token, row_slot;
-  size_t Xp, AB, H, Op, G, dAB, Hw, dXp, partial, dw, mk;
+  size_t Xp, AB, Hw, Op, G, dAB, dXp, partial, dw, mk;
   size_t total;
   int nb_route;  // router/permutation blocks
   int nt_dh;     // column tiles of the dH GEMM (partial dot products per row)
@@ -125,11 +125,10 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.row_slot = take(sizeof(int) * R);
   L.Xp = take(2 * R * d);
   L.AB = take(2 * Rs * 2 * f);
-  L.H = take(2 * Rs * f);
+  L.Hw = take(2 * Rs * f);
   L.Op = take(4 * Rs * d);
   L.G = take(2 * R * d);
   L.dAB = take(2 * Rs * 2 * f);
-  L.Hw = take(2 * Rs * f);
   L.dXp = take(4 * Rs * d);
   L.partial = take(4 * R * L.nt_dh);  // one partial dot per (row, 256-column tile)
   L.dw = take(4 * T * k);

@@ -8,9 +8,9 @@
 namespace moe {
 
 enum GemmKind : int {
-  kG1 = 0,    // forward gate/up: A = Xp (x for shared rows), B = [W1 | W3] -> H (+ [a|b])
-  kG2 = 1,    // forward down:    A = H, B = W2 -> O' = w * o (fp32)
-  kDH = 2,    // backward dH:     A = G (dy for shared rows), B = W2 (MN-major) -> dAB, Hw, dw partials
+  kG1 = 0,    // forward gate/up: A = Xp (x for shared rows), B = [W1 | W3] -> Hw = w * h (+ [a|b])
+  kG2 = 1,    // forward down:    A = Hw, B = W2 -> O' = w * o (fp32)
+  kDH = 2,    // backward dH:     A = G (dy for shared rows), B = W2 (MN-major) -> dAB, dw partials
   kDX = 3,    // backward dX:     A = dAB, B = [W1 ; W3] (MN-major) -> dXp (fp32)
   kDW13 = 4,  // backward dW1/3:  A = dAB^T, B = Xp^T (x^T for shared), ragged K -> dW1, dW3 (fp32)
   kDW2 = 5,   // backward dW2:    A = G^T (dy^T for shared), B = Hw^T, ragged K -> dW2 (fp32)
@@ -28,18 +28,16 @@ struct GemmArgs {
   const uint16_t* W1;
   const uint16_t* W3;
   const uint16_t* W2;
-  const uint16_t* H;
   const uint16_t* AB;
   const uint16_t* G;
   const uint16_t* dy;
   const uint16_t* dAB;
   const uint16_t* Hw;
   // outputs
-  uint16_t* H_out;
+  uint16_t* Hw_out;
   uint16_t* AB_out;
   float* Op_out;
   uint16_t* dAB_out;
-  uint16_t* Hw_out;
   float* partial_out;
   float* dXp_out;
   float* dW1_out;

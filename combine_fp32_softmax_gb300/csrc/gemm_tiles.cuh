@@ -17,8 +17,8 @@
 // Design (one CTA per SM, 192 threads; CG = 1 or 2 CTAs per tile):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //               (256 x 64, or this CTA's 128 x 64 half on a CTA pair) into
-//               a shared-memory ring: 3-4 stages of 48 KB (one CTA per
-//               tile), 5-6 of 32 KB (pairs).  MN-major operands come as one
+//               a shared-memory ring: 4 stages of 48 KB (one CTA per
+//               tile), 6 of 32 KB (pairs).  MN-major operands come as one
 //               3D box per operand (map3d_mn).
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma from one lane
 //               (M=128, or M=256 on a pair from the even CTA; N=256, K=16,
@@ -31,7 +31,7 @@
 //               tensor stores (coalesced, asynchronous).  Warps whose 32
 //               rows are not all valid (a segment's last m-tile) store
 //               their valid rows directly.  The dH epilogue TMA-loads its
-//               elementwise inputs ([a|b], H) per warp, double-buffered,
+//               elementwise inputs ([a|b]) per warp, double-buffered,
 //               and stages its outputs in the buffer the inputs came in.
 //               The weight-gradient kinds run warps 2-9: two per TMEM lane
 //               quadrant, each on half of the tile's columns.  The fp32
@@ -78,7 +78,7 @@ constexpr int kChunkBytes = 32 * 64;  // one staged chunk: 32 rows x 64 bytes (S
 struct GemmParams {
   CUtensorMap tmA0, tmA1, tmB0, tmB1;  // operands
   CUtensorMap tmO0, tmO1;              // outputs written with TMA stores
-  CUtensorMap tmX0, tmX1;              // dH epilogue inputs: [a|b] and H
+  CUtensorMap tmX0;                    // dH epilogue input: [a|b]
   int T, d, f, E, k, S, R;
   int N;       // output columns per expert
   int Mw;      // ragged-K kinds: output rows per expert
@@ -105,14 +105,14 @@ struct Traits {
   static constexpr bool RAGGED_K = (KIND == kDW13 || KIND == kDW2);
   static constexpr int BNE = (KIND == kG1) ? 128 : 256;  // output columns per tile
 
-  static constexpr int STAGES = (KIND == kDH) ? 3 : 4;
+  static constexpr int STAGES = 4;
   // fp32 kinds: 16-column chunks, two staging buffers in flight.
   static constexpr int F32_ROUNDS = 2;
-  // per epilogue warp: GEMM 1 one chunk of H, a, b; dH two buffers of three
-  // chunks, each taking a chunk's [a, b, H] inputs and then, in place, its
-  // dA, dB, Hw outputs; fp32 kinds F32_ROUNDS output chunks.
+  // per epilogue warp: GEMM 1 one chunk of Hw, a, b; dH two buffers of two
+  // chunks, each taking a chunk's [a, b] inputs and then, in place, its
+  // dA, dB outputs; fp32 kinds F32_ROUNDS output chunks.
   static constexpr int EPI_BYTES = (KIND == kG1)   ? 3 * kChunkBytes
-                                   : (KIND == kDH) ? 6 * kChunkBytes
+                                   : (KIND == kDH) ? 4 * kChunkBytes
                                                    : F32_ROUNDS * kChunkBytes;
 };
 
@@ -129,11 +129,11 @@ struct Pipe {
   // Epilogue warps of the stand-alone kernel: two per TMEM lane quadrant,
   // each taking half of a tile's columns, for the weight-gradient kinds
   // (their short-K tiles finish the MMAs about as fast as four warps move
-  // 256 fp32 columns out).  dH keeps four: eight would cost it a pipeline
-  // stage, which measured 11-16% slower.
+  // 256 fp32 columns out).  dH keeps four: one warp sums a row's dw dot over
+  // the whole tile, and eight would cost it a pipeline stage.
   static constexpr int EPI_WARPS = (KIND == kDW13 || KIND == kDW2) ? kMaxEpiWarps : kEpiWarps;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : (KIND == kDH ? 5 : 6);
+  static constexpr int STAGES = CG == 1 ? Traits<KIND>::STAGES : 6;
 };
 
 struct SharedState {
@@ -509,7 +509,6 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
   int orow0;                    // tensor-map row of the warp's first row
   float* optr;                  // this lane's output row (fallback path)
   bool full, rowok;
-  float scale = 1.f;
   int N;
   if constexpr (KIND == kG2 || KIND == kDX) {
     N = p.d;
@@ -518,7 +517,6 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
     const size_t grow = static_cast<size_t>(t.grow0) + r;
     orow0 = t.grow0 + 32 * q;
     optr = static_cast<float*>(p.out0) + grow * N;
-    if constexpr (KIND == kG2) scale = es.w;
   } else if constexpr (KIND == kDW13) {
     N = p.d;
     const int mw0 = t.m0 + 32 * q;  // the warp's 32 rows all sit in dW1 or all in dW3 (f % 32 == 0)
@@ -556,10 +554,6 @@ __device__ __forceinline__ void epilogue_f32(const GemmParams& p, const TileInfo
   for (int j = j0; j < j1; ++j) {
     const bool more = j + 1 < j1;
     if (more && !zero) tmem_ld_32x16(tacc + 16 * (j + 1), nxt);
-    if constexpr (KIND == kG2) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) cur[i] = __float_as_uint(scale * __uint_as_float(cur[i]));
-    }
     const int n = t.n0 + 16 * j;
     if (full) {
       uint8_t* buf = stg + (es.chunks % NR) * kChunkBytes;
@@ -617,12 +611,6 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
     valid_rows = p.d - t.m0 - 32 * q;
   }
   const bool zero = Traits<KIND>::RAGGED_K && t.nkb == 0;  // empty expert: exact zeros
-  // routing weight of each row this thread writes (GEMM 2 only)
-  float wrow[4] = {1.f, 1.f, 1.f, 1.f};
-  if constexpr (KIND == kG2) {
-#pragma unroll
-    for (int h = 0; h < 4; ++h) wrow[h] = __shfl_sync(0xffffffffu, es.w, 16 * (h >> 1) + 8 * (h & 1) + quad);
-  }
   // this warp's columns: [g0, ncols) of the tile, in groups of 32
   const int span = 256 / nparts;
   const int g0 = part * span;
@@ -651,7 +639,6 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {       // rows quad (sub 0) and quad + 8 (sub 1) of this half
-        const int h = 2 * half + sub;
         const int row = 16 * half + 8 * sub + quad;
 #pragma unroll
         for (int jp = 0; jp < 2; ++jp) {        // repetitions 2jp and 2jp + 1
@@ -672,12 +659,6 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
             o = make_float4(__uint_as_float(s0), __uint_as_float(s1), __uint_as_float(b[0]), __uint_as_float(b[1]));
             col = g + 8 * j1 + 2 * (c - 1);
           }
-          if constexpr (KIND == kG2) {
-            o.x *= wrow[h];
-            o.y *= wrow[h];
-            o.z *= wrow[h];
-            o.w *= wrow[h];
-          }
           if (row < valid_rows && t.n0 + col < N)
             *reinterpret_cast<float4*>(base + static_cast<long long>(row) * ld + t.n0 + col) = o;
         }
@@ -695,7 +676,8 @@ __device__ __forceinline__ void epilogue_f32_direct(const GemmParams& p, const T
 }
 
 // GEMM 1: columns [0,128) of the accumulator hold a (gate), [128,256) hold b
-// (up) for outputs n0..n0+127; H = bf16(silu(a) * b), optionally [a|b].
+// (up) for outputs n0..n0+127; Hw = bf16(w * (silu(a) * b)) with the row's
+// routing weight (1 for shared rows), optionally [a|b].
 __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo& t, int q, uint32_t tacc,
                                             uint8_t* stg, EpiState& es) {
   const int lane = threadIdx.x & 31;
@@ -703,8 +685,9 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
   const bool rowok = r < t.rows, full = t.rows >= 32 * q + 32;
   const size_t grow = static_cast<size_t>(t.grow0) + r;
   const int orow0 = t.grow0 + 32 * q;
-  uint16_t* H = static_cast<uint16_t*>(p.out0);
+  uint16_t* Hw = static_cast<uint16_t*>(p.out0);
   uint16_t* AB = static_cast<uint16_t*>(p.out1);
+  const float w = es.w;
   es.chunks = 0;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -719,7 +702,7 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
     for (int i = 0; i < 16; ++i) {
       const float a0 = __uint_as_float(a[2 * i]), a1 = __uint_as_float(a[2 * i + 1]);
       const float b0 = __uint_as_float(b[2 * i]), b1 = __uint_as_float(b[2 * i + 1]);
-      hp[i] = pack_bf16(__fdividef(a0, 1.f + __expf(-a0)) * b0, __fdividef(a1, 1.f + __expf(-a1)) * b1);
+      hp[i] = pack_bf16(w * (__fdividef(a0, 1.f + __expf(-a0)) * b0), w * (__fdividef(a1, 1.f + __expf(-a1)) * b1));
       ap[i] = pack_bf16(a0, a1);
       bp[i] = pack_bf16(b0, b1);
     }
@@ -741,7 +724,7 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
       }
       ++es.chunks;
     } else if (rowok) {
-      store_words16(H + grow * p.f + n, hp);
+      store_words16(Hw + grow * p.f + n, hp);
       if (p.has_ab) {
         store_words16(AB + grow * 2 * p.f + n, ap);
         store_words16(AB + grow * 2 * p.f + p.f + n, bp);
@@ -750,11 +733,13 @@ __device__ __forceinline__ void epilogue_g1(const GemmParams& p, const TileInfo&
   }
 }
 
-// dH: inputs a, b, H of the tile's 32-column chunks are TMA-loaded per warp
-// into two buffers (3 chunks of 2 KB each); a chunk's outputs dA, dB, Hw are
+// dH: inputs a, b of the tile's 32-column chunks are TMA-loaded per warp
+// into two buffers (2 chunks of 2 KB each); a chunk's outputs dA, dB are
 // staged in the buffer its inputs came in, which is refilled (two chunks
 // ahead) once the output stores have read it.  Sharing the buffers this way
-// left room for a fifth pipeline stage on CTA pairs.
+// leaves room for six pipeline stages on CTA pairs.  h for the dw dot is
+// formed again from the same bf16 a and b (the forward kept only w * h), so
+// dH reads 2 and writes 2 bf16 values per element.
 __device__ __forceinline__ int dh_chunks(const GemmParams& p, const TileInfo& t) {
   return min(8, (p.f - t.n0 + 31) / 32);
 }
@@ -768,13 +753,12 @@ __device__ __forceinline__ void dh_issue_inputs(const GemmParams& p, const TileI
   const int buf = es.auxn & 1;
   ++es.auxn;
   if ((threadIdx.x & 31) == 0) {
-    uint8_t* in = stg + buf * 3 * kChunkBytes;
+    uint8_t* in = stg + buf * 2 * kChunkBytes;
     uint64_t* bar = &ss.aux[epi_warp()][buf];
     const int n = t.n0 + 32 * c, row0 = t.grow0 + 32 * q;
-    mbar_arrive_expect_tx(bar, 3 * kChunkBytes);
+    mbar_arrive_expect_tx(bar, 2 * kChunkBytes);
     tma_load_2d(in, &p.tmX0, bar, n, row0);                    // a
     tma_load_2d(in + kChunkBytes, &p.tmX0, bar, p.f + n, row0);  // b
-    tma_load_2d(in + 2 * kChunkBytes, &p.tmX1, bar, n, row0);  // H
   }
   es.auxpend |= 1u << buf;
 }
@@ -798,7 +782,6 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
   const int orow0 = t.grow0 + 32 * q;
   const float w = es.w;
   uint16_t* dAB = static_cast<uint16_t*>(p.out0);
-  uint16_t* Hw = static_cast<uint16_t*>(p.out1);
   const int2 range = dh_range(p, t, part, nparts);
   const int c0 = range.x, c1 = range.y;
   const uint32_t first = es.auxn - min(2, c1 - c0);  // input chunk index of chunk c0
@@ -814,45 +797,40 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
     uint32_t g[32];
     tmem_ld_32x32(tacc + 32 * c, g);
     tmem_ld_wait();
-    const uint8_t* in = stg + buf * 3 * kChunkBytes;
-    uint32_t aw[16], bw[16], hw[16];
+    const uint8_t* in = stg + buf * 2 * kChunkBytes;
+    uint32_t aw[16], bw[16];
     load_row64(in, lane, aw);
     load_row64(in + kChunkBytes, lane, bw);
-    load_row64(in + 2 * kChunkBytes, lane, hw);
     // every lane has its rows in registers: the buffer now takes the outputs
     __syncwarp();
-    uint32_t ra[16], rb[16], rh[16];
+    uint32_t ra[16], rb[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-      float dA2[2], dB2[2], hw2[2];
+      float dA2[2], dB2[2];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const float a = half ? bf16_hi(aw[u]) : bf16_lo(aw[u]);
         const float b = half ? bf16_hi(bw[u]) : bf16_lo(bw[u]);
-        const float h = half ? bf16_hi(hw[u]) : bf16_lo(hw[u]);
         const float graw = __uint_as_float(g[2 * u + half]);
-        dot += graw * h;
-        const float dH = w * graw;
         const float s = __fdividef(1.f, 1.f + __expf(-a));
+        const float as = a * s;
+        dot += graw * (as * b);
+        const float dH = w * graw;
         dA2[half] = dH * b * s * (1.f + a * (1.f - s));
-        dB2[half] = dH * (a * s);
-        hw2[half] = w * h;
+        dB2[half] = dH * as;
       }
       ra[u] = pack_bf16(dA2[0], dA2[1]);
       rb[u] = pack_bf16(dB2[0], dB2[1]);
-      rh[u] = pack_bf16(hw2[0], hw2[1]);
     }
-    uint8_t* out = stg + buf * 3 * kChunkBytes;
+    uint8_t* out = stg + buf * 2 * kChunkBytes;
     if (full) {
       // Each lane overwrites only the row it read.
       stage_row64(out, lane, ra);
       stage_row64(out + kChunkBytes, lane, rb);
-      stage_row64(out + 2 * kChunkBytes, lane, rh);
       staging_publish();
       if (lane == 0) {
         tma_store_2d(&p.tmO0, out, n, orow0);
         tma_store_2d(&p.tmO0, out + kChunkBytes, p.f + n, orow0);
-        tma_store_2d(&p.tmO1, out + 2 * kChunkBytes, n, orow0);
         bulk_commit();
         if (c + 2 < c1) bulk_wait_read<0>();  // the stores have read the buffer before it is refilled
       }
@@ -862,7 +840,6 @@ __device__ __forceinline__ bool epilogue_dh(const GemmParams& p, const TileInfo&
       if (rowok) {
         store_words16(dAB + grow * 2 * p.f + n, ra);
         store_words16(dAB + grow * 2 * p.f + p.f + n, rb);
-        store_words16(Hw + grow * p.f + n, rh);
       }
       fence_proxy_async_smem();  // the inputs' generic reads before the refill's TMA writes
       __syncwarp();
@@ -1118,7 +1095,7 @@ __device__ __forceinline__ bool epilogue_step(const GemmParams& p, const TileInf
   ++es.it;
   if constexpr (KIND == kDH)
     if (t.active) dh_prefetch(p, t, q, stg, ss, es, part, NP);
-  if constexpr (KIND == kG2 || KIND == kDH)
+  if constexpr (KIND == kG1 || KIND == kDH)
     if (t.active) es.w = row_weight(p, t, q);
   if (!mbar_wait(&ss.tfull[acc], aph, abort, p.err, where)) return false;
   tc_fence_after();
@@ -1246,15 +1223,15 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA1, alt(a.x, a.Xp), d, a.x ? T : R, 64, 128);
     ok &= map2d(&p.tmB0, a.W1, d, nexp * f, 64, 128);
     ok &= map2d(&p.tmB1, a.W3, d, nexp * f, 64, 128);
-    ok &= map_chunk_bf16(&p.tmO0, a.H_out, f, Rs);
+    ok &= map_chunk_bf16(&p.tmO0, a.Hw_out, f, Rs);
     p.has_ab = a.AB_out != nullptr;
     if (p.has_ab) ok &= map_chunk_bf16(&p.tmO1, a.AB_out, 2 * f, Rs);
     p.N = a.f;
     p.K = a.d;
-    p.out0 = a.H_out;
+    p.out0 = a.Hw_out;
     p.out1 = a.AB_out;
   } else if constexpr (KIND == kG2) {
-    ok &= map2d(&p.tmA0, a.H, f, Rs, 64, 128);
+    ok &= map2d(&p.tmA0, a.Hw, f, Rs, 64, 128);
     ok &= map2d(&p.tmB0, a.W2, f, nexp * d, 64, 256 / CG);
     ok &= map_chunk_f32(&p.tmO0, a.Op_out, d, Rs);
     p.N = a.d;
@@ -1265,13 +1242,10 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA1, a.dy, d, T, 64, 128);
     ok &= map3d_mn(&p.tmB0, a.W2, f, nexp * d, 4 / CG);
     ok &= map_chunk_bf16(&p.tmO0, a.dAB_out, 2 * f, Rs);
-    ok &= map_chunk_bf16(&p.tmO1, a.Hw_out, f, Rs);
     ok &= map_chunk_bf16(&p.tmX0, a.AB, 2 * f, Rs);
-    ok &= map_chunk_bf16(&p.tmX1, a.H, f, Rs);
     p.N = a.f;
     p.K = a.d;
     p.out0 = a.dAB_out;
-    p.out1 = a.Hw_out;
     p.out_partial = a.partial_out;
   } else if constexpr (KIND == kDX) {
     ok &= map2d(&p.tmA0, a.dAB, 2 * f, Rs, 64, 128);

@@ -116,17 +116,17 @@ constexpr int mega_smem_bytes() {
          static_cast<int>(sizeof(MegaShared));
 }
 static_assert(mega_smem_bytes<kG1, kG2, 4>() <= 232448, "shared memory budget of one CTA");
-static_assert(mega_smem_bytes<kDH, kDX, 3>() <= 232448, "shared memory budget of one CTA");
+static_assert(mega_smem_bytes<kDH, kDX, 4>() <= 232448, "shared memory budget of one CTA");
 static_assert(mega_smem_bytes<kG1, kG2, 6, 2>() <= 232448, "shared memory budget of one CTA");
-static_assert(mega_smem_bytes<kDH, kDX, 5, 2>() <= 232448, "shared memory budget of one CTA");
+static_assert(mega_smem_bytes<kDH, kDX, 6, 2>() <= 232448, "shared memory budget of one CTA");
 // the token sums' staging fits the ring and epilogue staging of every shape
 template <int KA, int KB, int NST, int CG>
 constexpr bool sum_staging_fits() {
   return NST * Mega<KA, KB, NST, CG>::STAGE_BYTES + kEpiWarps * Mega<KA, KB, NST, CG>::EPI_BYTES >=
          kSumWarps * kSumBytes;
 }
-static_assert(sum_staging_fits<kG1, kG2, 4, 1>() && sum_staging_fits<kDH, kDX, 3, 1>() &&
-                  sum_staging_fits<kG1, kG2, 6, 2>() && sum_staging_fits<kDH, kDX, 5, 2>(),
+static_assert(sum_staging_fits<kG1, kG2, 4, 1>() && sum_staging_fits<kDH, kDX, 4, 1>() &&
+                  sum_staging_fits<kG1, kG2, 6, 2>() && sum_staging_fits<kDH, kDX, 6, 2>(),
               "token-sum staging");
 
 // Bounded acquire-spin until *c >= target.
@@ -647,8 +647,8 @@ int megakernel_fwd(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const uint1
   a.W1 = W1;
   a.W3 = W3;
   a.W2 = W2;
-  a.H = reinterpret_cast<const uint16_t*>(ws + L.H);
-  a.H_out = reinterpret_cast<uint16_t*>(ws + L.H);
+  a.Hw = reinterpret_cast<const uint16_t*>(ws + L.Hw);
+  a.Hw_out = reinterpret_cast<uint16_t*>(ws + L.Hw);
   a.AB_out = reinterpret_cast<uint16_t*>(ws + L.AB);
   a.Op_out = reinterpret_cast<float*>(ws + L.Op);
   a.err = reinterpret_cast<int*>(ws + L.err);
@@ -663,9 +663,9 @@ int megakernel_bwd_input(const moe_cfg& c, const WsLayout& L, uint8_t* ws, const
                          float* dx, int grid, cudaStream_t s) {
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + L.G);
   const float* dXp = reinterpret_cast<const float*>(ws + L.dXp);
-  if (mega_uses_pairs<kDH, kDX, 5>(c.d_model))
-    return mega_launch<kDH, kDX, 5, 2>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
-  return mega_launch<kDH, kDX, 3, 1>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
+  if (mega_uses_pairs<kDH, kDX, 6>(c.d_model))
+    return mega_launch<kDH, kDX, 6, 2>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
+  return mega_launch<kDH, kDX, 4, 1>(c, L, ws, a, dy, G, dXp, dx, grid, MOE_K_MEGAKERNEL_BWD, s);
 }
 
 }  // namespace moe

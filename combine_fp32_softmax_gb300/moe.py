@@ -59,7 +59,7 @@ _SIGS = {
     "moe_combine": ([_CFG, _P, _P, _P, _P, _P], _I),
     "moe_layer_fwd": ([_CFG] + [_P] * 9 + [_I, _P], _I),
     "moe_combine_bwd": ([_CFG, _P, _P, _P, _P, _P], _I),
-    "moe_group_gemm_swiglu_bwd": ([_CFG] + [_P] * 20 + [_I, _P, _P], _I),
+    "moe_group_gemm_swiglu_bwd": ([_CFG] + [_P] * 19 + [_I, _P, _P], _I),
     "moe_dispatch_bwd": ([_CFG, _P, _P, _P, _P, _P], _I),
     "moe_route_bwd": ([_CFG, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_layer_bwd": ([_CFG] + [_P] * 14 + [_I, _P], _I),
@@ -172,9 +172,9 @@ def moe_rank_bases(all_counts, owner, rank, rank_base, recv_rows=None, stream=No
           _ptr(recv_rows), _stream(stream))
 
 
-def moe_group_gemm_swiglu(cfg, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, H, AB, Oprime, ws, stream=None):
+def moe_group_gemm_swiglu(cfg, Xp, x, offsets, row_slot, topk_w, W1, W3, W2, Hw, AB, Oprime, ws, stream=None):
     _call("moe_group_gemm_swiglu", _cfg(cfg), _ptr(Xp), _ptr(x), _ptr(offsets), _ptr(row_slot), _ptr(topk_w),
-          _ptr(W1), _ptr(W3), _ptr(W2), _ptr(H), _ptr(AB), _ptr(Oprime), _ptr(ws), _stream(stream))
+          _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Hw), _ptr(AB), _ptr(Oprime), _ptr(ws), _stream(stream))
 
 
 def moe_combine(cfg, Oprime, dest, y, ws, stream=None):
@@ -190,11 +190,11 @@ def moe_combine_bwd(cfg, dy, row_token, G, ws, stream=None):
     _call("moe_combine_bwd", _cfg(cfg), _ptr(dy), _ptr(row_token), _ptr(G), _ptr(ws), _stream(stream))
 
 
-def moe_group_gemm_swiglu_bwd(cfg, G, dy, Xp, x, offsets, row_slot, dest, topk_w, W1, W3, W2, H, AB,
-                              dAB, Hw, dw, dXp, dW1, dW3, dW2, which, ws, stream=None):
+def moe_group_gemm_swiglu_bwd(cfg, G, dy, Xp, x, offsets, row_slot, dest, topk_w, W1, W3, W2, Hw, AB,
+                              dAB, dw, dXp, dW1, dW3, dW2, which, ws, stream=None):
     _call("moe_group_gemm_swiglu_bwd", _cfg(cfg), _ptr(G), _ptr(dy), _ptr(Xp), _ptr(x), _ptr(offsets),
-          _ptr(row_slot), _ptr(dest), _ptr(topk_w), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(H), _ptr(AB),
-          _ptr(dAB), _ptr(Hw), _ptr(dw), _ptr(dXp), _ptr(dW1), _ptr(dW3), _ptr(dW2), int(which), _ptr(ws),
+          _ptr(row_slot), _ptr(dest), _ptr(topk_w), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(Hw), _ptr(AB),
+          _ptr(dAB), _ptr(dw), _ptr(dXp), _ptr(dW1), _ptr(dW3), _ptr(dW2), int(which), _ptr(ws),
           _stream(stream))
 
 
@@ -370,8 +370,8 @@ def ws_offsets(cfg: MoEConfig) -> dict:
 
     for name, nbytes in [("err", 256), ("hist", 4 * E * nb), ("base", 4 * E * nb), ("counts", 4 * E),
                          ("offsets", 4 * (E + 1)), ("dest", 4 * R), ("row_token", 4 * R),
-                         ("row_slot", 4 * R), ("Xp", 2 * R * d), ("AB", 4 * Rs * f), ("H", 2 * Rs * f),
-                         ("Op", 4 * Rs * d), ("G", 2 * R * d), ("dAB", 4 * Rs * f), ("Hw", 2 * Rs * f),
+                         ("row_slot", 4 * R), ("Xp", 2 * R * d), ("AB", 4 * Rs * f), ("Hw", 2 * Rs * f),
+                         ("Op", 4 * Rs * d), ("G", 2 * R * d), ("dAB", 4 * Rs * f),
                          ("dXp", 4 * Rs * d), ("partial", 4 * R * nt), ("dw", 4 * T * k)]:
         take(name, nbytes)
     out["_mk"] = o
@@ -384,9 +384,9 @@ def ws_view(ws: torch.Tensor, cfg: MoEConfig, name: str) -> torch.Tensor:
     R, Rs = T * k, T * k + S * T
     shapes = {"err": ((64,), torch.int32), "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32), "dest": ((R,), torch.int32),
               "row_token": ((R,), torch.int32), "row_slot": ((R,), torch.int32),
-              "Xp": ((R, d), torch.bfloat16), "AB": ((Rs, 2 * f), torch.bfloat16), "H": ((Rs, f), torch.bfloat16),
+              "Xp": ((R, d), torch.bfloat16), "AB": ((Rs, 2 * f), torch.bfloat16), "Hw": ((Rs, f), torch.bfloat16),
               "Op": ((Rs, d), torch.float32), "G": ((R, d), torch.bfloat16), "dAB": ((Rs, 2 * f), torch.bfloat16),
-              "Hw": ((Rs, f), torch.bfloat16), "dXp": ((Rs, d), torch.float32), "dw": ((T, k), torch.float32)}
+              "dXp": ((Rs, d), torch.float32), "dw": ((T, k), torch.float32)}
     shape, dt = shapes[name]
     off = ws_offsets(cfg)[name]
     n = 1

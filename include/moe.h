@@ -182,16 +182,18 @@ int moe_rank_bases(const int32_t* all_counts, int G, int E, const int32_t* owner
  * grouped GEMM with per-segment pointer arithmetic, section 2.2).
  * GEMM 1, per GEMM row r of segment e (A row = Xp[r], or x[t] for shared
  * rows):  a = A.W1_e^T, b = A.W3_e^T accumulated in fp32;
- *         H[r] = bf16(silu(a) * b), silu(a) = a / (1 + exp(-a)).
+ *         Hw[r] = bf16(w_r * (silu(a) * b)), silu(a) = a / (1 + exp(-a)),
+ *         rounded once from fp32, with w_r = topk_w[row_slot[r]] for routed
+ *         rows and 1 for shared rows (the gate score applied before the
+ *         down projection, which is linear).
  *         If AB is non-NULL, AB[r] = [bf16(a) | bf16(b)]  ([R_s, 2f]).
- * GEMM 2: O'[r] = fl32(w_r * (H[r].W2_e^T)) with w_r = topk_w[row_slot[r]]
- *         for routed rows and 1 for shared rows.  H [R_s, f] bf16,
- *         O' [R_s, d] fp32.  Experts with no rows are skipped.
+ * GEMM 2: O'[r] = fl32(Hw[r].W2_e^T).  Hw [R_s, f] bf16, O' [R_s, d] fp32.
+ *         Experts with no rows are skipped.
  * offsets/row_slot come from moe_dispatch. */
 int moe_group_gemm_swiglu(const moe_cfg* cfg, const uint16_t* Xp, const uint16_t* x,
                           const int32_t* offsets, const int32_t* row_slot,
                           const float* topk_w, const uint16_t* W1, const uint16_t* W3,
-                          const uint16_t* W2, uint16_t* H, uint16_t* AB, float* Oprime,
+                          const uint16_t* W2, uint16_t* Hw, uint16_t* AB, float* Oprime,
                           void* ws, void* stream);
 
 /* Combine (UniEP page, section 1.1: weighted sum by gate score; the
@@ -235,11 +237,12 @@ int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_t
 
 /* Expert FFN backward.  For GEMM row r (token t, weight w_r, expert e):
  *   dHraw = dy_t . W2_e            (fp32 accumulate, K = d)
- *   dH = w_r * dHraw;  s = sigmoid(a)
+ *   a, b = the bf16 values in AB[r];  s = sigmoid(a)
+ *   dH = w_r * dHraw
  *   dA = dH * b * s * (1 + a * (1 - s));  dB = dH * a * s
  *   dAB[r] = [bf16(dA) | bf16(dB)]          ([R_s, 2f])
- *   Hw[r]  = bf16(w_r * H[r])               ([R_s, f])
- *   dw[t, j] = <dHraw, H[r]> for routed rows (= <dy_t, unscaled o_r>),
+ *   dw[t, j] = <dHraw, a * s * b> for routed rows (= <dy_t, unscaled o_r>
+ *              with h formed again from the saved a and b),
  *              summed over fixed column tiles in tile order      ([T, k])
  *   dXp[r] = dA . W1_e + dB . W3_e          (fp32 [R_s, d], K = 2f)
  *   dW1_e = sum_r dA_r^T A_r, dW3_e = sum_r dB_r^T A_r   (fp32 [E+S, f, d])
@@ -247,16 +250,16 @@ int moe_combine_bwd(const moe_cfg* cfg, const uint16_t* dy, const int32_t* row_t
  * where A_r = Xp[r] (routed) or x[t] (shared); each weight-gradient sum
  * runs over the segment's rows in ascending order inside one CTA (no
  * split-K atomics), and experts with no rows get exact zeros.
- * which: 1 = input part (dAB, Hw, dw, dXp), 2 = weight part (dW1, dW3, dW2;
- * needs dAB and Hw from a previous which=1 call), 3 = both.
- * G from moe_combine_bwd; AB, H from moe_group_gemm_swiglu. */
+ * which: 1 = input part (dAB, dw, dXp), 2 = weight part (dW1, dW3, dW2;
+ * needs dAB from a previous which=1 call), 3 = both.
+ * G from moe_combine_bwd; AB, Hw from moe_group_gemm_swiglu. */
 int moe_group_gemm_swiglu_bwd(const moe_cfg* cfg, const uint16_t* G, const uint16_t* dy,
                               const uint16_t* Xp, const uint16_t* x,
                               const int32_t* offsets, const int32_t* row_slot,
                               const int32_t* dest, const float* topk_w,
                               const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
-                              const uint16_t* H, const uint16_t* AB,
-                              uint16_t* dAB, uint16_t* Hw, float* dw, float* dXp,
+                              const uint16_t* Hw, const uint16_t* AB,
+                              uint16_t* dAB, float* dw, float* dXp,
                               float* dW1, float* dW3, float* dW2, int which,
                               void* ws, void* stream);
 

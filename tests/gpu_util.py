@@ -13,7 +13,7 @@ Tolerances (float outputs against the fp64 oracle):
     weight gradient sits ~11x the rms error above it (rows with large
     activations carry both large values and large rounding errors), so an
     rms-scaled bar would reject correct bf16 arithmetic;
-  * stored bf16 activations (H, [a|b]): |got - ref| <= 2^-8 |ref| +
+  * stored bf16 activations (Hw = w*h, [a|b]): |got - ref| <= 2^-8 |ref| +
     1e-4 rms(ref) elementwise: one bf16 rounding of an fp32 value whose own
     error is far below a bf16 ulp;
   * routing weights: relative <= 4e-6 (fp32 softmax error bound);

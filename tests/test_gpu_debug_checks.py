@@ -61,11 +61,11 @@ def test_grouped_gemm_reports_a_segment_table_not_ending_at_R():
     g, out, ws = _layer()
     offsets = moe.ws_view(ws, CFG, "offsets").clone()
     offsets[CFG.E] = CFG.R - 1  # the last entry is not read by the kernels, only checked
-    H = torch.empty(CFG.Rs, CFG.f, dtype=torch.bfloat16, device=DEV)
+    Hw = torch.empty(CFG.Rs, CFG.f, dtype=torch.bfloat16, device=DEV)
     Op = torch.empty(CFG.Rs, CFG.d, dtype=torch.float32, device=DEV)
     w2 = _fresh_ws()
     moe.moe_group_gemm_swiglu(CFG, moe.ws_view(ws, CFG, "Xp"), g["x"], offsets, moe.ws_view(ws, CFG, "row_slot"),
-                              out["topk_w"], g["W1"], g["W3"], g["W2"], H, None, Op, w2)
+                              out["topk_w"], g["W1"], g["W3"], g["W2"], Hw, None, Op, w2)
     code, info = moe.moe_get_device_error(w2)
     assert code == moe.MOE_ERR_ARG and (info >> 24) == SITE["segments"], (code, hex(info))
     # the rows themselves are computed as without the check

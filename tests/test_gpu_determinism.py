@@ -25,7 +25,7 @@ from tests.gpu_util import check_guards, device_error, empty_outputs, guarded_wo
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-SAVED = ("Xp", "H", "AB", "Op", "G", "dAB", "Hw", "dXp", "dw")
+SAVED = ("Xp", "Hw", "AB", "Op", "G", "dAB", "dXp", "dw")
 
 
 def _snapshot(out, ws, cfg):

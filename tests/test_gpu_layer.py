@@ -161,7 +161,7 @@ def test_cta_pair_tiles_equal_single_cta_tiles_bitwise(cfg):
     assert device_error(wsa) == (0, 0) and device_error(wsb) == (0, 0)
     for k in a:
         assert torch.equal(a[k], b[k]), k
-    for name in ("H", "AB", "Op", "dAB", "Hw"):
+    for name in ("Hw", "AB", "Op", "dAB"):
         assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
 
 
@@ -367,7 +367,7 @@ def test_megakernel_bitwise_equals_kernel_chain(cfg):
     assert device_error(wsb) == (0, 0)
     for k in a:
         assert torch.equal(a[k], b[k]), k
-    for name in ("Xp", "H", "AB", "Op"):
+    for name in ("Xp", "Hw", "AB", "Op"):
         assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
 
 
@@ -491,7 +491,7 @@ def test_bwd_megakernel_bitwise_equals_kernel_chain(cfg):
     assert device_error(wsb) == (0, 0)
     for k in a:
         assert torch.equal(a[k], b[k]), k
-    for name in ("G", "dAB", "Hw", "dXp", "dw"):
+    for name in ("G", "dAB", "dXp", "dw"):
         assert torch.equal(moe.ws_view(wsa, cfg, name), moe.ws_view(wsb, cfg, name)), name
 
 
