@@ -188,11 +188,12 @@ extern "C" int moe_autotune(const moe_cfg* cfg, const float* logits, const uint1
     keep_if_faster(us, [&](int k) { chosen.epi[k] = c.epi[k]; });
   }
   cur = chosen;
-  // Phase 3: one pipeline stage fewer than fits.
+  // Phase 3: one pipeline stage fewer than fits (with each kind's epilogue
+  // stores; direct stores leave room for one stage more).
   {
     Settings c = cur;
     for (int k = 0; k < kKinds; ++k)
-      c.stages[k] = gemm_max_stages(static_cast<GemmKind>(k), ((c.mask >> k) & 1) ? 2 : 1) - 1;
+      c.stages[k] = gemm_max_stages(static_cast<GemmKind>(k), ((c.mask >> k) & 1) ? 2 : 1, c.epi[k]) - 1;
     apply_settings(c);
     double us[kKinds];
     const int rc = time_candidate(us);
@@ -246,7 +247,7 @@ extern "C" int moe_autotune(const moe_cfg* cfg, const float* logits, const uint1
     out->tile_order[k] = cur.order[k];
     out->epi_direct[k] = cur.epi[k];
     out->stages[k] = cur.stages[k] > 0 ? cur.stages[k]
-                                       : gemm_max_stages(static_cast<GemmKind>(k), out->pair[k] ? 2 : 1);
+                                       : gemm_max_stages(static_cast<GemmKind>(k), out->pair[k] ? 2 : 1, cur.epi[k]);
     out->us[k] = best[k] < 0 ? 0.f : static_cast<float>(best[k]);
   }
   moe_trace_reset();

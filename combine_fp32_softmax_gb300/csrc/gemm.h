@@ -78,8 +78,11 @@ int set_gemm_epilogue(GemmKind kind, int direct);
 // Pipeline stages kind `kind` uses (0 or out of range: as many as fit; at
 // least 2).  Returns the previous request, or -1 for an unknown kind.
 int set_gemm_stages(GemmKind kind, int stages);
-// Stages that fit for `kind` with `cta_group` CTAs per tile.
+// Stages that fit for `kind` with `cta_group` CTAs per tile, with its
+// current epilogue stores; the second form names the epilogue mode
+// (1 = direct: no staging memory, so an fp32-output kind fits more).
 int gemm_max_stages(GemmKind kind, int cta_group);
+int gemm_max_stages(GemmKind kind, int cta_group, int direct);
 
 // CTA pairs of `kind` that fit on the device at once (0 on error).
 int gemm_pair_capacity(GemmKind kind);

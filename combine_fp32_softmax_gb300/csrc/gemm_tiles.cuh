@@ -58,7 +58,7 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 7;
 // Tile numbers in flight from the ticket-taking producer to the other roles
 // (dynamic tile scheduling of the grouped GEMM kernels).
 constexpr int kTileRing = 8;
@@ -166,10 +166,33 @@ __device__ __forceinline__ int seg_rows(const GemmParams& p, const SharedState& 
   return (s + 1 < p.E ? ss.seg_row0[s + 1] : p.R) - ss.seg_row0[s];
 }
 
+// Shared memory one CTA can have (the sm_100 family's per-block opt-in).
+constexpr int kSmemBudget = 232448;
+
+// Shared memory of the stand-alone kernel: the ring, the epilogue staging
+// (none when the fp32 kinds store straight from registers) and the state.
 template <int KIND, int CG = 1>
-constexpr int smem_bytes() {
-  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES + Pipe<KIND, CG>::EPI_WARPS * Traits<KIND>::EPI_BYTES +
-         static_cast<int>(sizeof(SharedState));
+constexpr int smem_bytes(bool direct = false) {
+  return Pipe<KIND, CG>::STAGES * Pipe<KIND, CG>::STAGE_BYTES +
+         (direct ? 0 : Pipe<KIND, CG>::EPI_WARPS * Traits<KIND>::EPI_BYTES) + static_cast<int>(sizeof(SharedState));
+}
+// Pipeline stages with direct epilogue stores: the staging memory they do
+// not need takes more of the ring (CTA pairs: a seventh 32 KB stage).
+template <int KIND, int CG = 1>
+constexpr int direct_stages() {
+  constexpr bool fp32_out = KIND == kG2 || KIND == kDX || KIND == kDW13 || KIND == kDW2;
+  constexpr int fit = (kSmemBudget - static_cast<int>(sizeof(SharedState))) / Pipe<KIND, CG>::STAGE_BYTES;
+  return !fp32_out ? Pipe<KIND, CG>::STAGES : (fit < kMaxStages ? fit : kMaxStages);
+}
+template <int KIND, int CG = 1>
+constexpr int direct_smem_bytes() {
+  return direct_stages<KIND, CG>() * Pipe<KIND, CG>::STAGE_BYTES + static_cast<int>(sizeof(SharedState));
+}
+// The larger of the two modes' footprints (what a launch asks for).
+template <int KIND, int CG = 1>
+constexpr int launch_smem_bytes() {
+  return smem_bytes<KIND, CG>() > direct_smem_bytes<KIND, CG>() ? smem_bytes<KIND, CG>()
+                                                                 : direct_smem_bytes<KIND, CG>();
 }
 
 // One CTA's part of a tile.  m0 and rows are this CTA's: in a pair the odd

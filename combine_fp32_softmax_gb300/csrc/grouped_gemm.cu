@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(Pipe<KIND, CG>::THREADS, 1) grouped_gemm_kerne
   }
   uint8_t* smem = smem_raw;
   uint8_t* stg_base = smem + NST * SB;  // epilogue staging, Traits::EPI_BYTES per epilogue warp
-  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + EW * Traits<KIND>::EPI_BYTES);
+  // Direct epilogue stores need no staging: the state follows the ring.
+  SharedState& ss = *reinterpret_cast<SharedState*>(stg_base + (p.epi_direct ? 0 : EW * Traits<KIND>::EPI_BYTES));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
 
@@ -381,7 +382,7 @@ template <int KIND, int CG>
 void launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t s) {
   cfg = {};
   cfg.blockDim = dim3(Pipe<KIND, CG>::THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<KIND, CG>();
+  cfg.dynamicSmemBytes = launch_smem_bytes<KIND, CG>();
   cfg.stream = s;
   if constexpr (CG == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -399,7 +400,7 @@ int pair_capacity() {
   static int cached = 0;
   if (cached == 0) {
     auto kern = grouped_gemm_kernel<KIND, 2>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<KIND, 2>()) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, launch_smem_bytes<KIND, 2>()) !=
         cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg;
@@ -422,10 +423,11 @@ int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
   p.epi_direct = g_epi_direct[KIND];
   // Fewer stages leave part of the ring unused; the launch still takes the
   // whole shared-memory budget, so one CTA per SM stays resident.
-  constexpr int kMaxSt = Pipe<KIND, CG>::STAGES;
-  p.nst = (g_stages[KIND] >= 2 && g_stages[KIND] < kMaxSt) ? g_stages[KIND] : kMaxSt;
-  constexpr int kSmem = smem_bytes<KIND, CG>();
-  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
+  const int max_st = p.epi_direct ? direct_stages<KIND, CG>() : Pipe<KIND, CG>::STAGES;
+  p.nst = (g_stages[KIND] >= 2 && g_stages[KIND] < max_st) ? g_stages[KIND] : max_st;
+  constexpr int kSmem = launch_smem_bytes<KIND, CG>();
+  static_assert(kSmem <= kSmemBudget, "shared memory budget of one CTA");
+  static_assert(direct_stages<KIND, CG>() <= kMaxStages, "stage barriers");
   auto kern = grouped_gemm_kernel<KIND, CG>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -553,16 +555,26 @@ int set_gemm_stages(GemmKind kind, int stages) {
   return prev;
 }
 
-int gemm_max_stages(GemmKind kind, int cta_group) {
+template <int KIND>
+int max_stages_of(int cta_group, bool direct) {
+  if (cta_group == 2) return direct ? direct_stages<KIND, 2>() : Pipe<KIND, 2>::STAGES;
+  return direct ? direct_stages<KIND, 1>() : Pipe<KIND, 1>::STAGES;
+}
+
+int gemm_max_stages(GemmKind kind, int cta_group, int direct) {
   switch (kind) {
-    case kG1: return cta_group == 2 ? Pipe<kG1, 2>::STAGES : Pipe<kG1, 1>::STAGES;
-    case kG2: return cta_group == 2 ? Pipe<kG2, 2>::STAGES : Pipe<kG2, 1>::STAGES;
-    case kDH: return cta_group == 2 ? Pipe<kDH, 2>::STAGES : Pipe<kDH, 1>::STAGES;
-    case kDX: return cta_group == 2 ? Pipe<kDX, 2>::STAGES : Pipe<kDX, 1>::STAGES;
-    case kDW13: return cta_group == 2 ? Pipe<kDW13, 2>::STAGES : Pipe<kDW13, 1>::STAGES;
-    case kDW2: return cta_group == 2 ? Pipe<kDW2, 2>::STAGES : Pipe<kDW2, 1>::STAGES;
+    case kG1: return max_stages_of<kG1>(cta_group, false);
+    case kG2: return max_stages_of<kG2>(cta_group, direct != 0);
+    case kDH: return max_stages_of<kDH>(cta_group, false);
+    case kDX: return max_stages_of<kDX>(cta_group, direct != 0);
+    case kDW13: return max_stages_of<kDW13>(cta_group, direct != 0);
+    case kDW2: return max_stages_of<kDW2>(cta_group, direct != 0);
   }
   return 0;
+}
+
+int gemm_max_stages(GemmKind kind, int cta_group) {
+  return kind >= kG1 && kind <= kDW2 ? gemm_max_stages(kind, cta_group, g_epi_direct[kind]) : 0;
 }
 
 int gemm_pair_kinds() { return g_pair_kinds; }

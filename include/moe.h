@@ -390,7 +390,9 @@ int moe_set_gemm_tile_order(int kind, int order);
  * through shared memory and a TMA tensor store writes them.  direct 1: the
  * accumulator is read in a 16-lane shape and written straight from
  * registers, 64 contiguous bytes per row and store, sparing the shared
- * memory traffic of the staging.  Same values either way.  Returns the
+ * memory traffic of the staging; the staging memory then holds one more
+ * pipeline stage on CTA pairs (see moe_gemm_max_stages).  Same values
+ * either way.  Returns the
  * previous mode, or MOE_ERR_ARG for another kind or mode.  Process-wide,
  * not thread-safe. */
 int moe_set_gemm_epilogue(int kind, int direct);
@@ -400,8 +402,10 @@ int moe_set_gemm_epilogue(int kind, int direct);
  * 2 and at most moe_gemm_max_stages().  A performance knob only.  Returns
  * the previous request, or MOE_ERR_ARG.  Process-wide, not thread-safe. */
 int moe_set_gemm_stages(int kind, int stages);
-/* Stages that fit for `kind` with cta_group (1 or 2) CTAs per tile; 0 for
- * an unknown kind or group. */
+/* Stages that fit for `kind` with cta_group (1 or 2) CTAs per tile and the
+ * kind's current epilogue stores (moe_set_gemm_epilogue: 6 on pairs, 7 for
+ * an fp32-output kind with direct stores; 4 on single CTAs); 0 for an
+ * unknown kind or group. */
 int moe_gemm_max_stages(int kind, int cta_group);
 
 /* ------------------------------------------------------------ autotuner

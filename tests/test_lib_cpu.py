@@ -97,9 +97,16 @@ def test_gemm_knobs_reject_bad_kinds_and_values(lib):
 
 def test_gemm_knobs_round_trip_and_stage_limits(lib):
     """Each setter returns the previous value; the stage limits are those of
-    the shared-memory ring (one CTA per tile: 48 KB stages, CTA pairs: 32 KB)."""
+    the shared-memory ring (one CTA per tile: 48 KB stages, CTA pairs: 32 KB).
+    Direct epilogue stores free the staging memory for a seventh stage on
+    pairs; a 48 KB stage does not fit in it."""
     assert [lib.moe_gemm_max_stages(k, 1) for k in range(6)] == [4] * 6
     assert [lib.moe_gemm_max_stages(k, 2) for k in range(6)] == [6] * 6
+    for kind in (1, 3, 4, 5):
+        prev = lib.moe_set_gemm_epilogue(kind, 1)
+        assert lib.moe_gemm_max_stages(kind, 2) == 7 and lib.moe_gemm_max_stages(kind, 1) == 4
+        lib.moe_set_gemm_epilogue(kind, prev)
+        assert lib.moe_gemm_max_stages(kind, 2) == 6
     for kind in (4, 5):
         prev = lib.moe_set_gemm_tile_order(kind, 1)
         assert lib.moe_set_gemm_tile_order(kind, prev) == 1
