@@ -374,6 +374,18 @@ __device__ __forceinline__ int k_steps(const TileInfo& t, int kb) {
     return kBK / 16;
 }
 
+// The last column tile of dH and dW2 when it holds at most 128 of the f
+// columns (f = 1408 leaves 128 of 256): its MMAs are N = 128 and its B boxes
+// half as wide, instead of spending half of each 256-wide MMA on zeros.  A
+// pair then splits B 64 + 64 columns.
+template <int KIND>
+__device__ __forceinline__ bool narrow_tile(const GemmParams& p, const TileInfo& t) {
+  if constexpr (KIND == kDH || KIND == kDW2)
+    return p.N - t.n0 <= kBN / 2;
+  else
+    return false;
+}
+
 // One stage of TMA loads: A (this CTA's 128 rows) and this CTA's part of B
 // (all 256 columns for CG = 1; columns [128 rank, 128 rank + 128) for
 // CG = 2).  Boxes that fall outside a tensor are zero-filled.  `to_even`:
@@ -402,7 +414,9 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
       moe::tma_load_3d(dst, map, b, 0, row, col / 64);
   };
   const int kk = kb * kBK;
-  const int bn0 = t.n0 + 128 * rank;  // first B column this CTA stages
+  const bool narrow = narrow_tile<KIND>(p, t);
+  const int bn0 = t.n0 + (narrow ? 64 : 128) * rank;  // first B column this CTA stages
+  const CUtensorMap* mapB = narrow ? &p.tmB1 : &p.tmB0;  // dH, dW2: tmB1 holds half the 64-column chunks
   if constexpr (KIND == kG1) {
     // accumulator columns [0,128) = gate rows of W1, [128,256) = up rows of W3
     tma_load_2d(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, kk, t.shared ? t.m0 : t.grow0);
@@ -413,7 +427,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     tma_load_2d(sB, &p.tmB0, bar, kk, t.seg * p.d + bn0);
   } else if constexpr (KIND == kDH) {
     tma_load_2d(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, kk, t.shared ? t.m0 : t.grow0);
-    tma_load_mn(sB, &p.tmB0, bar, bn0, t.seg * p.d + kk);
+    tma_load_mn(sB, mapB, bar, bn0, t.seg * p.d + kk);
   } else if constexpr (KIND == kDX) {
     tma_load_2d(sA, &p.tmA0, bar, kk, t.grow0);
     const bool second = kk >= p.f;
@@ -424,7 +438,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     tma_load_mn(sB, t.shared ? &p.tmB1 : &p.tmB0, bar, bn0, t.shared ? kk : t.grow0 + kk);
   } else {  // kDW2
     tma_load_mn(sA, t.shared ? &p.tmA1 : &p.tmA0, bar, t.m0, t.shared ? kk : t.grow0 + kk);
-    tma_load_mn(sB, &p.tmB0, bar, bn0, t.grow0 + kk);
+    tma_load_mn(sB, mapB, bar, bn0, t.grow0 + kk);
   }
 }
 
@@ -923,12 +937,14 @@ template <int KIND, int CG = 1>
 __device__ __forceinline__ bool produce_tile(const GemmParams& p, const TileInfo& t, SharedState& ss, uint8_t* smem,
                                              ProducerState& ps, volatile int* abort, int where, int NST, int rank = 0) {
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
+  // bytes one CTA's loads of a stage bring (half of B on a narrow tile)
+  const int sb = narrow_tile<KIND>(p, t) ? SB - Pipe<KIND, CG>::B_BYTES / 2 : SB;
   for (int kb = 0; kb < t.nkb; ++kb) {
     if (!mbar_wait(&ss.empty[ps.stage], ps.phase ^ 1, abort, p.err, where)) return false;
     uint8_t* sA = smem + ps.stage * SB;
     const uint32_t bit = 1u << ps.stage;
     const bool tail = CG == 2 && is_k_tail<KIND>(t, kb);
-    if (CG == 1 || rank == 0 || tail) mbar_arrive_expect_tx(&ss.full[ps.stage], CG == 2 && !tail ? 2 * SB : SB);
+    if (CG == 1 || rank == 0 || tail) mbar_arrive_expect_tx(&ss.full[ps.stage], CG == 2 && !tail ? 2 * sb : sb);
     issue_loads<KIND, CG>(p, t, kb, sA, sA + kABytes, &ss.full[ps.stage], rank, CG == 2 && rank == 1 && !tail);
     if (CG == 1 || rank == 0) {
       ps.filled |= bit;
@@ -1005,7 +1021,9 @@ __device__ __forceinline__ bool mma_tile(const GemmParams& p, const TileInfo& t,
                                          int rank = 0) {
   using Tr = Traits<KIND>;
   constexpr int SB = Pipe<KIND, CG>::STAGE_BYTES;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM * CG, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
+  constexpr uint32_t kIdescFull = idesc_bf16_f32(kBM * CG, kBN, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
+  constexpr uint32_t kIdescNarrow = idesc_bf16_f32(kBM * CG, kBN / 2, Tr::A_MN ? 1 : 0, Tr::B_MN ? 1 : 0);
+  const uint32_t kIdesc = narrow_tile<KIND>(p, t) ? kIdescNarrow : kIdescFull;
   const int lane = threadIdx.x & 31;
   if (CG == 2 && rank == 1) {
     // The odd CTA's MMA warp only zeroes its part of ragged-K tails, but it
@@ -1264,6 +1282,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map2d(&p.tmA0, a.G, d, R, 64, 128);
     ok &= map2d(&p.tmA1, a.dy, d, T, 64, 128);
     ok &= map3d_mn(&p.tmB0, a.W2, f, nexp * d, 4 / CG);
+    ok &= map3d_mn(&p.tmB1, a.W2, f, nexp * d, 2 / CG);  // narrow last column tile
     ok &= map_chunk_bf16(&p.tmO0, a.dAB_out, 2 * f, Rs);
     ok &= map_chunk_bf16(&p.tmX0, a.AB, 2 * f, Rs);
     p.N = a.f;
@@ -1292,6 +1311,7 @@ bool fill_params(const GemmArgs& a, GemmParams& p) {
     ok &= map3d_mn(&p.tmA0, a.G, d, R, 2);
     ok &= map3d_mn(&p.tmA1, a.dy, d, T, 2);
     ok &= map3d_mn(&p.tmB0, a.Hw, f, Rs, 4 / CG);
+    ok &= map3d_mn(&p.tmB1, a.Hw, f, Rs, 2 / CG);  // narrow last column tile
     ok &= map_chunk_f32(&p.tmO0, a.dW2_out, f, nexp * d);
     p.Mw = a.d;
     p.N = a.f;
