@@ -84,10 +84,10 @@ __device__ __forceinline__ void trace_record(const MegaParams& mp, int role, int
 }
 
 // Shapes of one MegaKernel: its two GEMM kinds, its pipeline depth and its
-// CTA group.  One CTA per tile: forward 4 stages of 48 KB, backward 3 (a
-// fourth does not fit beside dH's 12 KB a warp of epilogue staging).  CTA
-// pairs (256-row tiles, tcgen05 CTA group of two, as the stand-alone grouped
-// GEMMs run by default): 32 KB stages, forward 6, backward 5.
+// CTA group.  One CTA per tile: 4 stages of 48 KB.  CTA pairs (256-row
+// tiles, tcgen05 CTA group of two, as the stand-alone grouped GEMMs run by
+// default): 6 stages of 32 KB.  Both fit beside the larger of the two
+// kinds' epilogue staging (GEMM 1: 6 KB a warp, dH: 8 KB).
 template <int KA, int KB, int NST, int CG = 1>
 struct Mega {
   static constexpr int STAGES = NST;

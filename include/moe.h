@@ -74,7 +74,7 @@ enum {
 };
 
 /* Bytes of workspace for `cfg`.  The workspace holds the routing tables,
- * the activations the backward needs (Xp, [a|b], H, O'), the backward's
+ * the activations the backward needs (Xp, [a|b], Hw, O'), the backward's
  * intermediates, scratch counters and the device error word.  The caller
  * allocates it once; moe_layer_fwd fills it and moe_layer_bwd reads it, so
  * it must stay alive and unmodified between the two.  Calls that share a
