@@ -1,6 +1,8 @@
 // Shared definitions of the CUDA library: error recording, workspace layout,
 // tile constants.
 #pragma once
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -86,6 +88,28 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Launch attribute of programmatic dependent launch: the kernel may be
+// scheduled while the previous kernel on the stream still runs (it calls
+// griddep_wait() before touching global data).
+inline void set_pdl_attr(cudaLaunchAttribute& a) {
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  set_pdl_attr(attr[0]);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Offsets of the regions inside the caller's workspace (bytes from ws).

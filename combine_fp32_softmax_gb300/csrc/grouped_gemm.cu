@@ -95,6 +95,11 @@ __global__ void __launch_bounds__(Pipe<KIND, CG>::THREADS, 1) grouped_gemm_kerne
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anything arrives on them
   tc_fence_after();
+  // The set-up above overlaps the previous kernel's last wave: it reads only
+  // the routing tables, which are complete before the previous kernel may
+  // have let this one start.  Everything below may read that kernel's output.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = ss.tmem_base;
   const int total = ss.total_tiles;
   volatile int* abort = &ss.abort;
@@ -433,8 +438,11 @@ int launch_kind(const GemmArgs& a, cudaStream_t s, int grid_override) {
     return MOE_ERR_CUDA;
   int grid = grid_override > 0 ? grid_override : num_sms();
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   launch_config<KIND, CG>(cfg, attr, s);
+  set_pdl_attr(attr[cfg.numAttrs]);
+  cfg.attrs = attr;
+  ++cfg.numAttrs;
   if constexpr (CG == 2) {
     // Persistent: only as many pairs as can be resident at once (an SM
     // left without a partner stays idle rather than adding a second wave).

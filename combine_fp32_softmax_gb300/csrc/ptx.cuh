@@ -139,6 +139,20 @@ __device__ __forceinline__ void st_shared_rank(int* p, uint32_t rank, int v) {
       : "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before
+// the previous kernel on its stream has finished.  griddep_wait() returns once
+// that kernel has completed and its memory operations are visible (at once
+// when there is none); griddep_launch_dependents() lets the next such kernel
+// be scheduled.  Every kernel of the layer step calls them in that order,
+// after its set-up and before anything that reads or writes global data, so
+// a kernel that starts early still finds every kernel before its
+// predecessor complete.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -467,6 +467,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32, EPL <= 4 ? 2 : 1)
                         int32_t* __restrict__ dest, int32_t* __restrict__ row_token,
                         int32_t* __restrict__ row_slot, int* err) {
   __shared__ RouteTablesSmem sm;
+  griddep_launch_dependents();
   int* bar = err + kErrBarrierWord;
   for (int hb = blockIdx.x; hb < nb; hb += gridDim.x) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) sm.hist[e] = 0;
@@ -615,6 +616,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     scatter_rows_bf16_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ dest, int T, int k,
                              int ndst, int nvec, uint4* __restrict__ dst, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int kSpan = 32 * kGatherVec;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
@@ -655,6 +658,8 @@ template <int NR>
 __global__ void __launch_bounds__(256)
     sum_rows_f32_kernel(const float4* __restrict__ rows, const int32_t* __restrict__ sel, int T, int k, int S,
                         int nvec, float4* __restrict__ out, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const long long R = static_cast<long long>(T) * k;
@@ -706,6 +711,8 @@ __global__ void __launch_bounds__(256)
 // dw[i] = sum over column tiles n (in order) of partial[dest[i] * nt + n].
 __global__ void dw_reduce_kernel(const float* __restrict__ partial, const int32_t* __restrict__ dest, int R, int nt,
                                  float* __restrict__ dw, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= R) return;
   if (!debug_ok(static_cast<unsigned>(dest[i]) < static_cast<unsigned>(R), err, kDbgDwReduce, i)) return;
@@ -722,6 +729,8 @@ __global__ void __launch_bounds__(256)
     route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                      const float* __restrict__ topk_w, const float* __restrict__ dw, int T, int E, int k, int renorm,
                      float* __restrict__ dlogits, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -916,9 +925,8 @@ cudaError_t launch_scatter_rows_bf16(const uint16_t* src, const int32_t* dest, i
     resident = per_sm * num_sms();
   }
   const int blocks = static_cast<int>(std::min<long long>(ceil_div(units, 8), resident));
-  scatter_rows_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), dest, T, k, T * k, d / 8,
-                                                  reinterpret_cast<uint4*>(dst), err);
-  return cudaGetLastError();
+  return launch_pdl(scatter_rows_bf16_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const uint4*>(src),
+                    dest, T, k, T * k, d / 8, reinterpret_cast<uint4*>(dst), err);
 }
 
 cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, int k, int S, int d, float* out,
@@ -940,10 +948,12 @@ cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, in
     }
     return static_cast<int>(std::min<long long>(ceil_div(units, 8), resident[nr]));
   };
+  cudaError_t e = cudaSuccess;
   switch (k + S) {
 #define MOE_SUM_ROWS_CASE(N) \
   case N:                                                                                           \
-    sum_rows_f32_kernel<N><<<grid_for(sum_rows_f32_kernel<N>, N), 256, 0, s>>>(r4, sel, T, k, S, d / 4, o4, err); \
+    e = launch_pdl(sum_rows_f32_kernel<N>, dim3(grid_for(sum_rows_f32_kernel<N>, N)), dim3(256), 0, s, r4, sel, T, k, \
+                   S, d / 4, o4, err);                                                                                \
     break;
     MOE_SUM_ROWS_CASE(1)
     MOE_SUM_ROWS_CASE(2)
@@ -961,29 +971,33 @@ cudaError_t launch_sum_rows_f32(const float* rows, const int32_t* sel, int T, in
     static_assert(12 == kMaxRowsPerToken, "one instantiation per row count");
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_dw_reduce(const float* partial, const int32_t* dest, int R, int nt, float* dw, int* err,
                              cudaStream_t s) {
   TraceScope trace_scope(MOE_K_DW_REDUCE, s);
-  dw_reduce_kernel<<<ceil_div(R, 256), 256, 0, s>>>(partial, dest, R, nt, dw, err);
-  return cudaGetLastError();
+  return launch_pdl(dw_reduce_kernel, dim3(ceil_div(R, 256)), dim3(256), 0, s, partial, dest, R, nt, dw, err);
 }
 
 cudaError_t launch_route_bwd(const float* logits, const int32_t* topk_idx, const float* topk_w, const float* dw,
                              int T, int E, int k, int renorm, float* dlogits, int* err, cudaStream_t s) {
   TraceScope trace_scope(MOE_K_ROUTE_BWD, s);
   const int blocks = min(ceil_div(T, 8), num_sms() * 8);
+  cudaError_t e;
   if (E <= 32)
-    route_bwd_kernel<1><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
+    e = launch_pdl(route_bwd_kernel<1>, dim3(blocks), dim3(256), 0, s, logits, topk_idx, topk_w, dw, T, E, k,
+                   renorm, dlogits, err);
   else if (E <= 64)
-    route_bwd_kernel<2><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
+    e = launch_pdl(route_bwd_kernel<2>, dim3(blocks), dim3(256), 0, s, logits, topk_idx, topk_w, dw, T, E, k,
+                   renorm, dlogits, err);
   else if (E <= 128)
-    route_bwd_kernel<4><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
+    e = launch_pdl(route_bwd_kernel<4>, dim3(blocks), dim3(256), 0, s, logits, topk_idx, topk_w, dw, T, E, k,
+                   renorm, dlogits, err);
   else
-    route_bwd_kernel<8><<<blocks, 256, 0, s>>>(logits, topk_idx, topk_w, dw, T, E, k, renorm, dlogits, err);
-  return cudaGetLastError();
+    e = launch_pdl(route_bwd_kernel<8>, dim3(blocks), dim3(256), 0, s, logits, topk_idx, topk_w, dw, T, E, k,
+                   renorm, dlogits, err);
+  return e;
 }
 
 // Loads the modules of the kernels moe_dispatch runs (histogram, scan,
